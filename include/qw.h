@@ -1,0 +1,233 @@
+/*
+ * qw.h - C ABI of the GB300 (sm_103a) Qwen3 forward hot path.
+ *
+ * One shared library, libqw.so, exposes the steps of a nano-vllm-style
+ * Qwen3 forward pass: the vocab-sharded embedding, fused residual add +
+ * RMSNorm, the linear layers (merged QKV and gate_up column splits, o_proj
+ * and down_proj row splits), per-head QK-RMSNorm + RoPE + KV-cache store,
+ * causal GQA attention for prefill and decode, SiluAndMul and the
+ * vocab-sharded lm_head with greedy argmax.
+ *
+ * Sources, cited by page and section:
+ *   [VH]  devpress page "vocab 切 / head 切" (nano-vllm tensor parallelism):
+ *         §3 VocabParallelEmbedding, §4 ParallelLMHead, §5 head split and
+ *         KV cache, §6 sharded == single-card check.
+ *   [TP]  devpress page on tensor-parallel maths: §3 column vs row split,
+ *         §4 the two column->row pairs, §5 embedding/LM head, §6 RMSNorm.
+ *   [VPE] "从零实现 vLLM (1.1): 并行词嵌入 VocabParallelEmbedding".
+ *   [SK]  "3.3 模型骨架与核心算子" (AIInfraGuide): §1 decoder layer,
+ *         §2 RMSNorm, §3 RoPE, §4 SiluAndMul, §5 parallel Linear family,
+ *         §6 vocab-parallel Embedding/LMHead, §7 attention, §8 assembly.
+ *
+ * Tensor parallelism is a weight LAYOUT on one device: `tp` shards are
+ * slices of the same buffer; shard partial sums are reduced and logit
+ * slices concatenated inside the kernels, with no collective.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless the parameter says "host".  The
+ *     caller allocates and owns every buffer; the library keeps no pointer
+ *     after the call returns.
+ *   - Every tensor is dense row-major with the shape given; `dtype` is
+ *     QW_BF16 or QW_F32 and applies to all floating-point tensors of the
+ *     call except those documented as float (fp32) always.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronise.  Arguments are checked on the
+ *     host before any launch; a failed check launches nothing.
+ *   - The return value is a qw_status.  qw_last_error_string() describes the
+ *     last failure on the calling thread.
+ *   - A size of zero tokens is a valid no-op and returns QW_OK.
+ *   - Device-side data errors (token id outside [0, V), position outside the
+ *     RoPE table, slot outside the cache) do not fail the call: the affected
+ *     row is zero (embedding, q) or not written (cache), and, when the
+ *     caller passes a non-NULL `err_count` (device int32), it is incremented
+ *     once per affected token.
+ */
+#ifndef QW_H
+#define QW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QW_OK = 0,
+  QW_ERR_INVALID_ARG = 1, /* null or misaligned pointer, negative size, bad enum */
+  QW_ERR_SHAPE = 2,       /* a divisibility or size rule below is broken */
+  QW_ERR_DTYPE = 3,       /* dtype not supported by this entry point */
+  QW_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  QW_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (see qw_device_error) */
+  QW_ERR_WORKSPACE = 6    /* workspace pointer missing or too small */
+} qw_status;
+
+typedef enum { QW_BF16 = 0, QW_F32 = 1 } qw_dtype;
+
+typedef enum {
+  QW_GEMM_COLUMN = 0,     /* W cut along the output dim ([TP] §3, tp_dim = 0) */
+  QW_GEMM_ROW_REDUCE = 1  /* W cut along the input dim, shard partials summed ([TP] §3, tp_dim = 1) */
+} qw_gemm_mode;
+
+typedef enum {
+  QW_EPI_NONE = 0,
+  QW_EPI_SILU_MUL = 1     /* fused SiluAndMul on a merged gate_up output ([SK] §4) */
+} qw_epilogue;
+
+/* Version of this ABI (increments on any signature change). */
+int qw_abi_version(void);
+
+/* Description of the last failure on the calling thread ("" if none). */
+const char* qw_last_error_string(void);
+
+/*
+ * Synchronises `stream`, then reports and clears the device-side error word
+ * that bounded waits inside the tensor-core kernels set when they give up
+ * (a wait that should never time out; it exists so that a broken pipeline
+ * returns instead of hanging the GPU).  Returns QW_OK or QW_ERR_TIMEOUT.
+ */
+int qw_device_error(void* stream);
+
+/*
+ * Vocab-parallel embedding ([VH] §3, [VPE], [SK] §6).
+ * For each token t and each shard r of `tp` (rows [r*V/tp, (r+1)*V/tp) of
+ * the table): mask = id in the shard's range; local = mask * (id - start);
+ * row = mask ? W_r[local] : 0; out[t] = sum over shards (the all_reduce).
+ *   ids      int64 [T]
+ *   table    dtype [V, H]   (shard r = row block r; the layout of tp stacked shards)
+ *   out      dtype [T, H]
+ *   err_count int32 [1] or NULL: +1 per id outside [0, V) (its row is zero)
+ * Rules: V % tp == 0 (else QW_ERR_SHAPE); H * sizeof(dtype) % 16 == 0 and
+ * table/out 16-byte aligned (else QW_ERR_INVALID_ARG).
+ */
+int qw_embed_vocab(const int64_t* ids, int64_t T, const void* table, int64_t V, int64_t H, int tp,
+                   void* out, int32_t* err_count, int dtype, void* stream);
+
+/*
+ * Fused residual add + RMSNorm ([SK] §2 rms_forward / add_rms_forward, §1).
+ * residual_in == NULL (first layer): s = x.  Otherwise s = round(x + residual_in).
+ * residual_out (may alias residual_in, may be NULL) <- s;
+ * y = round(s * rsqrt(mean(s^2) + eps) * gamma), computed in fp32.
+ *   x, residual_in, residual_out, y : dtype [T, H];  gamma : dtype [H]
+ * Rules: H * sizeof(dtype) % 16 == 0, H <= 4096 (bf16) or 2048 (f32),
+ * 16-byte aligned pointers.  y must not alias x or residual_in.
+ */
+int qw_add_rmsnorm(const void* x, const void* residual_in, void* residual_out, const void* gamma,
+                   float eps, int64_t T, int64_t H, void* y, int dtype, void* stream);
+
+/*
+ * RoPE cos/sin table on the HOST ([SK] §3): host_out float [max_position, rotary_dim]
+ * with row p = [cos(p*f_0) .. cos(p*f_{d/2-1}), sin(p*f_0) .. sin(p*f_{d/2-1})],
+ * f_i = fp32(1 / theta^(2i/d)), each angle the fp32 product p*f_i, cos/sin
+ * rounded to fp32.  rotary_dim must be even and > 0.  Runs on the host only.
+ */
+int qw_rope_cos_sin_table(float* host_out, int64_t max_position, int rotary_dim, double theta);
+
+/*
+ * Per-head QK-RMSNorm, RoPE on q and k, KV-cache store ([SK] §8 ①, §3, §7.1).
+ *   qkv       dtype [T, tp * (nh/tp + 2*nkv/tp) * hd]: the merged QKV output,
+ *             shard r's block = [q_r | k_r | v_r] ([SK] §5 QKVParallelLinear)
+ *   positions int64 [T];  cos_sin float [max_position, hd] (qw_rope_cos_sin_table)
+ *   q_gamma, k_gamma dtype [hd]
+ *   slot_mapping int64 [T]: cache row of each token, -1 = do not store
+ *   k_cache, v_cache dtype [num_slots, nkv, hd] (kv head g = shard g/(nkv/tp))
+ *   q_out     dtype [T, nh, hd]
+ * Per q head: q = round(rmsnorm(q) * q_gamma); q_out = round(rope(q)).
+ * Per kv head: k likewise with k_gamma, stored with the raw v to the cache.
+ * Rules: nh % tp == 0, nkv % tp == 0, hd even and <= 256.
+ */
+int qw_qkv_norm_rope_store_kv(const void* qkv, int64_t T, int n_heads, int n_kv_heads, int head_dim,
+                              int tp, const int64_t* positions, const float* cos_sin,
+                              int64_t max_position, const void* q_gamma, const void* k_gamma, float eps,
+                              const int64_t* slot_mapping, void* k_cache, void* v_cache, int64_t num_slots,
+                              void* q_out, int32_t* err_count, int dtype, void* stream);
+
+/*
+ * Causal varlen GQA attention for prefill (flash_attn_varlen_func with
+ * causal=True, [SK] §7.2).
+ *   q   dtype [Tq, nh, hd], sequences packed by cu_seqlens_q (int32 [n_seqs+1])
+ *   k,v dtype [rows, nkv, hd]: key j of sequence s is row seq_base[s] + j when
+ *       seq_base (int32 [n_seqs]) is given (keys read from the KV cache),
+ *       else row cu_seqlens_k[s] + j (packed keys).
+ *   cu_seqlens_k int32 [n_seqs+1]: Lk_s = cu_seqlens_k[s+1] - cu_seqlens_k[s] >= Lq_s;
+ *       query i of sequence s sits at key position Lk_s - Lq_s + i and sees
+ *       keys 0 .. that position.
+ *   out dtype [Tq, nh, hd];  q head h reads kv head h / (nh / nkv).
+ *   max_seqlen_q: upper bound of Lq_s (sizes the grid).
+ * Rules: nh % nkv == 0; hd == 128 for bf16, hd <= 64 for f32.
+ */
+int qw_attention_prefill(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                         const int32_t* cu_seqlens_k, const int32_t* seq_base, int n_seqs,
+                         int max_seqlen_q, int n_heads, int n_kv_heads, int head_dim, float scale,
+                         void* out, int dtype, void* stream);
+
+/*
+ * Decode attention over the KV cache (flash_attn_with_kvcache, [SK] §7.2):
+ * one new query token per sequence, sees cache rows
+ * seq_base[b] .. seq_base[b] + context_lens[b] - 1 (the token just stored included).
+ *   q   dtype [B, nh, hd];  k_cache, v_cache dtype [num_slots, nkv, hd]
+ *   context_lens, seq_base int32 [B];  max_context >= every context_lens[b]
+ *   out dtype [B, nh, hd]
+ *   workspace: device scratch of qw_attention_decode_workspace_size(...) bytes
+ *   (split-KV partial results); may be NULL only when that size is 0.
+ * Rules: nh % nkv == 0, nh/nkv <= 8, hd == 128 (bf16 or f32).
+ */
+int qw_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* context_lens, const int32_t* seq_base, int B, int max_context,
+                        int n_heads, int n_kv_heads, int head_dim, float scale, void* out,
+                        void* workspace, size_t workspace_bytes, int dtype, void* stream);
+size_t qw_attention_decode_workspace_size(int B, int max_context, int n_heads, int head_dim);
+
+/*
+ * Linear layer C = A W^T with the tensor-parallel layouts of [TP] §3 / [SK] §5.
+ *   A dtype [M, K]
+ *   QW_GEMM_COLUMN:     W dtype [N, K] (tp shards stacked along N; shard r = rows
+ *                       [r*N/tp, (r+1)*N/tp)); C[M, N] = A W^T.
+ *     with QW_EPI_SILU_MUL: N = 2*I and shard r's rows are [gate_r (I/tp) ; up_r (I/tp)]
+ *                       ([SK] §5 MergedColumnParallelLinear); C is [M, I] with
+ *                       C[:, r*I/tp + j] = silu(G[:, j]) * U[:, j] of shard r.
+ *   QW_GEMM_ROW_REDUCE: W dtype [tp, N, K/tp] (shard r holds input columns
+ *                       [r*K/tp, (r+1)*K/tp)); C[M, N] = sum_r A[:, shard r] W_r^T,
+ *                       accumulated in fp32 across shards (the all_reduce), rounded once.
+ *   workspace: qw_gemm_workspace_size(...) bytes (may be 0).
+ * Rules (bf16): K % 8 == 0, K/tp % 8 == 0 (row), N % 16 == 0 (N/2/tp % 8 == 0 for
+ * SILU_MUL), A/W/C 16-byte aligned.  f32 runs on CUDA cores (exact fp32 FMA).
+ */
+int qw_gemm(const void* A, const void* W, void* C, int64_t M, int64_t N, int64_t K, int tp, int mode,
+            int epilogue, void* workspace, size_t workspace_bytes, int dtype, void* stream);
+size_t qw_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int tp, int mode, int epilogue, int dtype);
+
+/*
+ * SiluAndMul on a merged gate_up output ([SK] §4, [TP] §4.2).
+ *   x dtype [T, 2*I] with shard r's block [gate_r (I/tp) | up_r (I/tp)];
+ *   out dtype [T, I], out[:, r*I/tp + j] = round(silu(gate_r[j]) * up_r[j]).
+ * Rules: I % tp == 0, (I/tp) * sizeof(dtype) % 16 == 0.
+ */
+int qw_silu_mul(const void* x, void* out, int64_t T, int64_t I, int tp, int dtype, void* stream);
+
+/*
+ * Vocab-parallel lm_head with the tied table ([VH] §4, [SK] §6, §8) and greedy
+ * sampling.
+ *   hidden    dtype [T, H]
+ *   last_idx  int32 [n_out] or NULL.  Prefill: row last_idx[i] of hidden is
+ *             projected (cu_seqlens_q[1:] - 1).  NULL: rows 0 .. n_out-1.
+ *   table     dtype [V, H]  (shard r = vocab rows [r*V/tp, (r+1)*V/tp); its logit
+ *             slice lands at columns [r*V/tp, (r+1)*V/tp): the gather + cat)
+ *   logits    dtype [n_out, V]
+ *   next_tokens int64 [n_out] or NULL: argmax over each logits row, lowest index on ties
+ *   workspace: qw_lm_head_workspace_size(...) bytes.
+ * Rules: V % tp == 0, V % 16 == 0, H % 8 == 0.
+ */
+int qw_lm_head(const void* hidden, int64_t T, const int32_t* last_idx, int64_t n_out, const void* table,
+               int64_t V, int64_t H, int tp, void* logits, int64_t* next_tokens, void* workspace,
+               size_t workspace_bytes, int dtype, void* stream);
+size_t qw_lm_head_workspace_size(int64_t n_out, int64_t V, int64_t H, int tp, int dtype);
+
+/* Greedy argmax over rows of logits dtype [M, V] -> int64 [M], lowest index on ties. */
+int qw_argmax(const void* logits, int64_t M, int64_t V, int64_t* out, int dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QW_H */

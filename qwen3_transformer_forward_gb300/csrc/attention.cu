@@ -1,0 +1,606 @@
+// Causal GQA attention of the Qwen3 forward pass ([SK] §7.2): prefill over
+// packed variable-length sequences and decode over the KV cache.
+//
+// Prefill (bf16, head_dim 128): flash-attention style online softmax.  One
+// CTA of 8 warps owns 128 queries of one (sequence, q head); K/V tiles of 64
+// keys are double-buffered in XOR-swizzled shared memory with cp.async; QK^T
+// and PV run on the tensor cores (mma.sync m16n8k16, fp32 accumulate); the
+// softmax is fp32 in registers (exp2 with the scale folded in).
+//
+// Decode (head_dim 128): split-KV.  One CTA of 128 threads owns one
+// (sequence, kv head, key chunk) and all q heads of that GQA group, so each
+// cached K/V byte is read once.  K/V tiles of 64 keys stream through shared
+// memory (cp.async double buffer); partial (m, l, o) per chunk go to the
+// caller's workspace and a combine kernel merges them.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace qw {
+namespace attn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// tensor-core helpers (legacy warp-level MMA)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// rows of 128 bf16 (256 B = 16 chunks of 16 B); chunk c of row r is stored at
+// chunk c ^ (r & 7) so that 8 consecutive rows at one chunk hit 8 bank groups
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return uint32_t(row) * 256u + uint32_t(chunk ^ (row & 7)) * 16u;
+}
+
+constexpr int PF_BR = 128, PF_BC = 64, PF_HD = 128, PF_THREADS = 256;
+constexpr size_t PF_SMEM = size_t(PF_BR) * 256 + 2 * 2 * size_t(PF_BC) * 256;   // Q + 2 x (K, V)
+
+__global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16_kernel(
+    const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
+    const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, const int32_t* __restrict__ seq_base,
+    int nh, int nkv, float scale_log2, bf16* __restrict__ out) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + PF_BR * 256;
+  uint8_t* sV = sK + 2 * PF_BC * 256;
+  const int s = blockIdx.z, h = blockIdx.y;
+  const int qs = cu_q[s];
+  const int Lq = cu_q[s + 1] - qs;
+  const int Lk = cu_k[s + 1] - cu_k[s];
+  const int n_qt = (Lq + PF_BR - 1) / PF_BR;
+  const int qt = int(gridDim.x) - 1 - int(blockIdx.x);   // longest (causal) tiles first
+  if (qt >= n_qt) return;
+  const int g = h / (nh / nkv);
+  const int64_t kbase = seq_base != nullptr ? int64_t(seq_base[s]) : int64_t(cu_k[s]);
+  const int offset = Lk - Lq;
+  const int q_lo = qt * PF_BR;
+  const int q_hi = min(Lq, q_lo + PF_BR);
+  const int kv_end = min(Lk, offset + q_hi);
+  const int n_kt = (kv_end + PF_BC - 1) / PF_BC;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t qrow_stride = int64_t(nh) * PF_HD;
+  const int64_t krow_stride = int64_t(nkv) * PF_HD;
+
+  // Q tile (rows past the sequence end are zero)
+  for (int i = tid; i < PF_BR * 16; i += PF_THREADS) {
+    const int r = i >> 4, c = i & 15;
+    const int qi = q_lo + r;
+    const bool ok = qi < Lq;
+    const bf16* src = q + (int64_t(qs) + (ok ? qi : 0)) * qrow_stride + int64_t(h) * PF_HD + c * 8;
+    cp_async16_zfill(smem_u32(sQ) + swz(r, c), src, ok);
+  }
+  auto load_kv = [&](int kt, int buf) {
+    for (int i = tid; i < PF_BC * 16; i += PF_THREADS) {
+      const int r = i >> 4, c = i & 15;
+      const int kj = kt * PF_BC + r;
+      const bool ok = kj < kv_end;
+      const int64_t row = kbase + (ok ? kj : 0);
+      const int64_t off = row * krow_stride + int64_t(g) * PF_HD + c * 8;
+      cp_async16_zfill(smem_u32(sK + buf * PF_BC * 256) + swz(r, c), k + off, ok);
+      cp_async16_zfill(smem_u32(sV + buf * PF_BC * 256) + swz(r, c), v + off, ok);
+    }
+  };
+  if (n_kt > 0) load_kv(0, 0);
+  cp_async_commit();
+
+  const int gq = lane >> 2, tq = lane & 3;       // mma fragment coordinates
+  const int mi = lane >> 3, ri = lane & 7;       // ldmatrix matrix / row index
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.0f, 0.0f};
+  uint32_t qf[8][4];
+  const int row0 = warp * 16;
+  const int qpos0 = offset + q_lo + row0 + gq;   // key position of this thread's first row (second: +8)
+
+  for (int kt = 0; kt < n_kt; ++kt) {
+    const int buf = kt & 1;
+    if (kt + 1 < n_kt) load_kv(kt + 1, buf ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    if (kt == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        ldsm_x4(smem_u32(sQ) + swz(row0 + ri + 8 * (mi & 1), 2 * kk + (mi >> 1)), qf[kk][0], qf[kk][1], qf[kk][2],
+                qf[kk][3]);
+    }
+    const uint32_t kb = smem_u32(sK + buf * PF_BC * 256);
+    const uint32_t vb = smem_u32(sV + buf * PF_BC * 256);
+    // S = Q K^T : 16 x 64 per warp
+    float sc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+      for (int jp = 0; jp < 4; ++jp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + swz(16 * jp + ri + 8 * (mi >> 1), 2 * kk + (mi & 1)), b0, b1, b2, b3);
+        mma_bf16(sc[2 * jp], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+        mma_bf16(sc[2 * jp + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+      }
+    }
+    // scale, causal mask, online softmax
+    const int kpos0 = kt * PF_BC;
+    const bool need_mask = (kpos0 + PF_BC > offset + q_lo + row0) || (kpos0 + PF_BC > kv_end);
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float x = sc[j][e] * scale_log2;
+        if (need_mask) {
+          const int kp = kpos0 + 8 * j + 2 * tq + (e & 1);
+          const int qp = qpos0 + (e >> 1) * 8;
+          if (kp > qp || kp >= kv_end) x = -INFINITY;
+        }
+        sc[j][e] = x;
+        mx[e >> 1] = fmaxf(mx[e >> 1], x);
+      }
+    }
+    float alpha[2], m_use[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      const float m_new = fmaxf(m_run[r], mx[r]);
+      m_use[r] = m_new == -INFINITY ? 0.0f : m_new;
+      alpha[r] = exp2f(m_run[r] - m_use[r]);
+      m_run[r] = m_new;
+      l_run[r] *= alpha[r];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p = exp2f(sc[j][e] - m_use[e >> 1]);
+        sc[j][e] = p;
+        l_run[e >> 1] += p;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      o[i][0] *= alpha[0];
+      o[i][1] *= alpha[0];
+      o[i][2] *= alpha[1];
+      o[i][3] *= alpha[1];
+    }
+    // O += P V
+#pragma unroll
+    for (int kc = 0; kc < 4; ++kc) {
+      const uint32_t a0 = pack_bf16(sc[2 * kc][0], sc[2 * kc][1]);
+      const uint32_t a1 = pack_bf16(sc[2 * kc][2], sc[2 * kc][3]);
+      const uint32_t a2 = pack_bf16(sc[2 * kc + 1][0], sc[2 * kc + 1][1]);
+      const uint32_t a3 = pack_bf16(sc[2 * kc + 1][2], sc[2 * kc + 1][3]);
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vb + swz(16 * kc + ri + 8 * (mi & 1), 2 * dp + (mi >> 1)), b0, b1, b2, b3);
+        mma_bf16(o[2 * dp], a0, a1, a2, a3, b0, b1);
+        mma_bf16(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+  // normalise and store
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+  }
+  const float inv0 = l_run[0] > 0.0f ? 1.0f / l_run[0] : 0.0f;
+  const float inv1 = l_run[1] > 0.0f ? 1.0f / l_run[1] : 0.0f;
+  const int qi0 = q_lo + row0 + gq, qi1 = qi0 + 8;
+#pragma unroll
+  for (int dn = 0; dn < 16; ++dn) {
+    const int d = 8 * dn + 2 * tq;
+    if (qi0 < Lq)
+      *reinterpret_cast<uint32_t*>(out + (int64_t(qs) + qi0) * qrow_stride + int64_t(h) * PF_HD + d) =
+          pack_bf16(o[dn][0] * inv0, o[dn][1] * inv0);
+    if (qi1 < Lq)
+      *reinterpret_cast<uint32_t*>(out + (int64_t(qs) + qi1) * qrow_stride + int64_t(h) * PF_HD + d) =
+          pack_bf16(o[dn][2] * inv1, o[dn][3] * inv1);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// fp32 prefill (small head_dim): one warp per (query token, q head)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) attn_prefill_f32_kernel(
+    const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+    const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, const int32_t* __restrict__ seq_base,
+    int n_seqs, int max_q, int nh, int nkv, int hd, float scale, float* __restrict__ out) {
+  const int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= int64_t(n_seqs) * max_q * nh) return;
+  const int s = int(w / (int64_t(max_q) * nh));
+  const int i = int((w / nh) % max_q);
+  const int h = int(w % nh);
+  const int Lq = cu_q[s + 1] - cu_q[s], Lk = cu_k[s + 1] - cu_k[s];
+  if (i >= Lq) return;
+  const int64_t t = int64_t(cu_q[s]) + i;
+  const int last = Lk - Lq + i;   // last visible key
+  const int g = h / (nh / nkv);
+  const int64_t kbase = seq_base != nullptr ? int64_t(seq_base[s]) : int64_t(cu_k[s]);
+  const float* qv = q + (t * nh + h) * int64_t(hd);
+  float m = -INFINITY, l = 0.0f;
+  float acc0 = 0.0f, acc1 = 0.0f;   // lane owns d = lane and d = lane + 32
+  for (int j0 = 0; j0 <= last; j0 += 32) {
+    const int j = j0 + lane;
+    float sc = -INFINITY;
+    if (j <= last) {
+      const float* kv = k + ((kbase + j) * nkv + g) * int64_t(hd);
+      float d = 0.0f;
+      for (int e = 0; e < hd; ++e) d = fmaf(qv[e], kv[e], d);
+      sc = d * scale;
+    }
+    const float mt = warp_max(sc);
+    const float m_new = fmaxf(m, mt);
+    const float alpha = expf(m - m_new);
+    const float p = j <= last ? expf(sc - m_new) : 0.0f;
+    l = l * alpha + warp_sum(p);
+    acc0 *= alpha;
+    acc1 *= alpha;
+    for (int jj = 0; jj < 32 && j0 + jj <= last; ++jj) {
+      const float pj = __shfl_sync(0xffffffffu, p, jj);
+      const float* vv = v + ((kbase + j0 + jj) * nkv + g) * int64_t(hd);
+      if (lane < hd) acc0 = fmaf(pj, vv[lane], acc0);
+      if (lane + 32 < hd) acc1 = fmaf(pj, vv[lane + 32], acc1);
+    }
+    m = m_new;
+  }
+  float* o = out + (t * nh + h) * int64_t(hd);
+  if (lane < hd) o[lane] = acc0 / l;
+  if (lane + 32 < hd) o[lane + 32] = acc1 / l;
+}
+
+// ---------------------------------------------------------------------------
+// decode: split-KV over the cache
+// ---------------------------------------------------------------------------
+constexpr int DC_HD = 128, DC_KT = 64, DC_THREADS = 128;
+
+template <typename T>
+constexpr size_t decode_smem() {
+  return 2 * 2 * size_t(DC_KT) * DC_HD * sizeof(T);
+}
+
+// element e of row r in a swizzled [rows][128] tile of T
+template <typename T>
+__device__ __forceinline__ int dswz(int r, int e) {
+  constexpr int EPC = 16 / sizeof(T);
+  const int c = e / EPC;
+  return r * DC_HD + ((c ^ (r & 7)) * EPC) + (e % EPC);
+}
+
+template <typename T, int G>
+__global__ void __launch_bounds__(DC_THREADS) attn_decode_kernel(
+    const T* __restrict__ q, const T* __restrict__ kc, const T* __restrict__ vc, const int32_t* __restrict__ ctx_lens,
+    const int32_t* __restrict__ seq_base, int nh, int nkv, float scale_log2, int chunk, int n_splits,
+    float* __restrict__ ws_o, float* __restrict__ ws_ml, T* __restrict__ out) {
+  constexpr int EPC = 16 / sizeof(T);      // elements per 16-byte chunk
+  constexpr int CPR = DC_HD / EPC;         // chunks per row
+  extern __shared__ __align__(128) uint8_t smem[];
+  T* sK = reinterpret_cast<T*>(smem);
+  T* sV = sK + 2 * DC_KT * DC_HD;
+  __shared__ float sQ[G][DC_HD];
+  __shared__ float sS[G][DC_KT];
+  __shared__ float sAlpha[G];
+  __shared__ float sM[G], sL[G];
+  __shared__ float sO[G][DC_HD];
+
+  const int b = blockIdx.z, g = blockIdx.y, split = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int L = ctx_lens[b];
+  const int start = split * chunk;
+  const int end = min(L, start + chunk);
+  const int h0 = g * G;
+  const int64_t row_stride = int64_t(nkv) * DC_HD;
+  const int64_t base = seq_base[b];
+
+  if (start >= end) {
+    if (n_splits > 1) {
+      if (tid < G) {
+        const int64_t idx = (int64_t(b) * nh + h0 + tid) * n_splits + split;
+        ws_ml[2 * idx] = -INFINITY;
+        ws_ml[2 * idx + 1] = 0.0f;
+      }
+    } else {
+      for (int i = tid; i < G * DC_HD; i += DC_THREADS)
+        out[(int64_t(b) * nh + h0 + i / DC_HD) * DC_HD + i % DC_HD] = from_f<T>(0.0f);
+    }
+    return;
+  }
+  for (int i = tid; i < G * DC_HD; i += DC_THREADS)
+    sQ[i / DC_HD][i % DC_HD] = to_f(q[(int64_t(b) * nh + h0 + i / DC_HD) * DC_HD + i % DC_HD]);
+  if (tid < G) {
+    sM[tid] = -INFINITY;
+    sL[tid] = 0.0f;
+  }
+  const int n_kt = (end - start + DC_KT - 1) / DC_KT;
+  auto load = [&](int kt, int buf) {
+    for (int i = tid; i < DC_KT * CPR; i += DC_THREADS) {
+      const int r = i / CPR, c = i % CPR;
+      const int key = start + kt * DC_KT + r;
+      const bool ok = key < end;
+      const int64_t off = (base + (ok ? key : start)) * row_stride + int64_t(g) * DC_HD + c * EPC;
+      const int so = buf * DC_KT * DC_HD + r * DC_HD + ((c ^ (r & 7)) * EPC);
+      cp_async16_zfill(smem_u32(sK + so), kc + off, ok);
+      cp_async16_zfill(smem_u32(sV + so), vc + off, ok);
+    }
+  };
+  load(0, 0);
+  cp_async_commit();
+
+  // PV ownership: dims d0, d0+1 for the keys of one half of the tile
+  const int dpair = tid & 63, khalf = tid >> 6;
+  float acc[G][2];
+#pragma unroll
+  for (int j = 0; j < G; ++j) acc[j][0] = acc[j][1] = 0.0f;
+
+  for (int kt = 0; kt < n_kt; ++kt) {
+    const int buf = kt & 1;
+    if (kt + 1 < n_kt) load(kt + 1, buf ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    const T* tK = sK + buf * DC_KT * DC_HD;
+    const T* tV = sV + buf * DC_KT * DC_HD;
+    // scores: thread -> key (tid % 64), heads tid/64, tid/64 + 2, ...
+    {
+      const int kk = tid % DC_KT;
+      const int key = start + kt * DC_KT + kk;
+      for (int j = tid / DC_KT; j < G; j += DC_THREADS / DC_KT) {
+        float d = 0.0f;
+#pragma unroll 4
+        for (int c = 0; c < CPR; ++c) {
+          float f[EPC];
+          load16(tK + kk * DC_HD + ((c ^ (kk & 7)) * EPC), f);
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) d = fmaf(sQ[j][c * EPC + e], f[e], d);
+        }
+        sS[j][kk] = key < end ? d * scale_log2 : -INFINITY;
+      }
+    }
+    __syncthreads();
+    // online softmax: warp w handles heads w, w + 4
+    for (int j = warp; j < G; j += DC_THREADS / 32) {
+      const float s0 = sS[j][lane], s1 = sS[j][lane + 32];
+      const float mt = warp_max(fmaxf(s0, s1));
+      const float m_old = sM[j];
+      const float m_new = fmaxf(m_old, mt);
+      const float alpha = exp2f(m_old - m_new);       // m_new is finite: the tile has a valid key
+      const float p0 = exp2f(s0 - m_new), p1 = exp2f(s1 - m_new);
+      const float ps = warp_sum(p0 + p1);
+      sS[j][lane] = p0;
+      sS[j][lane + 32] = p1;
+      if (lane == 0) {
+        sM[j] = m_new;
+        sL[j] = sL[j] * alpha + ps;
+        sAlpha[j] = alpha;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const float al = sAlpha[j];
+      acc[j][0] *= al;
+      acc[j][1] *= al;
+    }
+    const int d0 = 2 * dpair;
+#pragma unroll 4
+    for (int kk = khalf * 32; kk < khalf * 32 + 32; ++kk) {
+      const float v0 = to_f(tV[dswz<T>(kk, d0)]);
+      const float v1 = to_f(tV[dswz<T>(kk, d0 + 1)]);
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const float p = sS[j][kk];
+        acc[j][0] = fmaf(p, v0, acc[j][0]);
+        acc[j][1] = fmaf(p, v1, acc[j][1]);
+      }
+    }
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+  // combine the two key halves
+  if (khalf == 1) {
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      sO[j][2 * dpair] = acc[j][0];
+      sO[j][2 * dpair + 1] = acc[j][1];
+    }
+  }
+  __syncthreads();
+  if (khalf == 0) {
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const float o0 = acc[j][0] + sO[j][2 * dpair];
+      const float o1 = acc[j][1] + sO[j][2 * dpair + 1];
+      const int64_t hrow = int64_t(b) * nh + h0 + j;
+      if (n_splits > 1) {
+        const int64_t idx = hrow * n_splits + split;
+        ws_o[idx * DC_HD + 2 * dpair] = o0;
+        ws_o[idx * DC_HD + 2 * dpair + 1] = o1;
+        if (dpair == 0) {
+          ws_ml[2 * idx] = sM[j];
+          ws_ml[2 * idx + 1] = sL[j];
+        }
+      } else {
+        const float inv = 1.0f / sL[j];
+        out[hrow * DC_HD + 2 * dpair] = from_f<T>(o0 * inv);
+        out[hrow * DC_HD + 2 * dpair + 1] = from_f<T>(o1 * inv);
+      }
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(DC_HD) attn_decode_combine_kernel(const float* __restrict__ ws_o,
+                                                                    const float* __restrict__ ws_ml, int n_splits,
+                                                                    T* __restrict__ out) {
+  const int64_t hrow = blockIdx.x;
+  const int d = threadIdx.x;
+  float M = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, ws_ml[2 * (hrow * n_splits + s)]);
+  float L = 0.0f, o = 0.0f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < n_splits; ++s) {
+      const int64_t idx = hrow * n_splits + s;
+      const float ms = ws_ml[2 * idx];
+      if (ms == -INFINITY) continue;
+      const float w = exp2f(ms - M);
+      L += ws_ml[2 * idx + 1] * w;
+      o += ws_o[idx * DC_HD + d] * w;
+    }
+  }
+  out[hrow * DC_HD + d] = from_f<T>(L > 0.0f ? o / L : 0.0f);
+}
+
+struct DecodePlan {
+  int splits;
+  int chunk;
+};
+
+inline DecodePlan decode_plan(int B, int max_context, int nkv_unused) {
+  (void)nkv_unused;
+  DecodePlan p{1, max_context > 0 ? max_context : 1};
+  if (max_context <= 0) return p;
+  // aim for >= ~4 CTAs per SM in total (152 SMs), keys chunks >= 128
+  const int pairs = B * 8 > 0 ? B * 8 : 1;
+  int s = (4 * 152 + pairs - 1) / pairs;
+  const int smax = (max_context + 127) / 128;
+  s = s < 1 ? 1 : (s > smax ? smax : s);
+  int chunk = (max_context + s - 1) / s;
+  chunk = (chunk + DC_KT - 1) / DC_KT * DC_KT;
+  p.chunk = chunk;
+  p.splits = (max_context + chunk - 1) / chunk;
+  return p;
+}
+
+}  // namespace attn
+}  // namespace qw
+
+using namespace qw;
+using namespace qw::attn;
+
+extern "C" int qw_attention_prefill(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                                    const int32_t* cu_seqlens_k, const int32_t* seq_base, int n_seqs,
+                                    int max_seqlen_q, int n_heads, int n_kv_heads, int head_dim, float scale,
+                                    void* out, int dtype, void* stream) {
+  if (dtype != QW_BF16 && dtype != QW_F32) return set_error(QW_ERR_DTYPE, "qw_attention_prefill: dtype %d", dtype);
+  if (n_seqs < 0 || max_seqlen_q < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_prefill: bad sizes");
+  if (n_heads % n_kv_heads) return set_error(QW_ERR_SHAPE, "qw_attention_prefill: nh %% nkv != 0");
+  if (dtype == QW_BF16 && head_dim != 128)
+    return set_error(QW_ERR_SHAPE, "qw_attention_prefill: bf16 path needs head_dim 128 (got %d)", head_dim);
+  if (dtype == QW_F32 && head_dim > 64)
+    return set_error(QW_ERR_SHAPE, "qw_attention_prefill: f32 path needs head_dim <= 64 (got %d)", head_dim);
+  if (n_seqs == 0 || max_seqlen_q == 0) return QW_OK;
+  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_prefill: null pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == QW_BF16) {
+    static bool configured = false;
+    if (!configured) {
+      cudaError_t e = cudaFuncSetAttribute(attn_prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(PF_SMEM));
+      if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      configured = true;
+    }
+    dim3 grid(unsigned((max_seqlen_q + PF_BR - 1) / PF_BR), unsigned(n_heads), unsigned(n_seqs));
+    attn_prefill_bf16_kernel<<<grid, PF_THREADS, PF_SMEM, st>>>(
+        static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v), cu_seqlens_q,
+        cu_seqlens_k, seq_base, n_heads, n_kv_heads, scale * kLog2e, static_cast<bf16*>(out));
+    return check_launch("attn_prefill_bf16_kernel");
+  }
+  const int64_t threads = int64_t(n_seqs) * max_seqlen_q * n_heads * 32;
+  attn_prefill_f32_kernel<<<unsigned((threads + 127) / 128), 128, 0, st>>>(
+      static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), cu_seqlens_q,
+      cu_seqlens_k, seq_base, n_seqs, max_seqlen_q, n_heads, n_kv_heads, head_dim, scale, static_cast<float*>(out));
+  return check_launch("attn_prefill_f32_kernel");
+}
+
+extern "C" size_t qw_attention_decode_workspace_size(int B, int max_context, int n_heads, int head_dim) {
+  if (B <= 0 || max_context <= 0 || n_heads <= 0 || head_dim <= 0) return 0;
+  const DecodePlan p = decode_plan(B, max_context, 0);
+  if (p.splits <= 1) return 0;
+  return size_t(B) * n_heads * p.splits * (size_t(head_dim) + 2) * sizeof(float);
+}
+
+template <typename T, int G>
+static int launch_decode(const void* q, const void* kc, const void* vc, const int32_t* cl, const int32_t* sb, int B,
+                         int nh, int nkv, float sl2, const DecodePlan& p, float* wo, float* wml, void* out,
+                         cudaStream_t st) {
+  constexpr size_t sm = decode_smem<T>();
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm));
+    if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    configured = true;
+  }
+  dim3 grid(unsigned(p.splits), unsigned(nkv), unsigned(B));
+  attn_decode_kernel<T, G><<<grid, DC_THREADS, sm, st>>>(static_cast<const T*>(q), static_cast<const T*>(kc),
+                                                         static_cast<const T*>(vc), cl, sb, nh, nkv, sl2, p.chunk,
+                                                         p.splits, wo, wml, static_cast<T*>(out));
+  int rc = check_launch("attn_decode_kernel");
+  if (rc || p.splits <= 1) return rc;
+  attn_decode_combine_kernel<T><<<unsigned(B * nh), DC_HD, 0, st>>>(wo, wml, p.splits, static_cast<T*>(out));
+  return check_launch("attn_decode_combine_kernel");
+}
+
+extern "C" int qw_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* context_lens, const int32_t* seq_base, int B, int max_context,
+                                   int n_heads, int n_kv_heads, int head_dim, float scale, void* out, void* workspace,
+                                   size_t workspace_bytes, int dtype, void* stream) {
+  if (dtype != QW_BF16 && dtype != QW_F32) return set_error(QW_ERR_DTYPE, "qw_attention_decode: dtype %d", dtype);
+  if (B < 0 || max_context < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode: bad sizes");
+  if (n_heads % n_kv_heads || head_dim != 128)
+    return set_error(QW_ERR_SHAPE, "qw_attention_decode: needs nh %% nkv == 0 and head_dim 128");
+  const int G = n_heads / n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return set_error(QW_ERR_SHAPE, "qw_attention_decode: group %d", G);
+  if (B == 0) return QW_OK;
+  if (!q || !k_cache || !v_cache || !context_lens || !seq_base || !out)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode: null pointer");
+  const DecodePlan p = decode_plan(B, max_context, n_kv_heads);
+  const size_t need = qw_attention_decode_workspace_size(B, max_context, n_heads, head_dim);
+  if (need && (!workspace || workspace_bytes < need))
+    return set_error(QW_ERR_WORKSPACE, "qw_attention_decode: workspace of %zu bytes needed", need);
+  float* wml = static_cast<float*>(workspace);
+  float* wo = wml ? wml + size_t(B) * n_heads * p.splits * 2 : nullptr;
+  const float sl2 = scale * kLog2e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+#define QW_DEC(TT)                                                                                                   \
+  switch (G) {                                                                                                       \
+    case 1: return launch_decode<TT, 1>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, sl2, p, \
+                                        wo, wml, out, st);                                                           \
+    case 2: return launch_decode<TT, 2>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, sl2, p, \
+                                        wo, wml, out, st);                                                           \
+    case 4: return launch_decode<TT, 4>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, sl2, p, \
+                                        wo, wml, out, st);                                                           \
+    default: return launch_decode<TT, 8>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, sl2,  \
+                                         p, wo, wml, out, st);                                                       \
+  }
+  if (dtype == QW_BF16) { QW_DEC(bf16) }
+  QW_DEC(float)
+#undef QW_DEC
+}

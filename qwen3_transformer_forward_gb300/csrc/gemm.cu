@@ -1,0 +1,813 @@
+// Linear layers of the Qwen3 forward pass on GB300 tensor cores.
+//
+// C = A W^T in the tensor-parallel layouts of the parallel Linear family
+// ([TP] §3-§4, [SK] §5):
+//   COLUMN      W [N, K], tp shards stacked along N (merged QKV, gate_up, lm_head)
+//   ROW_REDUCE  W [tp, N, K/tp]; the shard partial sums are accumulated in
+//               the same fp32 TMEM accumulator (the emulated all_reduce)
+//   SILU_MUL    fused SiluAndMul epilogue on a merged gate_up ([SK] §4)
+//
+// bf16 path: one CTA of 6 warps per 128 x BN output tile.
+//   warp 0      TMA producer: 64-wide K slabs of both operands into a
+//               STAGES-deep shared-memory ring (128-byte swizzle)
+//   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=BN, K=16)
+//               from one thread; tcgen05.commit frees ring slots
+//   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator, convert,
+//               store (or fp32 split-K partials)
+// Prefill (many tokens): MMA-A = activations, MMA-B = weights, BN = 256.
+// Decode (<= 64 tokens): operands swapped (MMA-A = 128 weight rows,
+// MMA-B = the tokens padded to 16/32/64) and split along K so that enough
+// CTAs stream the weights; a reduce kernel sums the fp32 partials.
+//
+// Every mbarrier wait is bounded (2 s of %globaltimer); on timeout the kernel
+// records an error word, drains its own copies and frees TMEM.
+//
+// f32 path: exact fp32 FMA on CUDA cores (used by the small fp32 model).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <math.h>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "common.cuh"
+
+namespace qw {
+
+template <typename T>
+int launch_gather_rows(const void* src, int64_t n_src, const int32_t* idx, int64_t n, int64_t H, void* out,
+                       cudaStream_t st);
+template <typename T>
+int launch_argmax(const void* logits, int64_t M, int64_t V, int64_t* out, cudaStream_t st);
+
+namespace tc {
+
+__device__ unsigned int g_tc_timeout = 0;
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int EPI_NONE = 0, EPI_SILU = 1;
+
+struct TcArgs {
+  bf16* C;              // output (bf16)
+  float* partial;       // split-K fp32 partials [splits][M][Nfull] or nullptr
+  int64_t ldc;          // output row stride
+  int64_t M;            // token rows
+  int64_t N;            // output features (full width before SiluAndMul)
+  int p_tiles, q_tiles; // tiles along MMA-A rows (128) and MMA-B rows (BN)
+  int p_fastest;        // raster order
+  int kblocks;          // k-blocks per split
+  int kblocks_total;
+  int kpb;              // k-blocks per shard (ROW_REDUCE)
+  int64_t k_shard;      // K / tp
+  int64_t i_l;          // intermediate per shard (SILU)
+  int silu_tps;         // output tiles per shard (SILU)
+};
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of parity `parity`; gives up after kTimeoutNs, recording `code`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      atomicOr(&g_tc_timeout, code);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulator
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes grouped in 1024-byte (8-row) atoms.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= uint64_t(1) << 16;                  // leading byte offset (unused for swizzled K-major)
+  d |= uint64_t(1024 >> 4) << 32;          // stride byte offset between 8-row atoms
+  d |= uint64_t(1) << 46;                  // descriptor version
+  d |= uint64_t(2) << 61;                  // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor for kind::f16: bf16 A and B (K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+__device__ __forceinline__ float silu_mul_bf16(float g, float u) {
+  // gate_up is a model-dtype tensor before SiluAndMul: round both halves first
+  g = round_t<bf16>(g);
+  u = round_t<bf16>(u);
+  return g / (1.0f + expf(-g)) * u;
+}
+
+template <int BN>
+struct TileCfg {
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+};
+
+template <int BN, int STAGES>
+constexpr size_t smem_bytes() {
+  return 1024 + size_t(STAGES) * (TileCfg<BN>::A_BYTES + TileCfg<BN>::B_BYTES) + 256;
+}
+
+// SWAP=false: MMA-A = activations rows (M), MMA-B = weight rows (N).
+// SWAP=true : MMA-A = weight rows (N),      MMA-B = token rows (M, padded to BN).
+template <int BN, int STAGES, bool SWAP, int EPI, bool WROW>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmAct, const __grid_constant__ CUtensorMap tmW, TcArgs a) {
+  using Cfg = TileCfg<BN>;
+  constexpr uint32_t A_BYTES = Cfg::A_BYTES, B_BYTES = Cfg::B_BYTES;
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = sm;
+  uint8_t* sB = sm + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* consumed = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  auto bar_full = [&](int s) { return smem_u32(bars + s); };
+  auto bar_empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  const uint32_t bar_done = smem_u32(bars + 2 * STAGES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lin = blockIdx.x;
+  const int tile_p = a.p_fastest ? lin % a.p_tiles : lin / a.q_tiles;
+  const int tile_q = a.p_fastest ? lin / a.p_tiles : lin % a.q_tiles;
+  const int split = blockIdx.y;
+  const int kb0 = split * a.kblocks;
+  const int kb1 = min(a.kblocks_total, kb0 + a.kblocks);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    *consumed = 0;
+    fence_mbar_init();
+    prefetch_map(&tmAct);
+    prefetch_map(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  int issued = kb0;
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    int r_s = 0;
+    int64_t jl0 = 0;
+    if (EPI == EPI_SILU && !SWAP) {
+      r_s = tile_q / a.silu_tps;
+      jl0 = int64_t(tile_q % a.silu_tps) * (BN / 2);
+    }
+    for (int kb = kb0; kb < kb1; ++kb) {
+      const int i = kb - kb0;
+      const int s = i % STAGES;
+      const uint32_t ph = (i / STAGES) & 1;
+      if (!mbar_wait(bar_empty(s), ph ^ 1, 1u)) {
+        *abort_flag = 1;
+        break;
+      }
+      if (*abort_flag) break;
+      mbar_expect_tx(bar_full(s), A_BYTES + B_BYTES);
+      int xa, xw, rw = 0;
+      if (WROW) {
+        rw = kb / a.kpb;
+        xw = (kb % a.kpb) * BK;
+        xa = int(rw * a.k_shard) + xw;
+      } else {
+        xa = xw = kb * BK;
+      }
+      const uint32_t dA = smem_u32(sA + s * A_BYTES);
+      const uint32_t dB = smem_u32(sB + s * B_BYTES);
+      if (!SWAP) {
+        tma_load_2d(dA, &tmAct, bar_full(s), xa, tile_p * BM);
+        if (EPI == EPI_SILU) {
+          const int64_t g0 = int64_t(r_s) * 2 * a.i_l + jl0;
+          tma_load_2d(dB, &tmW, bar_full(s), xw, int(g0));
+          tma_load_2d(dB + B_BYTES / 2, &tmW, bar_full(s), xw, int(g0 + a.i_l));
+        } else if (WROW) {
+          tma_load_3d(dB, &tmW, bar_full(s), xw, tile_q * BN, rw);
+        } else {
+          tma_load_2d(dB, &tmW, bar_full(s), xw, tile_q * BN);
+        }
+      } else {
+        if (WROW) tma_load_3d(dA, &tmW, bar_full(s), xw, tile_p * BM, rw);
+        else tma_load_2d(dA, &tmW, bar_full(s), xw, tile_p * BM);
+        tma_load_2d(dB, &tmAct, bar_full(s), xa, tile_q * BN);
+      }
+      issued = kb + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idesc = idesc_bf16(BM, BN);
+    int kb = kb0;
+    for (; kb < kb1; ++kb) {
+      const int i = kb - kb0;
+      const int s = i % STAGES;
+      const uint32_t ph = (i / STAGES) & 1;
+      if (!mbar_wait(bar_full(s), ph, 2u)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t da = sw128_desc(smem_u32(sA + s * A_BYTES));
+      const uint64_t db = sw128_desc(smem_u32(sB + s * B_BYTES));
+#pragma unroll
+      for (int k = 0; k < BK / UMMA_K; ++k)
+        umma_bf16(tmem, da + uint64_t(2 * k), db + uint64_t(2 * k), idesc, (i > 0 || k > 0) ? 1u : 0u);
+      umma_commit(bar_empty(s));
+    }
+    *consumed = kb;
+    umma_commit(bar_done);
+  } else if (warp >= 2) {
+    // ---------------- epilogue ----------------
+    const bool ok = mbar_wait(bar_done, 0, 4u);
+    tc_fence_after();
+    const int quarter = warp & 3;
+    const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16);
+    const bool has_acc = kb1 > kb0;
+    if (!SWAP) {
+      const int64_t m = int64_t(tile_p) * BM + quarter * 32 + lane;
+      if (EPI == EPI_NONE) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(trow + c, r);
+          tmem_ld_wait();
+          if (!ok || !has_acc) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = 0u;
+          }
+          const int64_t n0 = int64_t(tile_q) * BN + c;
+          if (m < a.M) {
+            bf16* dst = a.C + m * a.ldc + n0;
+            if (n0 + 32 <= a.N) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint4 u;
+                u.x = pack_bf16(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                u.y = pack_bf16(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                u.z = pack_bf16(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                u.w = pack_bf16(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                d4[v] = u;
+              }
+            } else {
+              for (int e = 0; e < 32; ++e)
+                if (n0 + e < a.N) dst[e] = __float2bfloat16_rn(__uint_as_float(r[e]));
+            }
+          }
+        }
+      } else {  // EPI_SILU
+        const int r_s = tile_q / a.silu_tps;
+        const int64_t jl0 = int64_t(tile_q % a.silu_tps) * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(trow + c, g);
+          tmem_ld32(trow + BN / 2 + c, u);
+          tmem_ld_wait();
+          if (m < a.M && ok && has_acc) {
+            const int64_t j0 = jl0 + c;
+            bf16* dst = a.C + m * a.ldc + int64_t(r_s) * a.i_l + j0;
+            if (j0 + 32 <= a.i_l) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                float o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  o[e] = silu_mul_bf16(__uint_as_float(g[8 * v + e]), __uint_as_float(u[8 * v + e]));
+                uint4 w;
+                w.x = pack_bf16(o[0], o[1]);
+                w.y = pack_bf16(o[2], o[3]);
+                w.z = pack_bf16(o[4], o[5]);
+                w.w = pack_bf16(o[6], o[7]);
+                d4[v] = w;
+              }
+            } else {
+              for (int e = 0; e < 32; ++e)
+                if (j0 + e < a.i_l)
+                  dst[e] = __float2bfloat16_rn(silu_mul_bf16(__uint_as_float(g[e]), __uint_as_float(u[e])));
+            }
+          }
+        }
+      }
+    } else {
+      // swapped: TMEM lane = output feature, column = token
+      const int64_t p = int64_t(tile_p) * BM + quarter * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(trow + c, r);   // TMEM_COLS >= 32 >= BN - c: the load stays inside the allocation
+        tmem_ld_wait();
+        if (!ok || !has_acc) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
+        }
+        if (p < a.N) {
+          const int lim = BN - c < 32 ? BN - c : 32;
+          for (int e = 0; e < lim; ++e) {
+            const int64_t j = int64_t(tile_q) * BN + c + e;
+            if (j < a.M) {
+              if (a.partial != nullptr)
+                a.partial[(int64_t(split) * a.M + j) * a.N + p] = __uint_as_float(r[e]);
+              else
+                a.C[j * a.ldc + p] = __float2bfloat16_rn(__uint_as_float(r[e]));
+            }
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // drain copies that were issued but never consumed, so that no TMA write
+    // lands in shared memory after the CTA exits
+    for (int kb = *consumed; kb < issued; ++kb) {
+      const int i = kb - kb0;
+      mbar_wait(bar_full(i % STAGES), (i / STAGES) & 1, 8u);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  }
+}
+
+// fp32 split-K partials -> bf16 output, with an optional SiluAndMul on the
+// merged gate_up columns ([SK] §4)
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, int splits, int64_t M,
+                                                            int64_t N, bf16* __restrict__ C, int64_t ldc, int epi,
+                                                            int64_t i_l) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = int64_t(splits) > 0 ? M * N : 0;
+  if (epi == EPI_NONE) {
+    if (idx >= M * N) return;
+    float s = 0.0f;
+    for (int k = 0; k < splits; ++k) s += part[k * stride + idx];
+    const int64_t m = idx / N, n = idx % N;
+    C[m * ldc + n] = __float2bfloat16_rn(s);
+  } else {
+    const int64_t I = N / 2;
+    if (idx >= M * I) return;
+    const int64_t m = idx / I, o = idx % I;
+    const int64_t r = o / i_l, j = o % i_l;
+    const int64_t gcol = r * 2 * i_l + j;
+    float g = 0.0f, u = 0.0f;
+    for (int k = 0; k < splits; ++k) {
+      g += part[k * stride + m * N + gcol];
+      u += part[k * stride + m * N + gcol + i_l];
+    }
+    C[m * ldc + o] = __float2bfloat16_rn(silu_mul_bf16(g, u));
+  }
+}
+
+}  // namespace tc
+
+// ===========================================================================
+// fp32 GEMM on CUDA cores (exact fp32 FMA; the small fp32 model)
+// ===========================================================================
+__device__ __forceinline__ float w_at(const float* W, int64_t n, int64_t k, int64_t N, int64_t K, int64_t K_l,
+                                      int row) {
+  if (!row) return W[n * K + k];
+  const int64_t r = k / K_l;
+  return W[(r * N + n) * K_l + (k - r * K_l)];
+}
+
+__global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__ A, const float* __restrict__ W,
+                                                       float* __restrict__ C, int64_t M, int64_t Nout, int64_t N,
+                                                       int64_t K, int64_t K_l, int row, int silu, int64_t i_l) {
+  __shared__ float sa[16][17];
+  __shared__ float sw[2][16][17];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int64_t m = int64_t(blockIdx.y) * 16 + ty;
+  const int64_t o = int64_t(blockIdx.x) * 16 + tx;      // output column
+  const int64_t o_load = int64_t(blockIdx.x) * 16 + ty; // column whose weights thread (ty, tx) loads
+  int64_t n0 = o_load, n1 = 0;
+  if (silu) {
+    const int64_t r = o_load / i_l, j = o_load % i_l;
+    n0 = r * 2 * i_l + j;
+    n1 = n0 + i_l;
+  }
+  float acc0 = 0.0f, acc1 = 0.0f;
+  for (int64_t k0 = 0; k0 < K; k0 += 16) {
+    const int64_t mm = int64_t(blockIdx.y) * 16 + ty;
+    sa[ty][tx] = (mm < M && k0 + tx < K) ? A[mm * K + k0 + tx] : 0.0f;
+    const bool ok = o_load < Nout && k0 + tx < K;
+    sw[0][ty][tx] = ok ? w_at(W, n0, k0 + tx, N, K, K_l, row) : 0.0f;
+    sw[1][ty][tx] = (ok && silu) ? w_at(W, n1, k0 + tx, N, K, K_l, row) : 0.0f;
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      acc0 = fmaf(sa[ty][kk], sw[0][tx][kk], acc0);
+      if (silu) acc1 = fmaf(sa[ty][kk], sw[1][tx][kk], acc1);
+    }
+    __syncthreads();
+  }
+  if (m < M && o < Nout) {
+    float v = acc0;
+    if (silu) v = acc0 / (1.0f + expf(-acc0)) * acc1;
+    C[m * Nout + o] = v;
+  }
+}
+
+// ===========================================================================
+// host side: tensor maps (cached), planning, launch
+// ===========================================================================
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+struct MapKey {
+  uint64_t ptr;
+  uint64_t d0, d1, d2, s0, s1;
+  uint32_t b0, b1, rank;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 && s0 == o.s0 && s1 == o.s1 && b0 == o.b0 &&
+           b1 == o.b1 && rank == o.rank;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = k.ptr * 0x9E3779B97F4A7C15ull;
+    for (uint64_t v : {k.d0, k.d1, k.d2, k.s0, k.s1, uint64_t(k.b0) << 32 | k.b1, uint64_t(k.rank)})
+      h = (h ^ v) * 0x100000001B3ull;
+    return size_t(h);
+  }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+// 2D (rank 2) or 3D (rank 3) bf16 map, innermost dim first, 128-byte swizzle,
+// box = 64 elements x box_rows (x 1)
+int make_map(CUtensorMap* out, const void* ptr, int rank, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s0_bytes,
+             uint64_t s1_bytes, uint32_t box_rows) {
+  MapKey key{reinterpret_cast<uint64_t>(ptr), d0, d1, d2, s0_bytes, s1_bytes, 64u, box_rows, uint32_t(rank)};
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+      *out = it->second;
+      return QW_OK;
+    }
+  }
+  auto fn = encode_fn();
+  if (!fn) return set_error(QW_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s0_bytes, s1_bytes};
+  cuuint32_t box[3] = {64u, box_rows, 1u};
+  cuuint32_t es[3] = {1u, 1u, 1u};
+  CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(QW_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  if (g_maps.size() > 8192) g_maps.clear();
+  g_maps.emplace(key, *out);
+  return QW_OK;
+}
+
+struct Plan {
+  bool swap;
+  int bn;
+  int splits;
+  int kblocks_total;
+  int kpb;
+  size_t ws_bytes;
+};
+
+constexpr int kSms = 152;
+
+Plan plan_bf16(int64_t M, int64_t N, int64_t K, int tp, int mode) {
+  Plan p{};
+  const int64_t Kl = mode == QW_GEMM_ROW_REDUCE ? K / tp : K;
+  p.kpb = int((Kl + tc::BK - 1) / tc::BK);
+  p.kblocks_total = mode == QW_GEMM_ROW_REDUCE ? p.kpb * tp : p.kpb;
+  p.swap = M <= 64;
+  p.splits = 1;
+  if (p.swap) {
+    p.bn = M <= 16 ? 16 : M <= 32 ? 32 : 64;
+    const int p_tiles = int((N + tc::BM - 1) / tc::BM);
+    int s = (2 * kSms + p_tiles - 1) / p_tiles;
+    s = s < 1 ? 1 : s;
+    const int smax = p.kblocks_total / 2 > 1 ? p.kblocks_total / 2 : 1;
+    p.splits = s < smax ? s : smax;
+    // even out the k-blocks per split
+    const int per = (p.kblocks_total + p.splits - 1) / p.splits;
+    p.splits = (p.kblocks_total + per - 1) / per;
+    p.ws_bytes = p.splits > 1 ? size_t(p.splits) * size_t(M) * size_t(N) * sizeof(float) : 0;
+  } else {
+    p.bn = 256;
+  }
+  return p;
+}
+
+template <int BN, int STAGES, bool SWAP, int EPI, bool WROW>
+int launch_tc(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArgs& args, int splits, cudaStream_t st) {
+  auto kern = tc::gemm_tc_kernel<BN, STAGES, SWAP, EPI, WROW>;
+  constexpr size_t smem = tc::smem_bytes<BN, STAGES>();
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    configured = true;
+  }
+  dim3 grid(unsigned(args.p_tiles * args.q_tiles), unsigned(splits));
+  kern<<<grid, 192, smem, st>>>(act, w, args);
+  return check_launch("gemm_tc_kernel");
+}
+
+int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64_t K, int tp, int mode, int epi,
+              void* ws, size_t ws_bytes, cudaStream_t st) {
+  const Plan p = plan_bf16(M, N, K, tp, mode);
+  const int64_t Kl = mode == QW_GEMM_ROW_REDUCE ? K / tp : K;
+  const bool wrow = mode == QW_GEMM_ROW_REDUCE;
+  int rc;
+  CUtensorMap mA, mW;
+  tc::TcArgs a{};
+  a.C = C;
+  a.ldc = epi == QW_EPI_SILU_MUL ? N / 2 : N;
+  a.M = M;
+  a.N = N;
+  a.kblocks_total = p.kblocks_total;
+  a.kpb = p.kpb;
+  a.k_shard = Kl;
+  a.i_l = epi == QW_EPI_SILU_MUL ? N / 2 / tp : 0;
+  if (!p.swap) {
+    rc = make_map(&mA, A, 2, uint64_t(K), uint64_t(M), 1, uint64_t(K) * 2, 0, tc::BM);
+    if (rc) return rc;
+    const uint32_t wrows = epi == QW_EPI_SILU_MUL ? uint32_t(p.bn / 2) : uint32_t(p.bn);
+    if (wrow) rc = make_map(&mW, W, 3, uint64_t(Kl), uint64_t(N), uint64_t(tp), uint64_t(Kl) * 2,
+                            uint64_t(Kl) * 2 * uint64_t(N), wrows);
+    else rc = make_map(&mW, W, 2, uint64_t(K), uint64_t(N), 1, uint64_t(K) * 2, 0, wrows);
+    if (rc) return rc;
+    a.p_tiles = int((M + tc::BM - 1) / tc::BM);
+    if (epi == QW_EPI_SILU_MUL) {
+      a.silu_tps = int((a.i_l + p.bn / 2 - 1) / (p.bn / 2));
+      a.q_tiles = a.silu_tps * tp;
+    } else {
+      a.q_tiles = int((N + p.bn - 1) / p.bn);
+    }
+    a.p_fastest = (M * K * 2) <= (int64_t(48) << 20) ? 1 : 0;
+    a.kblocks = p.kblocks_total;
+    a.partial = nullptr;
+    if (epi == QW_EPI_SILU_MUL) return launch_tc<256, 4, false, tc::EPI_SILU, false>(mA, mW, a, 1, st);
+    if (wrow) return launch_tc<256, 4, false, tc::EPI_NONE, true>(mA, mW, a, 1, st);
+    return launch_tc<256, 4, false, tc::EPI_NONE, false>(mA, mW, a, 1, st);
+  }
+  // swapped operands for few tokens
+  rc = make_map(&mA, A, 2, uint64_t(K), uint64_t(M), 1, uint64_t(K) * 2, 0, uint32_t(p.bn));
+  if (rc) return rc;
+  if (wrow) rc = make_map(&mW, W, 3, uint64_t(Kl), uint64_t(N), uint64_t(tp), uint64_t(Kl) * 2,
+                          uint64_t(Kl) * 2 * uint64_t(N), tc::BM);
+  else rc = make_map(&mW, W, 2, uint64_t(K), uint64_t(N), 1, uint64_t(K) * 2, 0, tc::BM);
+  if (rc) return rc;
+  a.p_tiles = int((N + tc::BM - 1) / tc::BM);
+  a.q_tiles = 1;
+  a.p_fastest = 1;
+  a.kblocks = (p.kblocks_total + p.splits - 1) / p.splits;
+  const bool need_reduce = p.splits > 1 || epi == QW_EPI_SILU_MUL;
+  float* part = nullptr;
+  if (need_reduce) {
+    const size_t need = size_t(p.splits) * size_t(M) * size_t(N) * sizeof(float);
+    if (!ws || ws_bytes < need)
+      return set_error(QW_ERR_WORKSPACE, "qw_gemm: workspace of %zu bytes needed", need);
+    part = static_cast<float*>(ws);
+  }
+  a.partial = part;
+  int r;
+#define QW_SWAP_LAUNCH(BNV)                                                                        \
+  r = wrow ? launch_tc<BNV, 8, true, tc::EPI_NONE, true>(mA, mW, a, p.splits, st)                  \
+           : launch_tc<BNV, 8, true, tc::EPI_NONE, false>(mA, mW, a, p.splits, st);
+  if (p.bn == 16) { QW_SWAP_LAUNCH(16) }
+  else if (p.bn == 32) { QW_SWAP_LAUNCH(32) }
+  else { QW_SWAP_LAUNCH(64) }
+#undef QW_SWAP_LAUNCH
+  if (r) return r;
+  if (need_reduce) {
+    const int64_t outs = epi == QW_EPI_SILU_MUL ? M * (N / 2) : M * N;
+    tc::splitk_reduce_kernel<<<unsigned((outs + 255) / 256), 256, 0, st>>>(
+        part, p.splits, M, N, C, a.ldc, epi == QW_EPI_SILU_MUL ? tc::EPI_SILU : tc::EPI_NONE, a.i_l);
+    return check_launch("splitk_reduce_kernel");
+  }
+  return QW_OK;
+}
+
+size_t gemm_ws(int64_t M, int64_t N, int64_t K, int tp, int mode, int epi, int dtype) {
+  if (dtype != QW_BF16) return 0;
+  const Plan p = plan_bf16(M, N, K, tp, mode);
+  if (!p.swap) return 0;
+  if (p.splits > 1 || epi == QW_EPI_SILU_MUL) return size_t(p.splits) * size_t(M) * size_t(N) * sizeof(float);
+  return 0;
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+unsigned int take_tc_timeouts() {
+  unsigned int v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, tc::g_tc_timeout, sizeof(v));
+  if (v) cudaMemcpyToSymbol(tc::g_tc_timeout, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace qw
+
+using namespace qw;
+
+static int gemm_check(const void* A, const void* W, void* C, int64_t M, int64_t N, int64_t K, int tp, int mode,
+                      int epi, int dtype, const char* who) {
+  if (dtype != QW_BF16 && dtype != QW_F32) return set_error(QW_ERR_DTYPE, "%s: dtype %d", who, dtype);
+  if (M < 0 || N <= 0 || K <= 0 || tp <= 0) return set_error(QW_ERR_INVALID_ARG, "%s: bad sizes", who);
+  if (mode != QW_GEMM_COLUMN && mode != QW_GEMM_ROW_REDUCE)
+    return set_error(QW_ERR_INVALID_ARG, "%s: mode %d", who, mode);
+  if (epi != QW_EPI_NONE && epi != QW_EPI_SILU_MUL) return set_error(QW_ERR_INVALID_ARG, "%s: epilogue %d", who, epi);
+  if (epi == QW_EPI_SILU_MUL && mode != QW_GEMM_COLUMN)
+    return set_error(QW_ERR_INVALID_ARG, "%s: SiluAndMul needs the column (gate_up) layout", who);
+  if (mode == QW_GEMM_ROW_REDUCE && K % tp) return set_error(QW_ERR_SHAPE, "%s: K=%lld %% tp=%d", who, (long long)K, tp);
+  if (mode == QW_GEMM_COLUMN && N % tp) return set_error(QW_ERR_SHAPE, "%s: N=%lld %% tp=%d", who, (long long)N, tp);
+  if (epi == QW_EPI_SILU_MUL && (N % (2 * tp)))
+    return set_error(QW_ERR_SHAPE, "%s: gate_up width %lld not 2*tp*I_l", who, (long long)N);
+  if (M == 0) return QW_OK;
+  if (!A || !W || !C) return set_error(QW_ERR_INVALID_ARG, "%s: null pointer", who);
+  if (dtype == QW_BF16) {
+    const int64_t Kl = mode == QW_GEMM_ROW_REDUCE ? K / tp : K;
+    if (K % 8 || Kl % 8) return set_error(QW_ERR_SHAPE, "%s: K and K/tp must be multiples of 8", who);
+    if (N % 16) return set_error(QW_ERR_SHAPE, "%s: N must be a multiple of 16", who);
+    if (epi == QW_EPI_SILU_MUL && ((N / 2 / tp) % 8))
+      return set_error(QW_ERR_SHAPE, "%s: I/tp must be a multiple of 8", who);
+    if (!al16(A) || !al16(W) || !al16(C)) return set_error(QW_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", who);
+    if (N > (int64_t(1) << 31) || M > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+      return set_error(QW_ERR_SHAPE, "%s: dimension too large", who);
+  }
+  return -1;  // continue
+}
+
+extern "C" size_t qw_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int tp, int mode, int epilogue, int dtype) {
+  if (M <= 0 || N <= 0 || K <= 0 || tp <= 0) return 0;
+  return gemm_ws(M, N, K, tp, mode, epilogue, dtype);
+}
+
+extern "C" int qw_gemm(const void* A, const void* W, void* C, int64_t M, int64_t N, int64_t K, int tp, int mode,
+                       int epilogue, void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+  int rc = gemm_check(A, W, C, M, N, K, tp, mode, epilogue, dtype, "qw_gemm");
+  if (rc >= 0) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == QW_F32) {
+    const int64_t Nout = epilogue == QW_EPI_SILU_MUL ? N / 2 : N;
+    const int64_t Kl = mode == QW_GEMM_ROW_REDUCE ? K / tp : K;
+    dim3 grid(unsigned((Nout + 15) / 16), unsigned((M + 15) / 16));
+    gemm_f32_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(A), static_cast<const float*>(W),
+                                          static_cast<float*>(C), M, Nout, N, K, Kl, mode == QW_GEMM_ROW_REDUCE,
+                                          epilogue == QW_EPI_SILU_MUL, epilogue == QW_EPI_SILU_MUL ? N / 2 / tp : 0);
+    return check_launch("gemm_f32_kernel");
+  }
+  return gemm_bf16(static_cast<const bf16*>(A), static_cast<const bf16*>(W), static_cast<bf16*>(C), M, N, K, tp,
+                   mode, epilogue, workspace, workspace_bytes, st);
+}
+
+extern "C" size_t qw_lm_head_workspace_size(int64_t n_out, int64_t V, int64_t H, int tp, int dtype) {
+  if (n_out <= 0 || V <= 0 || H <= 0) return 0;
+  const size_t es = dtype == QW_BF16 ? 2 : 4;
+  const size_t rows = (size_t(n_out) * size_t(H) * es + 255) / 256 * 256;
+  return rows + gemm_ws(n_out, V, H, tp > 0 ? tp : 1, QW_GEMM_COLUMN, QW_EPI_NONE, dtype);
+}
+
+extern "C" int qw_lm_head(const void* hidden, int64_t T, const int32_t* last_idx, int64_t n_out, const void* table,
+                          int64_t V, int64_t H, int tp, void* logits, int64_t* next_tokens, void* workspace,
+                          size_t workspace_bytes, int dtype, void* stream) {
+  if (dtype != QW_BF16 && dtype != QW_F32) return set_error(QW_ERR_DTYPE, "qw_lm_head: dtype %d", dtype);
+  if (T < 0 || n_out < 0 || V <= 0 || H <= 0 || tp <= 0) return set_error(QW_ERR_INVALID_ARG, "qw_lm_head: bad sizes");
+  if (V % tp) return set_error(QW_ERR_SHAPE, "qw_lm_head: V=%lld %% tp=%d", (long long)V, tp);
+  if (n_out == 0) return QW_OK;
+  if (!hidden || !table || !logits) return set_error(QW_ERR_INVALID_ARG, "qw_lm_head: null pointer");
+  if (!last_idx && n_out > T) return set_error(QW_ERR_SHAPE, "qw_lm_head: n_out > T without last_idx");
+  const size_t es = dtype == QW_BF16 ? 2 : 4;
+  const size_t need = qw_lm_head_workspace_size(n_out, V, H, tp, dtype);
+  const void* x = hidden;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  size_t rows = 0;
+  if (last_idx) {
+    if (!ws || workspace_bytes < need) return set_error(QW_ERR_WORKSPACE, "qw_lm_head: workspace of %zu bytes needed", need);
+    if ((H * int64_t(es)) % 16 || !al16(hidden)) return set_error(QW_ERR_INVALID_ARG, "qw_lm_head: H rows must be 16-byte");
+    rows = (size_t(n_out) * size_t(H) * es + 255) / 256 * 256;
+    int rc = dtype == QW_BF16 ? launch_gather_rows<bf16>(hidden, T, last_idx, n_out, H, ws, st)
+                              : launch_gather_rows<float>(hidden, T, last_idx, n_out, H, ws, st);
+    if (rc) return rc;
+    x = ws;
+  }
+  // each vocab shard r projects onto its rows [r*V/tp, (r+1)*V/tp) and writes
+  // logit columns [r*V/tp, (r+1)*V/tp): with the shards stacked in one table
+  // that is a single column-split GEMM over the whole vocab
+  int rc = qw_gemm(x, table, logits, n_out, V, H, 1, QW_GEMM_COLUMN, QW_EPI_NONE, ws ? ws + rows : nullptr,
+                   workspace_bytes > rows ? workspace_bytes - rows : 0, dtype, stream);
+  if (rc) return rc;
+  if (next_tokens) return qw_argmax(logits, n_out, V, next_tokens, dtype, stream);
+  return QW_OK;
+}

@@ -1,0 +1,44 @@
+// Error reporting, version and device-error query of the libqw C ABI.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <string>
+
+#include "common.cuh"
+
+namespace qw {
+
+static thread_local std::string g_last_error;
+
+int set_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return QW_OK;
+}
+
+// defined next to the kernels that own a bounded-wait error word
+unsigned int take_tc_timeouts();
+
+}  // namespace qw
+
+extern "C" int qw_abi_version(void) { return 1; }
+
+extern "C" const char* qw_last_error_string(void) { return qw::g_last_error.c_str(); }
+
+extern "C" int qw_device_error(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return qw::set_error(QW_ERR_CUDA, "qw_device_error: %s", cudaGetErrorString(e));
+  const unsigned int t = qw::take_tc_timeouts();
+  if (t) return qw::set_error(QW_ERR_TIMEOUT, "a tensor-core pipeline wait timed out (code 0x%x)", t);
+  return QW_OK;
+}

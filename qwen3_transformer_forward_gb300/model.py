@@ -1,0 +1,246 @@
+"""Qwen3 forward pass on one GB300: sequences the libqw entry points.
+
+This module does no arithmetic of the model.  It owns device buffers (via
+PyTorch), builds the tensor-parallel weight layout at load time, and calls
+one C-ABI entry point per step, in the order of Qwen3DecoderLayer.forward
+and Qwen3ForCausalLM ([SK] §1, §8; [VH] §3-§5):
+
+  embed (vocab-parallel) -> per layer:
+     add+RMSNorm -> QKV GEMM (column) -> QK-norm + RoPE + KV store ->
+     attention (prefill: varlen causal; decode: over the cache) ->
+     o_proj GEMM (row, shard sum) -> add+RMSNorm ->
+     gate_up GEMM (column) with fused SiluAndMul -> down GEMM (row, shard sum)
+  -> final add+RMSNorm -> lm_head (last token per sequence in prefill) -> argmax
+
+Sources: [VH] devpress "vocab 切 / head 切"; [TP] devpress tensor-parallel
+maths; [SK] AIInfraGuide "3.3 模型骨架与核心算子".
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional
+
+import torch
+
+from . import _lib as L
+
+
+# ----------------------------------------------------------------------------
+# load-time layout (the weight_loader of the parallel Linear family)
+# ----------------------------------------------------------------------------
+
+@dataclass
+class LayerParams:
+    qkv: torch.Tensor        # [tp * (nh/tp + 2 nkv/tp) * hd, H]   shard r = [q_r; k_r; v_r]
+    o: torch.Tensor          # [tp, H, nh/tp * hd]                 shard r = input columns of its heads
+    gate_up: torch.Tensor    # [tp * 2 * I/tp, H]                  shard r = [gate_r; up_r]
+    down: torch.Tensor       # [tp, H, I/tp]
+    input_ln: torch.Tensor
+    post_ln: torch.Tensor
+    q_norm: torch.Tensor
+    k_norm: torch.Tensor
+
+
+@dataclass
+class ModelParams:
+    embed: torch.Tensor      # [V, H]; tied with the lm_head ([SK] §8); shard r = row block r
+    layers: List[LayerParams]
+    final_norm: torch.Tensor
+
+
+def shard_layer(shape, ck: Dict[str, torch.Tensor], layer: int, device) -> LayerParams:
+    """Places one layer's checkpoint tensors into the per-shard stacked layout.
+
+    QKVParallelLinear / MergedColumnParallelLinear narrow each checkpoint
+    tensor along the output dim per shard; RowParallelLinear narrows along the
+    input dim ([SK] §5, [TP] §3-§4).  Runs once at load time.
+    """
+    tp, hd = shape.tp, shape.head_dim
+    nh_l, nkv_l, i_l = shape.n_heads // tp, shape.n_kv_heads // tp, shape.intermediate // tp
+    p = f"layer{layer}."
+    wq, wk, wv = ck[p + "q_proj"], ck[p + "k_proj"], ck[p + "v_proj"]
+    wg, wu = ck[p + "gate_proj"], ck[p + "up_proj"]
+    qkv = torch.cat([torch.cat([wq.narrow(0, r * nh_l * hd, nh_l * hd), wk.narrow(0, r * nkv_l * hd, nkv_l * hd),
+                                wv.narrow(0, r * nkv_l * hd, nkv_l * hd)]) for r in range(tp)])
+    gate_up = torch.cat([torch.cat([wg.narrow(0, r * i_l, i_l), wu.narrow(0, r * i_l, i_l)]) for r in range(tp)])
+    wo, wd = ck[p + "o_proj"], ck[p + "down_proj"]
+    o = torch.stack([wo.narrow(1, r * nh_l * hd, nh_l * hd) for r in range(tp)])
+    down = torch.stack([wd.narrow(1, r * i_l, i_l) for r in range(tp)])
+
+    def dev(t):
+        return t.contiguous().to(device)
+    return LayerParams(dev(qkv), dev(o), dev(gate_up), dev(down), dev(ck[p + "input_layernorm"]),
+                       dev(ck[p + "post_attention_layernorm"]), dev(ck[p + "q_norm"]), dev(ck[p + "k_norm"]))
+
+
+def load_params(shape, seed: int = 0, device="cuda", n_layers: Optional[int] = None, gen_device=None) -> ModelParams:
+    """Random-init parameters of the given shape from the seeded generator."""
+    import seeded_inputs as si
+    gen_device = gen_device or device
+    nl = shape.n_layers if n_layers is None else n_layers
+    embed = si.checkpoint_tensor(shape, "embed_tokens", seed, gen_device).to(device)
+    layers = []
+    for l in range(nl):
+        ck = {n: si.checkpoint_tensor(shape, n, seed, gen_device)
+              for n in si.weight_names(l) + [f"layer{l}.{x}" for x in
+                                             ("input_layernorm", "post_attention_layernorm", "q_norm", "k_norm")]}
+        layers.append(shard_layer(shape, ck, l, device))
+        del ck
+    final = si.checkpoint_tensor(shape, "norm", seed, gen_device).to(device)
+    return ModelParams(embed, layers, final)
+
+
+# ----------------------------------------------------------------------------
+# batch descriptions (the get_context() fields, [SK] §6-§7)
+# ----------------------------------------------------------------------------
+
+@dataclass
+class PrefillContext:
+    ids: torch.Tensor            # int64 [T]
+    positions: torch.Tensor      # int64 [T]
+    cu_seqlens: torch.Tensor     # int32 [S+1]
+    slot_mapping: torch.Tensor   # int64 [T]
+    seq_base: torch.Tensor       # int32 [S]
+    last_idx: torch.Tensor       # int32 [S]
+    max_seqlen: int
+
+    @property
+    def n_tokens(self):
+        return self.ids.shape[0]
+
+
+@dataclass
+class DecodeContext:
+    ids: torch.Tensor            # int64 [B]
+    positions: torch.Tensor      # int64 [B]
+    context_lens: torch.Tensor   # int32 [B]
+    slot_mapping: torch.Tensor   # int64 [B]
+    seq_base: torch.Tensor       # int32 [B]
+    max_context: int
+
+    @property
+    def n_tokens(self):
+        return self.ids.shape[0]
+
+
+def to_device_prefill(b, device="cuda") -> PrefillContext:
+    return PrefillContext(b.ids.to(device), b.positions.to(device), b.cu_seqlens.to(device),
+                          b.slot_mapping.to(device), b.seq_base.to(device), b.last_idx.to(device), max(b.seq_lens))
+
+
+def to_device_decode(b, device="cuda") -> DecodeContext:
+    return DecodeContext(b.ids.to(device), b.positions.to(device), b.context_lens.to(device),
+                         b.slot_mapping.to(device), b.seq_base.to(device), int(b.context_lens.max()))
+
+
+# ----------------------------------------------------------------------------
+# the forward pass
+# ----------------------------------------------------------------------------
+
+class Qwen3Forward:
+    """Device buffers + the sequence of libqw calls for prefill and decode."""
+
+    def __init__(self, shape, params: ModelParams, max_tokens: int, num_slots: int, max_seqs: int,
+                 max_context: int, device="cuda", kv_caches=None):
+        self.m = shape
+        self.p = params
+        self.device = device
+        dt = params.embed.dtype
+        self.dtype = dt
+        H, I, hd = shape.hidden, shape.intermediate, shape.head_dim
+        tp = shape.tp
+        self.qkv_width = tp * (shape.n_heads // tp + 2 * (shape.n_kv_heads // tp)) * hd
+        T = max_tokens
+        z = lambda *s: torch.empty(*s, dtype=dt, device=device)  # noqa: E731
+        self.h = z(T, H)
+        self.res = z(T, H)
+        self.y = z(T, H)
+        self.qkv = z(T, self.qkv_width)
+        self.q = z(T, shape.n_heads * hd)
+        self.attn = z(T, shape.n_heads * hd)
+        self.act = z(T, I)
+        self.gate_up = z(T, 2 * I)
+        self.logits = z(max_seqs if max_seqs > 0 else T, shape.vocab)
+        self.next_tokens = torch.empty(max(max_seqs, T), dtype=torch.int64, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        nl = len(params.layers)
+        if kv_caches is None:
+            self.k_cache = [torch.zeros(num_slots, shape.n_kv_heads, hd, dtype=dt, device=device) for _ in range(nl)]
+            self.v_cache = [torch.zeros(num_slots, shape.n_kv_heads, hd, dtype=dt, device=device) for _ in range(nl)]
+        else:
+            self.k_cache, self.v_cache = kv_caches
+        self.cos_sin = L.rope_cos_sin_table(shape.max_position, hd, shape.rope_theta).to(device)
+        ws = 0
+        for (M, N, K, mode, epi) in self._gemm_shapes(T) + self._gemm_shapes(max(max_seqs, 1)):
+            ws = max(ws, L.gemm_workspace_size(M, N, K, tp, mode, epi, dt))
+        ws = max(ws, L.attention_decode_workspace_size(max(max_seqs, 1), max_context, shape.n_heads, hd))
+        ws = max(ws, L.lm_head_workspace_size(max(max_seqs, 1), shape.vocab, H, tp, dt))
+        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
+        self.scale = hd ** -0.5
+
+    def _gemm_shapes(self, M):
+        m = self.m
+        return [(M, self.qkv_width, m.hidden, L.QW_GEMM_COLUMN, L.QW_EPI_NONE),
+                (M, m.hidden, m.n_heads * m.head_dim, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE),
+                (M, 2 * m.intermediate, m.hidden, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL),
+                (M, m.hidden, m.intermediate, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE)]
+
+    # -- one decoder layer ([SK] §1) ------------------------------------------
+    def _layer(self, l: int, T: int, ctx, first: bool, decode: bool, stream=None):
+        m, p = self.m, self.p.layers[l]
+        tp = m.tp
+        h, res, y = self.h[:T], self.res[:T], self.y[:T]
+        L.add_rmsnorm(h, None if first else res, res, p.input_ln, m.eps, y, stream)
+        qkv = self.qkv[:T]
+        L.gemm(y, p.qkv, qkv, self.qkv_width, tp, L.QW_GEMM_COLUMN, L.QW_EPI_NONE, self.workspace, stream)
+        q = self.q[:T]
+        L.qkv_norm_rope_store_kv(qkv, m.n_heads, m.n_kv_heads, m.head_dim, tp, ctx.positions, self.cos_sin,
+                                 p.q_norm, p.k_norm, m.eps, ctx.slot_mapping, self.k_cache[l], self.v_cache[l], q,
+                                 self.err, stream)
+        attn = self.attn[:T]
+        if decode:
+            L.attention_decode(q, self.k_cache[l], self.v_cache[l], ctx.context_lens, ctx.seq_base, ctx.max_context,
+                               m.n_heads, m.n_kv_heads, m.head_dim, self.scale, attn, self.workspace, stream)
+        else:
+            L.attention_prefill(q, self.k_cache[l], self.v_cache[l], ctx.cu_seqlens, ctx.cu_seqlens, ctx.seq_base,
+                                ctx.max_seqlen, m.n_heads, m.n_kv_heads, m.head_dim, self.scale, attn, stream)
+        L.gemm(attn, p.o, h, m.hidden, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, self.workspace, stream)
+        L.add_rmsnorm(h, res, res, p.post_ln, m.eps, y, stream)
+        act = self.act[:T]
+        L.gemm(y, p.gate_up, act, 2 * m.intermediate, tp, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL, self.workspace,
+               stream)
+        L.gemm(act, p.down, h, m.hidden, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, self.workspace, stream)
+
+    def run_layers(self, ctx, decode: bool, hidden_in: Optional[torch.Tensor] = None, final_norm: bool = True,
+                   stream=None):
+        """embedding (or hidden_in) -> layers -> optional final add+RMSNorm; returns the hidden buffer view."""
+        m = self.m
+        T = ctx.n_tokens
+        if hidden_in is None:
+            L.embed_vocab(ctx.ids, self.p.embed, m.tp, self.h[:T], self.err, stream)
+        else:
+            self.h[:T].copy_(hidden_in)
+        for l in range(len(self.p.layers)):
+            self._layer(l, T, ctx, l == 0, decode, stream)
+        if not final_norm:
+            return self.h[:T], self.res[:T]
+        if len(self.p.layers) == 0:
+            L.add_rmsnorm(self.h[:T], None, None, self.p.final_norm, m.eps, self.y[:T], stream)
+        else:
+            L.add_rmsnorm(self.h[:T], self.res[:T], None, self.p.final_norm, m.eps, self.y[:T], stream)
+        return self.y[:T]
+
+    def compute_logits(self, hidden: torch.Tensor, last_idx: Optional[torch.Tensor], n_out: int, stream=None):
+        """ParallelLMHead ([SK] §6): last token of each sequence in prefill, then greedy argmax."""
+        logits = self.logits[:n_out]
+        nt = self.next_tokens[:n_out]
+        L.lm_head(hidden, last_idx, n_out, self.p.embed, self.m.tp, logits, nt, self.workspace, stream)
+        return logits, nt
+
+    def prefill(self, ctx: PrefillContext, stream=None):
+        hidden = self.run_layers(ctx, decode=False, stream=stream)
+        return self.compute_logits(hidden, ctx.last_idx, ctx.last_idx.shape[0], stream)
+
+    def decode(self, ctx: DecodeContext, stream=None):
+        hidden = self.run_layers(ctx, decode=True, stream=stream)
+        return self.compute_logits(hidden, None, ctx.n_tokens, stream)

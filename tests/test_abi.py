@@ -1,0 +1,99 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library builds with nvcc for sm_103a, loads, exports every entry point
+declared in include/qw.h, rejects bad arguments before touching the device,
+and its host-only RoPE table equals the oracle's bit for bit.
+"""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from qwen3_transformer_forward_gb300 import _lib as L
+from qwen3_transformer_forward_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return L.load()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "qw.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qw_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    syms = declared_symbols()
+    assert len(syms) >= 15
+    for s in syms:
+        assert hasattr(lib, s), s
+    # and the binding declares a signature for each of them
+    assert set(syms) == set(L.SIGNATURES), set(syms) ^ set(L.SIGNATURES)
+
+
+def test_abi_version(lib):
+    assert lib.qw_abi_version() == 1
+
+
+def test_argument_errors_are_reported_before_launch(lib):
+    fake = C.c_void_p(16)   # never dereferenced: every call below fails its host-side check
+    # V not divisible by tp
+    assert lib.qw_embed_vocab(fake, 4, fake, 10, 64, 4, fake, None, L.QW_BF16, None) == L.QW_ERR_SHAPE
+    assert "not divisible" in lib.qw_last_error_string().decode()
+    # bad dtype
+    assert lib.qw_embed_vocab(fake, 4, fake, 8, 64, 2, fake, None, 7, None) == L.QW_ERR_DTYPE
+    # zero tokens is a no-op
+    assert lib.qw_embed_vocab(None, 0, fake, 8, 64, 2, fake, None, L.QW_BF16, None) == L.QW_OK
+    # null pointer
+    assert lib.qw_add_rmsnorm(None, None, None, fake, 1e-6, 3, 64, fake, L.QW_BF16, None) == L.QW_ERR_INVALID_ARG
+    # misaligned
+    assert lib.qw_add_rmsnorm(C.c_void_p(18), None, None, fake, 1e-6, 3, 64, fake, L.QW_BF16,
+                              None) == L.QW_ERR_INVALID_ARG
+    # heads not divisible by tp
+    assert lib.qw_qkv_norm_rope_store_kv(fake, 3, 16, 8, 128, 3, fake, fake, 64, fake, fake, 1e-6, fake, fake, fake,
+                                         10, fake, None, L.QW_BF16, None) == L.QW_ERR_SHAPE
+    # gemm: K/tp not a multiple of 8, SiluAndMul with the row layout, N not a multiple of 16
+    assert lib.qw_gemm(fake, fake, fake, 4, 64, 36, 2, L.QW_GEMM_ROW_REDUCE, 0, None, 0, L.QW_BF16,
+                       None) == L.QW_ERR_SHAPE
+    assert lib.qw_gemm(fake, fake, fake, 4, 64, 64, 1, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_SILU_MUL, None, 0, L.QW_BF16,
+                       None) == L.QW_ERR_INVALID_ARG
+    assert lib.qw_gemm(fake, fake, fake, 4, 60, 64, 1, L.QW_GEMM_COLUMN, 0, None, 0, L.QW_BF16,
+                       None) == L.QW_ERR_SHAPE
+    # attention: bf16 path needs head_dim 128; decode group must be 1/2/4/8
+    assert lib.qw_attention_prefill(fake, fake, fake, fake, fake, None, 2, 8, 16, 8, 64, 0.1, fake, L.QW_BF16,
+                                    None) == L.QW_ERR_SHAPE
+    assert lib.qw_attention_decode(fake, fake, fake, fake, fake, 2, 8, 12, 4, 128, 0.1, fake, None, 0, L.QW_BF16,
+                                   None) == L.QW_ERR_SHAPE
+    # decode without the workspace it needs
+    need = lib.qw_attention_decode_workspace_size(8, 4096, 16, 128)
+    assert need > 0
+    assert lib.qw_attention_decode(fake, fake, fake, fake, fake, 8, 4096, 16, 8, 128, 0.1, fake, None, 0,
+                                   L.QW_BF16, None) == L.QW_ERR_WORKSPACE
+    # lm_head: V not divisible by tp
+    assert lib.qw_lm_head(fake, 4, None, 4, fake, 10, 64, 4, fake, None, None, 0, L.QW_BF16,
+                          None) == L.QW_ERR_SHAPE
+
+
+@pytest.mark.parametrize("max_pos,d,theta", [(64, 16, 1e6), (2200, 128, 1e6), (300, 8, 1e4)])
+def test_rope_table_equals_oracle(lib, max_pos, d, theta):
+    t = L.rope_cos_sin_table(max_pos, d, theta).double().numpy()
+    cos_t, sin_t = O.rope_cos_sin(max_pos, d, theta)
+    assert np.array_equal(t[:, : d // 2], cos_t)
+    assert np.array_equal(t[:, d // 2:], sin_t)
+
+
+def test_workspace_sizes(lib):
+    # prefill-sized GEMMs need no workspace; decode-sized ones split K and do
+    assert L.gemm_workspace_size(2048, 4096, 1024, 2, L.QW_GEMM_COLUMN, 0, torch.bfloat16) == 0
+    assert L.gemm_workspace_size(8, 1024, 3072, 2, L.QW_GEMM_ROW_REDUCE, 0, torch.bfloat16) > 0
+    assert L.gemm_workspace_size(8, 1024, 3072, 2, L.QW_GEMM_ROW_REDUCE, 0, torch.float32) == 0
+    assert L.attention_decode_workspace_size(64, 2048, 16, 128) > 0

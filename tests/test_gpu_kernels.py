@@ -1,0 +1,420 @@
+"""Per-kernel parity of the CUDA path with the CPU oracle (needs a GB300).
+
+Every call goes through the C ABI (ctypes binding).  Inputs come from the
+seeded generator; expected values come from the oracle only.  Sizes span
+several tiles plus a ragged tail.
+
+Tolerances:
+  * integer/index/copy work (embedding, KV placement, v cache, argmax): bit-exact;
+  * bf16 outputs of one rounding step: within 1 bf16 ulp of the oracle (the
+    oracle rounds its float64 result once; the kernel rounds its fp32 result
+    once, so they differ only where the two sit on opposite sides of a
+    rounding midpoint); GEMMs add the fp32 accumulation error, at most
+    (K/16) * 2^-24 * sum_k |a_k w_k| for K/16 sequential fp32 additions of
+    16-term tensor-core products, taken as 2^-18 * sum_k |a_k w_k| (K <= 4096);
+  * attention: P is rounded to bf16 before the PV product on the tensor
+    cores, so |err| <= 2 ulp(|out|) + 2^-9 * max|v| (derived below);
+  * fp32 paths: normwise relative error <= 1e-5.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import seeded_inputs as si
+from tests._util import assert_within_ulps, bf16_ulp, normwise_rel_err, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from qwen3_transformer_forward_gb300 import build
+    build.build()
+    from qwen3_transformer_forward_gb300 import _lib
+    _lib.load()
+    return _lib
+
+
+def dev(t):
+    return t.to("cuda")
+
+
+def sync_ok(L):
+    torch.cuda.synchronize()
+    L.device_error()
+
+
+# ----------------------------------------------------------------------------
+# embedding
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("tp", [1, 2, 4])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_embed_vocab_bit_exact(L, tp, dtype):
+    m = si.ModelShape(vocab=4096, hidden=1024 if dtype == "bf16" else 64, n_heads=1, n_kv_heads=1, head_dim=8,
+                      intermediate=8, n_layers=0, dtype=dtype)
+    table = si.checkpoint_tensor(m, "embed_tokens")
+    ids = si.embed_ids(m, 1000, 0.05)
+    ids[:8] = torch.tensor([0, 1023, 1024, 2047, 2048, 3071, 3072, 4095])
+    ids[10] = -1          # out of range: zero row and one error count each
+    ids[11] = 4096
+    ids[12] = 10 ** 9
+    out = torch.full((1000, m.hidden), 7.0, dtype=table.dtype, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L.embed_vocab(dev(ids), dev(table), tp, out, err)
+    sync_ok(L)
+    ref = O.vocab_parallel_embedding(ids.numpy(), table.double().numpy(), tp)
+    assert np.array_equal(to_np(out), ref)
+    assert int(err.item()) == 3
+    assert np.all(to_np(out)[[10, 11, 12]] == 0)
+
+
+def test_embed_empty_is_noop(L):
+    out = torch.full((1, 64), 3.0, device="cuda")
+    L.embed_vocab(torch.zeros(0, dtype=torch.int64, device="cuda"), torch.zeros(8, 64, device="cuda"), 2, out[:0])
+    sync_ok(L)
+    assert torch.all(out == 3.0)
+
+
+# ----------------------------------------------------------------------------
+# add + RMSNorm
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,H", [("bf16", 1024), ("bf16", 2048), ("bf16", 64), ("f32", 64), ("f32", 1024)])
+@pytest.mark.parametrize("with_res", [False, True])
+def test_add_rmsnorm(L, dtype, H, with_res):
+    T = 37
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    x = si.normal(0, "t.x", (T, H), 1.0, dtype)
+    r = si.normal(0, "t.r", (T, H), 2.0, dtype)
+    g = (si.normal(0, "t.g", (H,), 0.2, "f32") + 1.0).to(dt)
+    y = torch.empty(T, H, dtype=dt, device="cuda")
+    res_buf = dev(r.clone())
+    L.add_rmsnorm(dev(x), res_buf if with_res else None, res_buf, dev(g), 1e-6, y)
+    sync_ok(L)
+    if with_res:
+        ry, rres = O.add_rms_norm(x.double().numpy(), r.double().numpy(), g.double().numpy(), 1e-6, dtype)
+    else:
+        ry = O.rms_norm(x.double().numpy(), g.double().numpy(), 1e-6, dtype)
+        rres = x.double().numpy()
+    if dtype == "bf16":
+        assert np.array_equal(to_np(res_buf), rres)          # residual add: one rounding of an exact sum
+        assert_within_ulps(to_np(y), ry, 1.0, 0.98, "rmsnorm y")
+    else:
+        assert normwise_rel_err(to_np(res_buf), rres) <= 1e-6
+        assert normwise_rel_err(to_np(y), ry) <= 1e-5
+
+
+# ----------------------------------------------------------------------------
+# QK-norm + RoPE + KV store
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,nh,nkv,hd,tp", [("bf16", 16, 8, 128, 2), ("bf16", 16, 8, 128, 1),
+                                                ("bf16", 8, 2, 64, 2), ("f32", 4, 2, 16, 2)])
+def test_qkv_norm_rope_store_kv(L, dtype, nh, nkv, hd, tp):
+    T, num_slots = 45, 80
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    m = si.ModelShape(vocab=64, hidden=64, n_heads=nh, n_kv_heads=nkv, head_dim=hd, intermediate=64, n_layers=1,
+                      tp=tp, dtype=dtype, max_position=3000)
+    width = tp * (nh // tp + 2 * (nkv // tp)) * hd
+    qkv = si.normal(0, "t.qkv", (T, width), 1.0, dtype)
+    qg = (si.normal(0, "t.qg", (hd,), 0.2, "f32") + 1.0).to(dt)
+    kg = (si.normal(0, "t.kg", (hd,), 0.2, "f32") + 1.0).to(dt)
+    pos = si.uniform_int(0, "t.pos", (T,), 0, 2176)
+    pos[0] = 0
+    pos[1] = 2175
+    perm = torch.randperm(num_slots, generator=torch.Generator().manual_seed(0))[:T]
+    slots = perm.clone()
+    slots[[3, 17, 40]] = -1
+    sentinel = 5.0
+    kc = torch.full((num_slots, nkv, hd), sentinel, dtype=dt, device="cuda")
+    vc = torch.full((num_slots, nkv, hd), sentinel, dtype=dt, device="cuda")
+    q_out = torch.empty(T, nh * hd, dtype=dt, device="cuda")
+    cs = L.rope_cos_sin_table(m.max_position, hd, m.rope_theta)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L.qkv_norm_rope_store_kv(dev(qkv), nh, nkv, hd, tp, dev(pos), dev(cs), dev(qg), dev(kg), m.eps, dev(slots),
+                             kc, vc, q_out, err)
+    sync_ok(L)
+    assert int(err.item()) == 0
+    # oracle: per shard, split the merged block, norm, rope, store
+    cos_t, sin_t = O.rope_cos_sin(m.max_position, hd, m.rope_theta)
+    nh_l, nkv_l = nh // tp, nkv // tp
+    x = qkv.double().numpy()
+    wr = (nh_l + 2 * nkv_l) * hd
+    qs, ks, vs = [], [], []
+    for r in range(tp):
+        blk = x[:, r * wr:(r + 1) * wr]
+        qs.append(blk[:, : nh_l * hd].reshape(T, nh_l, hd))
+        ks.append(blk[:, nh_l * hd:(nh_l + nkv_l) * hd].reshape(T, nkv_l, hd))
+        vs.append(blk[:, (nh_l + nkv_l) * hd:].reshape(T, nkv_l, hd))
+    q = np.concatenate(qs, 1)
+    k = np.concatenate(ks, 1)
+    v = np.concatenate(vs, 1)
+    q = O.apply_rope(O.rms_norm(q, qg.double().numpy(), m.eps, dtype), pos.numpy(), cos_t, sin_t, dtype)
+    k = O.apply_rope(O.rms_norm(k, kg.double().numpy(), m.eps, dtype), pos.numpy(), cos_t, sin_t, dtype)
+    cache = O.KVCache(1, num_slots, nkv, hd, 1)
+    cache.k[0][0][:] = sentinel
+    cache.v[0][0][:] = sentinel
+    cache.store(0, 0, k, v, slots.numpy())
+    kc_n, vc_n = to_np(kc), to_np(vc)
+    assert np.array_equal(vc_n, cache.v[0][0])                  # placement + bit copy of v
+    untouched = np.ones(num_slots, bool)
+    untouched[slots.numpy()[slots.numpy() >= 0]] = False
+    assert np.all(kc_n[untouched] == sentinel)                 # slots not in the mapping keep the sentinel
+    if dtype == "bf16":
+        # two roundings (norm, rope): a midpoint flip at the first can move the second by one ulp
+        assert_within_ulps(kc_n, cache.k[0][0], 2.0, 0.97, "k cache")
+        assert_within_ulps(to_np(q_out).reshape(T, nh, hd), q, 2.0, 0.97, "q")
+    else:
+        assert normwise_rel_err(kc_n, cache.k[0][0]) <= 1e-5
+        assert normwise_rel_err(to_np(q_out).reshape(T, nh, hd), q) <= 1e-5
+
+
+# ----------------------------------------------------------------------------
+# GEMMs (tcgen05 for bf16, CUDA cores for f32)
+# ----------------------------------------------------------------------------
+
+def _gemm_abs_bound(A, W, mode, epi, tp):
+    """2^-18 * sum_k |a_k||w_k| per output (for SiluAndMul: scaled by the gate/up sizes)."""
+    a = np.abs(A.double().numpy())
+    w = np.abs(W.double().numpy())
+    if mode == 1:
+        w = np.concatenate([w[r] for r in range(tp)], axis=1)
+    s = a @ w.T
+    if epi == 1:
+        i_l = w.shape[0] // 2 // tp
+        g = np.concatenate([s[:, r * 2 * i_l:r * 2 * i_l + i_l] for r in range(tp)], -1)
+        u = np.concatenate([s[:, r * 2 * i_l + i_l:(r + 1) * 2 * i_l] for r in range(tp)], -1)
+        s = (g + u) * (1.0 + g + u)
+    return 2.0 ** -18 * s
+
+
+def _gemm_ref(A, W, mode, epi, tp, dtype):
+    a = A.double().numpy()
+    w = W.double().numpy()
+    if mode == 0:
+        if epi == 0:
+            return O.linear(a, w, dtype)
+        N = w.shape[0]
+        i_l = N // 2 // tp
+        outs = []
+        for r in range(tp):
+            gu = O.linear(a, w[r * 2 * i_l:(r + 1) * 2 * i_l], dtype)
+            outs.append(O.silu_and_mul(gu, dtype))
+        return np.concatenate(outs, -1)
+    # row reduce: W is [tp, N, K/tp] -> full [N, K]
+    full = np.concatenate([w[r] for r in range(tp)], axis=1)
+    k_l = full.shape[1] // tp
+    return O.row_parallel_linear([a[:, r * k_l:(r + 1) * k_l] for r in range(tp)], full, tp, dtype)
+
+
+GEMM_CASES = [
+    # M,    N,    K,    tp, mode, epi
+    (300, 784, 1024, 1, 0, 0),      # prefill path: 3 M tiles (ragged), 4 N tiles (last one 16 wide)
+    (129, 4096, 1024, 2, 0, 0),
+    (300, 1024, 2048, 2, 1, 0),     # row split, shard sum in the accumulator
+    (257, 1024, 3072, 2, 1, 0),
+    (200, 1536, 1024, 2, 0, 1),     # gate_up + SiluAndMul, I/tp = 384 (3 tiles per shard)
+    (130, 1000 // 8 * 16, 1000, 1, 0, 0),   # K not a multiple of 64 (TMA zero fill)
+    (1, 4096, 1024, 2, 0, 0),       # decode path (swapped operands, split K)
+    (7, 1024, 2048, 2, 1, 0),
+    (16, 6144, 1024, 2, 0, 1),
+    (33, 1024, 3072, 2, 1, 0),
+    (64, 4096, 1024, 1, 0, 0),
+    (64, 6144, 1024, 1, 0, 1),
+    (65, 1024, 2048, 2, 1, 0),      # first size on the prefill path
+]
+
+
+@pytest.mark.parametrize("M,N,K,tp,mode,epi", GEMM_CASES)
+def test_gemm_bf16(L, M, N, K, tp, mode, epi):
+    A = si.normal(0, f"g.A{M}.{K}", (M, K), 1.0, "bf16")
+    if mode == 1:
+        W = si.normal(0, f"g.W{N}.{K}", (tp, N, K // tp), 0.02, "bf16")
+    else:
+        W = si.normal(0, f"g.W{N}.{K}", (N, K), 0.02, "bf16")
+    n_out = N // 2 if epi == 1 else N
+    C = torch.full((M, n_out), 123.0, dtype=torch.bfloat16, device="cuda")
+    ws_n = L.gemm_workspace_size(M, N, K, tp, mode, epi, torch.bfloat16)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+    L.gemm(dev(A), dev(W), C, N, tp, mode, epi, ws)
+    sync_ok(L)
+    ref = _gemm_ref(A, W, mode, epi, tp, "bf16")
+    # fp32 accumulation vs exact: one rounding each; SiluAndMul adds one more
+    assert_within_ulps(to_np(C), ref, 1.0 if epi == 0 else 2.0, 0.9, f"gemm {M}x{N}x{K} mode{mode} epi{epi}",
+                       atol=_gemm_abs_bound(A, W, mode, epi, tp))
+
+
+@pytest.mark.parametrize("M,N,K,tp,mode,epi", [(32, 128, 64, 2, 0, 0), (32, 64, 64, 2, 1, 0),
+                                               (32, 256, 64, 2, 0, 1), (5, 512, 64, 1, 0, 0)])
+def test_gemm_f32(L, M, N, K, tp, mode, epi):
+    A = si.normal(0, "gf.A", (M, K), 1.0, "f32")
+    W = si.normal(0, "gf.W", (tp, N, K // tp) if mode == 1 else (N, K), 0.02, "f32")
+    n_out = N // 2 if epi == 1 else N
+    C = torch.empty(M, n_out, dtype=torch.float32, device="cuda")
+    L.gemm(dev(A), dev(W), C, N, tp, mode, epi)
+    sync_ok(L)
+    assert normwise_rel_err(to_np(C), _gemm_ref(A, W, mode, epi, tp, "f32")) <= 1e-5
+
+
+def test_silu_mul(L):
+    T, I, tp = 33, 3072, 2
+    x = si.normal(0, "t.gu", (T, 2 * I), 2.0, "bf16")
+    out = torch.empty(T, I, dtype=torch.bfloat16, device="cuda")
+    L.silu_mul(dev(x), out, tp)
+    sync_ok(L)
+    xn = x.double().numpy()
+    i_l = I // tp
+    ref = np.concatenate([O.silu_and_mul(xn[:, r * 2 * i_l:(r + 1) * 2 * i_l], "bf16") for r in range(tp)], -1)
+    assert_within_ulps(to_np(out), ref, 1.0, 0.98, "silu_mul")
+
+
+# ----------------------------------------------------------------------------
+# attention
+# ----------------------------------------------------------------------------
+
+def _attn_tol(ref, v):
+    # P in bf16 (relative error <= 2^-9 per weight) -> |sum p_j v_j| error <= 2^-9 * max|v|,
+    # plus the final rounding of out (<= 1 ulp) and fp32 accumulation slack (1 ulp)
+    return 2.0 * bf16_ulp(ref) + 2.0 ** -9 * np.max(np.abs(v)) + 1e-6
+
+
+@pytest.mark.parametrize("seq_lens", [[1, 77, 200, 129], [512, 512], [3]])
+def test_attention_prefill_bf16_from_cache(L, seq_lens):
+    nh, nkv, hd = 16, 8, 128
+    b = si.prefill_batch(si.QWEN3_0_6B, seq_lens, extra_capacity=5)
+    T = sum(seq_lens)
+    q = si.normal(0, "a.q", (T, nh, hd), 1.0, "bf16")
+    k = si.normal(0, "a.k", (T, nkv, hd), 1.0, "bf16")
+    v = si.normal(0, "a.v", (T, nkv, hd), 1.0, "bf16")
+    kc = torch.zeros(b.num_slots, nkv, hd, dtype=torch.bfloat16)
+    vc = torch.zeros(b.num_slots, nkv, hd, dtype=torch.bfloat16)
+    kc[b.slot_mapping] = k
+    vc[b.slot_mapping] = v
+    out = torch.empty(T, nh * hd, dtype=torch.bfloat16, device="cuda")
+    cu = dev(b.cu_seqlens)
+    L.attention_prefill(dev(q), dev(kc), dev(vc), cu, cu, dev(b.seq_base), max(seq_lens), nh, nkv, hd,
+                        hd ** -0.5, out)
+    sync_ok(L)
+    ref = O.attention_prefill(q.double().numpy(), k.double().numpy(), v.double().numpy(), b.cu_seqlens.numpy(),
+                              hd ** -0.5, "bf16")
+    got = to_np(out).reshape(T, nh, hd)
+    err = np.abs(got - ref)
+    assert np.all(err <= _attn_tol(ref, v.double().numpy())), float(err.max())
+    assert float(np.mean(err)) < 2e-3
+
+
+def test_attention_prefill_packed_and_prefix(L):
+    # packed keys (no seq_base) and a query suffix over a longer key prefix
+    nh, nkv, hd = 16, 8, 128
+    Lk, Lq = [150, 40], [10, 40]
+    k = si.normal(0, "a.pk", (sum(Lk), nkv, hd), 1.0, "bf16")
+    v = si.normal(0, "a.pv", (sum(Lk), nkv, hd), 1.0, "bf16")
+    q = si.normal(0, "a.pq", (sum(Lq), nh, hd), 1.0, "bf16")
+    cu_k = torch.tensor([0, 150, 190], dtype=torch.int32)
+    cu_q = torch.tensor([0, 10, 50], dtype=torch.int32)
+    out = torch.empty(sum(Lq), nh * hd, dtype=torch.bfloat16, device="cuda")
+    L.attention_prefill(dev(q), dev(k), dev(v), dev(cu_q), dev(cu_k), None, 40, nh, nkv, hd, hd ** -0.5, out)
+    sync_ok(L)
+    # the oracle's full causal attention over the whole key sequence, keeping the last Lq rows
+    qd, kd, vd = q.double().numpy(), k.double().numpy(), v.double().numpy()
+    refs = []
+    for s in range(2):
+        a, bq = int(cu_q[s]), int(cu_q[s + 1])
+        ka, kb = int(cu_k[s]), int(cu_k[s + 1])
+        qfull = np.zeros((kb - ka, nh, hd))
+        qfull[(kb - ka) - (bq - a):] = qd[a:bq]
+        o = O.attention_prefill(qfull, kd[ka:kb], vd[ka:kb], [0, kb - ka], hd ** -0.5, "bf16")
+        refs.append(o[(kb - ka) - (bq - a):])
+    ref = np.concatenate(refs)
+    got = to_np(out).reshape(-1, nh, hd)
+    assert np.all(np.abs(got - ref) <= _attn_tol(ref, vd))
+
+
+def test_attention_prefill_f32(L):
+    nh, nkv, hd = 4, 2, 16
+    b = si.prefill_batch(si.TINY, [16, 16])
+    T = 32
+    q = si.normal(0, "af.q", (T, nh, hd), 1.0, "f32")
+    k = si.normal(0, "af.k", (T, nkv, hd), 1.0, "f32")
+    v = si.normal(0, "af.v", (T, nkv, hd), 1.0, "f32")
+    out = torch.empty(T, nh * hd, dtype=torch.float32, device="cuda")
+    cu = dev(b.cu_seqlens)
+    L.attention_prefill(dev(q), dev(k), dev(v), cu, cu, dev(b.seq_base), 16, nh, nkv, hd, hd ** -0.5, out)
+    sync_ok(L)
+    ref = O.attention_prefill(q.double().numpy(), k.double().numpy(), v.double().numpy(), b.cu_seqlens.numpy(),
+                              hd ** -0.5, "f32")
+    assert normwise_rel_err(to_np(out).reshape(T, nh, hd), ref) <= 1e-5
+
+
+@pytest.mark.parametrize("ctx", [[1, 63, 64, 65, 700], [2048] * 3 + [256], [2176] * 8])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_attention_decode(L, ctx, dtype):
+    nh, nkv, hd = 16, 8, 128
+    B = len(ctx)
+    cap = [c + 3 for c in ctx]
+    base = np.concatenate([[0], np.cumsum(cap)[:-1]]).astype(np.int32)
+    S = int(sum(cap))
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    kc = si.normal(0, "d.k", (S, nkv, hd), 1.0, dtype)
+    vc = si.normal(0, "d.v", (S, nkv, hd), 1.0, dtype)
+    q = si.normal(0, "d.q", (B, nh, hd), 1.0, dtype)
+    out = torch.empty(B, nh * hd, dtype=dt, device="cuda")
+    ws = torch.empty(max(L.attention_decode_workspace_size(B, max(ctx), nh, hd), 16), dtype=torch.uint8,
+                     device="cuda")
+    L.attention_decode(dev(q), dev(kc), dev(vc), dev(torch.tensor(ctx, dtype=torch.int32)),
+                       dev(torch.tensor(base)), max(ctx), nh, nkv, hd, hd ** -0.5, out, ws)
+    sync_ok(L)
+    kd, vd = kc.double().numpy(), vc.double().numpy()
+    ref = O.attention_decode(q.double().numpy(), [kd[base[b]:base[b] + ctx[b]] for b in range(B)],
+                             [vd[base[b]:base[b] + ctx[b]] for b in range(B)], hd ** -0.5, dtype)
+    got = to_np(out).reshape(B, nh, hd)
+    if dtype == "bf16":
+        # fp32 accumulation over up to a few thousand keys plus exp2/normalisation
+        # rounding: absolute slack 2^-16 * max|v| on top of the two output ulps
+        assert_within_ulps(got, ref, 2.0, 0.8, "decode attention", atol=2.0 ** -16 * np.max(np.abs(vd)))
+    else:
+        assert normwise_rel_err(got, ref) <= 1e-5
+
+
+# ----------------------------------------------------------------------------
+# lm_head and argmax
+# ----------------------------------------------------------------------------
+
+def test_argmax_lowest_index_on_ties(L):
+    x = si.normal(0, "am.x", (5, 4096), 1.0, "bf16")
+    x[0, 100] = 9.0
+    x[0, 50] = 9.0          # tie: 50 wins
+    x[1, 4095] = 9.0
+    x[2, :] = -1.0          # all equal: 0 wins
+    out = torch.empty(5, dtype=torch.int64, device="cuda")
+    L.argmax(dev(x), out)
+    sync_ok(L)
+    assert list(out.cpu().numpy()) == list(O.greedy(x.double().numpy()))
+    assert out[0].item() == 50 and out[2].item() == 0
+
+
+@pytest.mark.parametrize("tp", [1, 2, 4])
+@pytest.mark.parametrize("n_out", [3, 300])
+def test_lm_head_with_last_token_select(L, tp, n_out):
+    V, H, T = 4096, 1024, 400
+    table = si.normal(0, "lm.W", (V, H), 0.02, "bf16")
+    hidden = si.normal(0, "lm.h", (T, H), 1.0, "bf16")
+    last = si.uniform_int(0, "lm.idx", (n_out,), 0, T).to(torch.int32)
+    logits = torch.empty(n_out, V, dtype=torch.bfloat16, device="cuda")
+    nt = torch.empty(n_out, dtype=torch.int64, device="cuda")
+    ws = torch.empty(L.lm_head_workspace_size(n_out, V, H, tp, torch.bfloat16), dtype=torch.uint8, device="cuda")
+    L.lm_head(dev(hidden), dev(last), n_out, dev(table), tp, logits, nt, ws)
+    sync_ok(L)
+    m = si.QWEN3_0_6B.replace(vocab=V)
+    cu = None
+    ref = O.compute_logits(m, table.double().numpy(), hidden.double().numpy()[last.numpy()], tp, cu)
+    got = to_np(logits)
+    acc = 2.0 ** -18 * (np.abs(hidden.double().numpy()[last.numpy()]) @ np.abs(table.double().numpy()).T)
+    assert_within_ulps(got, ref, 1.0, 0.9, "logits", atol=acc)
+    assert np.array_equal(nt.cpu().numpy(), O.greedy(got))     # argmax of the kernel's own logits: exact
