@@ -154,7 +154,8 @@ int qw_qkv_norm_rope_store_kv(const void* qkv, int64_t T, int n_heads, int n_kv_
  *       keys 0 .. that position.
  *   out dtype [Tq, nh, hd];  q head h reads kv head h / (nh / nkv).
  *   max_seqlen_q: upper bound of Lq_s (sizes the grid).
- * Rules: nh % nkv == 0; hd == 128 for bf16, hd <= 64 for f32.
+ * Rules: nh % nkv == 0; hd == 128 (bf16, tensor-core path) or hd <= 64 (bf16 or
+ * f32, CUDA-core path).
  */
 int qw_attention_prefill(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
                          const int32_t* cu_seqlens_k, const int32_t* seq_base, int n_seqs,
@@ -170,7 +171,8 @@ int qw_attention_prefill(const void* q, const void* k, const void* v, const int3
  *   out dtype [B, nh, hd]
  *   workspace: device scratch of qw_attention_decode_workspace_size(...) bytes
  *   (split-KV partial results); may be NULL only when that size is 0.
- * Rules: nh % nkv == 0, nh/nkv <= 8, hd == 128 (bf16 or f32).
+ * Rules: nh % nkv == 0; hd == 128 with nh/nkv in {1, 2, 4, 8} (split-KV path),
+ * or hd <= 64 (one warp per (sequence, q head), no workspace); bf16 or f32.
  */
 int qw_attention_decode(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* context_lens, const int32_t* seq_base, int B, int max_context,

@@ -398,10 +398,11 @@ def load_layer(m, layer: int, seed: int = 0) -> LayerWeights:
         "input_layernorm", "post_attention_layernorm", "q_norm", "k_norm")])
 
 
-def load_weights(m, seed: int = 0, layers: Optional[int] = None, lazy: bool = False) -> ModelWeights:
+def load_weights(m, seed: int = 0, layers: Optional[int] = None, lazy: bool = False,
+                 with_embed: bool = True) -> ModelWeights:
     from seeded_inputs import checkpoint_tensor as ct
     n = m.n_layers if layers is None else layers
-    embed = _np(ct(m, "embed_tokens", seed))
+    embed = _np(ct(m, "embed_tokens", seed)) if with_embed else None
     lw = [None] * n if lazy else [load_layer(m, l, seed) for l in range(n)]
     return ModelWeights(embed, lw, _np(ct(m, "norm", seed)))
 

@@ -224,34 +224,47 @@ __global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// fp32 prefill (small head_dim): one warp per (query token, q head)
+// small head_dim (<= 64), any dtype: one warp per (query token, q head).
+// Prefill: query i of sequence s sees keys 0 .. Lk - Lq + i.  Decode
+// (ctx_lens != nullptr): one query per sequence that sees ctx_lens[s] keys.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) attn_prefill_f32_kernel(
-    const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+template <typename T>
+__global__ void __launch_bounds__(128) attn_small_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, const int32_t* __restrict__ seq_base,
-    int n_seqs, int max_q, int nh, int nkv, int hd, float scale, float* __restrict__ out) {
+    const int32_t* __restrict__ ctx_lens, int n_seqs, int max_q, int nh, int nkv, int hd, float scale,
+    T* __restrict__ out) {
   const int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= int64_t(n_seqs) * max_q * nh) return;
   const int s = int(w / (int64_t(max_q) * nh));
   const int i = int((w / nh) % max_q);
   const int h = int(w % nh);
-  const int Lq = cu_q[s + 1] - cu_q[s], Lk = cu_k[s + 1] - cu_k[s];
+  int Lq, Lk;
+  int64_t t;
+  if (ctx_lens != nullptr) {
+    Lq = 1;
+    Lk = ctx_lens[s];
+    t = s;
+  } else {
+    Lq = cu_q[s + 1] - cu_q[s];
+    Lk = cu_k[s + 1] - cu_k[s];
+    t = int64_t(cu_q[s]) + i;
+  }
   if (i >= Lq) return;
-  const int64_t t = int64_t(cu_q[s]) + i;
   const int last = Lk - Lq + i;   // last visible key
   const int g = h / (nh / nkv);
   const int64_t kbase = seq_base != nullptr ? int64_t(seq_base[s]) : int64_t(cu_k[s]);
-  const float* qv = q + (t * nh + h) * int64_t(hd);
+  const T* qv = q + (t * nh + h) * int64_t(hd);
   float m = -INFINITY, l = 0.0f;
   float acc0 = 0.0f, acc1 = 0.0f;   // lane owns d = lane and d = lane + 32
   for (int j0 = 0; j0 <= last; j0 += 32) {
     const int j = j0 + lane;
     float sc = -INFINITY;
     if (j <= last) {
-      const float* kv = k + ((kbase + j) * nkv + g) * int64_t(hd);
+      const T* kv = k + ((kbase + j) * nkv + g) * int64_t(hd);
       float d = 0.0f;
-      for (int e = 0; e < hd; ++e) d = fmaf(qv[e], kv[e], d);
+      for (int e = 0; e < hd; ++e) d = fmaf(to_f(qv[e]), to_f(kv[e]), d);
       sc = d * scale;
     }
     const float mt = warp_max(sc);
@@ -263,15 +276,27 @@ __global__ void __launch_bounds__(128) attn_prefill_f32_kernel(
     acc1 *= alpha;
     for (int jj = 0; jj < 32 && j0 + jj <= last; ++jj) {
       const float pj = __shfl_sync(0xffffffffu, p, jj);
-      const float* vv = v + ((kbase + j0 + jj) * nkv + g) * int64_t(hd);
-      if (lane < hd) acc0 = fmaf(pj, vv[lane], acc0);
-      if (lane + 32 < hd) acc1 = fmaf(pj, vv[lane + 32], acc1);
+      const T* vv = v + ((kbase + j0 + jj) * nkv + g) * int64_t(hd);
+      if (lane < hd) acc0 = fmaf(pj, to_f(vv[lane]), acc0);
+      if (lane + 32 < hd) acc1 = fmaf(pj, to_f(vv[lane + 32]), acc1);
     }
     m = m_new;
   }
-  float* o = out + (t * nh + h) * int64_t(hd);
-  if (lane < hd) o[lane] = acc0 / l;
-  if (lane + 32 < hd) o[lane + 32] = acc1 / l;
+  T* o = out + (t * nh + h) * int64_t(hd);
+  const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+  if (lane < hd) o[lane] = from_f<T>(acc0 * inv);
+  if (lane + 32 < hd) o[lane + 32] = from_f<T>(acc1 * inv);
+}
+
+template <typename T>
+int launch_attn_small(const void* q, const void* k, const void* v, const int32_t* cu_q, const int32_t* cu_k,
+                      const int32_t* seq_base, const int32_t* ctx_lens, int n_seqs, int max_q, int nh, int nkv,
+                      int hd, float scale, void* out, cudaStream_t st) {
+  const int64_t threads = int64_t(n_seqs) * max_q * nh * 32;
+  attn_small_kernel<T><<<unsigned((threads + 127) / 128), 128, 0, st>>>(
+      static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), cu_q, cu_k, seq_base, ctx_lens,
+      n_seqs, max_q, nh, nkv, hd, scale, static_cast<T*>(out));
+  return check_launch("attn_small_kernel");
 }
 
 // ---------------------------------------------------------------------------
@@ -510,15 +535,13 @@ extern "C" int qw_attention_prefill(const void* q, const void* k, const void* v,
   if (n_seqs < 0 || max_seqlen_q < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0)
     return set_error(QW_ERR_INVALID_ARG, "qw_attention_prefill: bad sizes");
   if (n_heads % n_kv_heads) return set_error(QW_ERR_SHAPE, "qw_attention_prefill: nh %% nkv != 0");
-  if (dtype == QW_BF16 && head_dim != 128)
-    return set_error(QW_ERR_SHAPE, "qw_attention_prefill: bf16 path needs head_dim 128 (got %d)", head_dim);
-  if (dtype == QW_F32 && head_dim > 64)
-    return set_error(QW_ERR_SHAPE, "qw_attention_prefill: f32 path needs head_dim <= 64 (got %d)", head_dim);
+  if (!(head_dim == 128 && dtype == QW_BF16) && head_dim > 64)
+    return set_error(QW_ERR_SHAPE, "qw_attention_prefill: head_dim %d (bf16 needs 128 or <= 64, f32 <= 64)", head_dim);
   if (n_seqs == 0 || max_seqlen_q == 0) return QW_OK;
   if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out)
     return set_error(QW_ERR_INVALID_ARG, "qw_attention_prefill: null pointer");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (dtype == QW_BF16) {
+  if (dtype == QW_BF16 && head_dim == 128) {
     static bool configured = false;
     if (!configured) {
       cudaError_t e = cudaFuncSetAttribute(attn_prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -532,15 +555,15 @@ extern "C" int qw_attention_prefill(const void* q, const void* k, const void* v,
         cu_seqlens_k, seq_base, n_heads, n_kv_heads, scale * kLog2e, static_cast<bf16*>(out));
     return check_launch("attn_prefill_bf16_kernel");
   }
-  const int64_t threads = int64_t(n_seqs) * max_seqlen_q * n_heads * 32;
-  attn_prefill_f32_kernel<<<unsigned((threads + 127) / 128), 128, 0, st>>>(
-      static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), cu_seqlens_q,
-      cu_seqlens_k, seq_base, n_seqs, max_seqlen_q, n_heads, n_kv_heads, head_dim, scale, static_cast<float*>(out));
-  return check_launch("attn_prefill_f32_kernel");
+  if (dtype == QW_BF16)
+    return launch_attn_small<bf16>(q, k, v, cu_seqlens_q, cu_seqlens_k, seq_base, nullptr, n_seqs, max_seqlen_q,
+                                   n_heads, n_kv_heads, head_dim, scale, out, st);
+  return launch_attn_small<float>(q, k, v, cu_seqlens_q, cu_seqlens_k, seq_base, nullptr, n_seqs, max_seqlen_q,
+                                  n_heads, n_kv_heads, head_dim, scale, out, st);
 }
 
 extern "C" size_t qw_attention_decode_workspace_size(int B, int max_context, int n_heads, int head_dim) {
-  if (B <= 0 || max_context <= 0 || n_heads <= 0 || head_dim <= 0) return 0;
+  if (B <= 0 || max_context <= 0 || n_heads <= 0 || head_dim != 128) return 0;
   const DecodePlan p = decode_plan(B, max_context, 0);
   if (p.splits <= 1) return 0;
   return size_t(B) * n_heads * p.splits * (size_t(head_dim) + 2) * sizeof(float);
@@ -574,13 +597,22 @@ extern "C" int qw_attention_decode(const void* q, const void* k_cache, const voi
   if (dtype != QW_BF16 && dtype != QW_F32) return set_error(QW_ERR_DTYPE, "qw_attention_decode: dtype %d", dtype);
   if (B < 0 || max_context < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0)
     return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode: bad sizes");
-  if (n_heads % n_kv_heads || head_dim != 128)
-    return set_error(QW_ERR_SHAPE, "qw_attention_decode: needs nh %% nkv == 0 and head_dim 128");
+  if (n_heads % n_kv_heads || (head_dim != 128 && head_dim > 64))
+    return set_error(QW_ERR_SHAPE, "qw_attention_decode: needs nh %% nkv == 0 and head_dim 128 or <= 64");
   const int G = n_heads / n_kv_heads;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return set_error(QW_ERR_SHAPE, "qw_attention_decode: group %d", G);
+  if (head_dim == 128 && G != 1 && G != 2 && G != 4 && G != 8)
+    return set_error(QW_ERR_SHAPE, "qw_attention_decode: group %d", G);
   if (B == 0) return QW_OK;
   if (!q || !k_cache || !v_cache || !context_lens || !seq_base || !out)
     return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode: null pointer");
+  if (head_dim != 128) {
+    cudaStream_t st0 = static_cast<cudaStream_t>(stream);
+    return dtype == QW_BF16
+               ? launch_attn_small<bf16>(q, k_cache, v_cache, nullptr, nullptr, seq_base, context_lens, B, 1, n_heads,
+                                         n_kv_heads, head_dim, scale, out, st0)
+               : launch_attn_small<float>(q, k_cache, v_cache, nullptr, nullptr, seq_base, context_lens, B, 1,
+                                          n_heads, n_kv_heads, head_dim, scale, out, st0);
+  }
   const DecodePlan p = decode_plan(B, max_context, n_kv_heads);
   const size_t need = qw_attention_decode_workspace_size(B, max_context, n_heads, head_dim);
   if (need && (!workspace || workspace_bytes < need))

@@ -17,6 +17,7 @@ maths; [SK] AIInfraGuide "3.3 模型骨架与核心算子".
 """
 from __future__ import annotations
 
+import contextlib
 from dataclasses import dataclass, field
 from typing import Dict, List, Optional
 
@@ -159,7 +160,6 @@ class Qwen3Forward:
         self.q = z(T, shape.n_heads * hd)
         self.attn = z(T, shape.n_heads * hd)
         self.act = z(T, I)
-        self.gate_up = z(T, 2 * I)
         self.logits = z(max_seqs if max_seqs > 0 else T, shape.vocab)
         self.next_tokens = torch.empty(max(max_seqs, T), dtype=torch.int64, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
@@ -177,6 +177,12 @@ class Qwen3Forward:
         ws = max(ws, L.lm_head_workspace_size(max(max_seqs, 1), shape.vocab, H, tp, dt))
         self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
         self.scale = hd ** -0.5
+        self.probe = None      # optional timing hook: probe(name, layer) -> context manager
+
+    def _around(self, name: str, layer: int):
+        if self.probe is None:
+            return contextlib.nullcontext()
+        return self.probe(name, layer)
 
     def _gemm_shapes(self, M):
         m = self.m
@@ -190,26 +196,37 @@ class Qwen3Forward:
         m, p = self.m, self.p.layers[l]
         tp = m.tp
         h, res, y = self.h[:T], self.res[:T], self.y[:T]
-        L.add_rmsnorm(h, None if first else res, res, p.input_ln, m.eps, y, stream)
+        ph = "decode" if decode else "prefill"
+        with self._around(f"{ph}.add_rmsnorm", l):
+            L.add_rmsnorm(h, None if first else res, res, p.input_ln, m.eps, y, stream)
         qkv = self.qkv[:T]
-        L.gemm(y, p.qkv, qkv, self.qkv_width, tp, L.QW_GEMM_COLUMN, L.QW_EPI_NONE, self.workspace, stream)
+        with self._around(f"{ph}.gemm_qkv", l):
+            L.gemm(y, p.qkv, qkv, self.qkv_width, tp, L.QW_GEMM_COLUMN, L.QW_EPI_NONE, self.workspace, stream)
         q = self.q[:T]
-        L.qkv_norm_rope_store_kv(qkv, m.n_heads, m.n_kv_heads, m.head_dim, tp, ctx.positions, self.cos_sin,
-                                 p.q_norm, p.k_norm, m.eps, ctx.slot_mapping, self.k_cache[l], self.v_cache[l], q,
-                                 self.err, stream)
+        with self._around(f"{ph}.qkv_norm_rope_store_kv", l):
+            L.qkv_norm_rope_store_kv(qkv, m.n_heads, m.n_kv_heads, m.head_dim, tp, ctx.positions, self.cos_sin,
+                                     p.q_norm, p.k_norm, m.eps, ctx.slot_mapping, self.k_cache[l], self.v_cache[l],
+                                     q, self.err, stream)
         attn = self.attn[:T]
-        if decode:
-            L.attention_decode(q, self.k_cache[l], self.v_cache[l], ctx.context_lens, ctx.seq_base, ctx.max_context,
-                               m.n_heads, m.n_kv_heads, m.head_dim, self.scale, attn, self.workspace, stream)
-        else:
-            L.attention_prefill(q, self.k_cache[l], self.v_cache[l], ctx.cu_seqlens, ctx.cu_seqlens, ctx.seq_base,
-                                ctx.max_seqlen, m.n_heads, m.n_kv_heads, m.head_dim, self.scale, attn, stream)
-        L.gemm(attn, p.o, h, m.hidden, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, self.workspace, stream)
-        L.add_rmsnorm(h, res, res, p.post_ln, m.eps, y, stream)
+        with self._around(f"{ph}.attention", l):
+            if decode:
+                L.attention_decode(q, self.k_cache[l], self.v_cache[l], ctx.context_lens, ctx.seq_base,
+                                   ctx.max_context, m.n_heads, m.n_kv_heads, m.head_dim, self.scale, attn,
+                                   self.workspace, stream)
+            else:
+                L.attention_prefill(q, self.k_cache[l], self.v_cache[l], ctx.cu_seqlens, ctx.cu_seqlens,
+                                    ctx.seq_base, ctx.max_seqlen, m.n_heads, m.n_kv_heads, m.head_dim, self.scale,
+                                    attn, stream)
+        with self._around(f"{ph}.gemm_o", l):
+            L.gemm(attn, p.o, h, m.hidden, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, self.workspace, stream)
+        with self._around(f"{ph}.add_rmsnorm", l):
+            L.add_rmsnorm(h, res, res, p.post_ln, m.eps, y, stream)
         act = self.act[:T]
-        L.gemm(y, p.gate_up, act, 2 * m.intermediate, tp, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL, self.workspace,
-               stream)
-        L.gemm(act, p.down, h, m.hidden, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, self.workspace, stream)
+        with self._around(f"{ph}.gemm_gate_up_silu", l):
+            L.gemm(y, p.gate_up, act, 2 * m.intermediate, tp, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL,
+                   self.workspace, stream)
+        with self._around(f"{ph}.gemm_down", l):
+            L.gemm(act, p.down, h, m.hidden, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, self.workspace, stream)
 
     def run_layers(self, ctx, decode: bool, hidden_in: Optional[torch.Tensor] = None, final_norm: bool = True,
                    stream=None):
@@ -217,7 +234,8 @@ class Qwen3Forward:
         m = self.m
         T = ctx.n_tokens
         if hidden_in is None:
-            L.embed_vocab(ctx.ids, self.p.embed, m.tp, self.h[:T], self.err, stream)
+            with self._around("embed_vocab", -1):
+                L.embed_vocab(ctx.ids, self.p.embed, m.tp, self.h[:T], self.err, stream)
         else:
             self.h[:T].copy_(hidden_in)
         for l in range(len(self.p.layers)):
@@ -234,7 +252,8 @@ class Qwen3Forward:
         """ParallelLMHead ([SK] §6): last token of each sequence in prefill, then greedy argmax."""
         logits = self.logits[:n_out]
         nt = self.next_tokens[:n_out]
-        L.lm_head(hidden, last_idx, n_out, self.p.embed, self.m.tp, logits, nt, self.workspace, stream)
+        with self._around("lm_head", -1):
+            L.lm_head(hidden, last_idx, n_out, self.p.embed, self.m.tp, logits, nt, self.workspace, stream)
         return logits, nt
 
     def prefill(self, ctx: PrefillContext, stream=None):
