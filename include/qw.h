@@ -181,6 +181,40 @@ int qw_attention_decode(const void* q, const void* k_cache, const void* v_cache,
 size_t qw_attention_decode_workspace_size(int B, int max_context, int n_heads, int head_dim);
 
 /*
+ * Decode attention that needs no workspace from the caller.  The pages have
+ * no counterpart: this entry point exists for callers that cannot allocate
+ * device memory themselves, such as a plugin that a host framework hands
+ * only input and output pointers (the framework owns the allocator), or a
+ * serving loop that sizes all device memory at start-up and forbids any
+ * later allocation.
+ *
+ * Same arguments, semantics and results as qw_attention_decode, minus the
+ * workspace: the split-KV partial results go to one fixed array of
+ * qw_attention_decode_static_scratch_bytes() bytes (2 MiB) that lives in the
+ * library's device image; every GPU that loads the library holds it until
+ * the process exits.  A batch whose split-KV scratch
+ * (qw_attention_decode_workspace_size) exceeds that size is rejected with
+ * QW_ERR_WORKSPACE and nothing is launched.  The call makes no allocation
+ * (no cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (the caller's current device), once; make that first call before
+ * any stream capture.
+ *
+ * All calls share the one array and it keeps whatever the last call left in
+ * it.  Nothing in it has to start at zero: every entry a call reads was
+ * written earlier in the same call.  Calls that can run at the same time on
+ * the GPU (on two streams, or from two host threads) race on the array and
+ * give wrong results: keep them on one stream.  Each process has its own
+ * copy of the array.
+ */
+int qw_attention_decode_static(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* context_lens, const int32_t* seq_base, int B, int max_context,
+                               int n_heads, int n_kv_heads, int head_dim, float scale, void* out, int dtype,
+                               void* stream);
+size_t qw_attention_decode_static_scratch_bytes(void);
+
+/*
  * Linear layer C = A W^T with the tensor-parallel layouts of [TP] §3 / [SK] §5.
  *   A dtype [M, K]
  *   QW_GEMM_COLUMN:     W dtype [N, K] (tp shards stacked along N; shard r = rows

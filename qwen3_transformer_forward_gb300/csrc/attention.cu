@@ -14,6 +14,8 @@
 // caller's workspace and a combine kernel merges them.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace qw {
@@ -635,4 +637,66 @@ extern "C" int qw_attention_decode(const void* q, const void* k_cache, const voi
   if (dtype == QW_BF16) { QW_DEC(bf16) }
   QW_DEC(float)
 #undef QW_DEC
+}
+
+// ===========================================================================
+// Decode attention without any device allocation by the caller.
+//
+// Some callers cannot hand this library a workspace: a plugin inside a host
+// framework that owns the device allocator and passes in only its input and
+// output pointers, or a serving loop that plans all device memory at
+// start-up and allows no allocation afterwards.  For them the split-KV
+// partial results live in one fixed array in this library's device image.
+// ===========================================================================
+namespace qw {
+namespace attn {
+
+constexpr size_t kStaticScratchBytes = size_t(2) << 20;   // 2 MiB on every GPU that loads the library
+static __device__ __align__(256) float g_decode_scratch[kStaticScratchBytes / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_scratch_mu;
+static void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_decode_scratch on the current device, looked up once per
+// device (host code only sees a host-side stand-in for the array's name).
+static int decode_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return set_error(QW_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return set_error(QW_ERR_CUDA, "cudaGetSymbolAddress(decode scratch): %s", cudaGetErrorString(e));
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return QW_OK;
+}
+
+}  // namespace attn
+}  // namespace qw
+
+extern "C" size_t qw_attention_decode_static_scratch_bytes(void) { return qw::attn::kStaticScratchBytes; }
+
+extern "C" int qw_attention_decode_static(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* context_lens, const int32_t* seq_base, int B,
+                                          int max_context, int n_heads, int n_kv_heads, int head_dim, float scale,
+                                          void* out, int dtype, void* stream) {
+  const size_t need = qw_attention_decode_workspace_size(B, max_context, n_heads, head_dim);
+  if (need > qw::attn::kStaticScratchBytes)
+    return set_error(QW_ERR_WORKSPACE,
+                     "qw_attention_decode_static: this batch needs %zu bytes of split-KV scratch but the fixed "
+                     "array holds %zu; pass a workspace to qw_attention_decode instead",
+                     need, qw::attn::kStaticScratchBytes);
+  void* ws = nullptr;
+  if (need > 0) {
+    const int rc = qw::attn::decode_scratch_address(&ws);
+    if (rc != QW_OK) return rc;
+  }
+  return qw_attention_decode(q, k_cache, v_cache, context_lens, seq_base, B, max_context, n_heads, n_kv_heads,
+                             head_dim, scale, out, ws, need > 0 ? qw::attn::kStaticScratchBytes : 0, dtype, stream);
 }
