@@ -55,6 +55,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-layers", type=int, default=4)
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)
+    ap.add_argument("--profile-window", action="store_true",
+                    help="after the timed region, run one more step between cudaProfilerStart/Stop "
+                         "(for ncu --profile-from-start off)")
     return ap.parse_args(argv)
 
 
@@ -391,6 +394,13 @@ def run_ours(args, rank, world, local):
                         "unit": kd["unit"], "frac": kd["frac"], "traffic": None,
                         "peak_source": f"{peaks['source']} ({'HBM copy' if kd['bound'] == 'hbm' else 'bf16 sustained'})",
                         "timing": probe_method}
+
+    if args.profile_window:
+        torch.cuda.synchronize()
+        torch.cuda.profiler.start()
+        wl.step()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
 
     e2e = None
     if not args.no_e2e:
