@@ -433,19 +433,10 @@ def count_launches(wl):
     from qwen3_transformer_forward_gb300 import _lib as L
     m = wl.m
     per_layer = 2 + 1 + 1 + 1 + 1 + 1 + 1   # 2 norms, qkv gemm, rope/kv, attention, o, gate_up, down
-    # decode extras: split-K reduce kernels for the 4 GEMMs + the attention combine
-    dec_extra = 0
-    B, T = wl.B, sum(wl.seq_lens)
-    for (M, N, K, mode, epi) in wl.fwd._gemm_shapes(B):
-        if L.gemm_workspace_size(M, N, K, m.tp, mode, epi, torch.bfloat16) > 0:
-            dec_extra += 1
-    if L.attention_decode_workspace_size(B, wl.max_context, m.n_heads, m.head_dim) > 0:
-        dec_extra += 1
-    lm_reduce = 1 if L.gemm_workspace_size(B, m.vocab, m.hidden, 1, L.QW_GEMM_COLUMN, L.QW_EPI_NONE,
-                                           torch.bfloat16) > 0 else 0
-    prefill = 1 + m.n_layers * per_layer + 1 + 3 + lm_reduce   # embed, layers, final norm, gather+gemm+argmax
-    lm_dec = 1 + lm_reduce + 1
-    decode = 1 + m.n_layers * (per_layer + dec_extra) + 1 + lm_dec
+    # split-K sums and the split-KV merge happen inside the GEMM and attention kernels
+    prefill = 1 + m.n_layers * per_layer + 1 + 3     # embed, layers, final norm, gather + gemm + argmax
+    lm_dec = 2                                       # gemm + argmax
+    decode = 1 + m.n_layers * per_layer + 1 + lm_dec
     return prefill + wl.S * decode
 
 

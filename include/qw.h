@@ -36,6 +36,12 @@
  *   - The return value is a qw_status.  qw_last_error_string() describes the
  *     last failure on the calling thread.
  *   - A size of zero tokens is a valid no-op and returns QW_OK.
+ *   - Workspaces (qw_attention_decode, qw_lm_head; sizes from the
+ *     *_workspace_size queries) begin with 64 KiB of completion counters
+ *     followed by scratch.  Zero-fill a workspace once when it is allocated;
+ *     every call leaves the counters at zero again, so one workspace serves
+ *     successive calls on one stream.  Calls that may run concurrently need
+ *     separate workspaces.
  *   - Device-side data errors (token id outside [0, V), position outside the
  *     RoPE table, slot outside the cache) do not fail the call: the affected
  *     row is zero (embedding, q) or not written (cache), and, when the
@@ -74,7 +80,7 @@ typedef enum {
   QW_EPI_SILU_MUL = 1     /* fused SiluAndMul on a merged gate_up output ([SK] §4) */
 } qw_epilogue;
 
-/* Version of this ABI (increments on any signature change). */
+/* Version of this ABI (increments on any signature change); this is version 2. */
 int qw_abi_version(void);
 
 /* Description of the last failure on the calling thread ("" if none). */
@@ -166,15 +172,16 @@ int qw_attention_prefill(const void* q, const void* k, const void* v, const int3
  * Decode attention over the KV cache (flash_attn_with_kvcache, [SK] §7.2):
  * one new query token per sequence, sees cache rows
  * seq_base[b] .. seq_base[b] + context_lens[b] - 1 (the token just stored included).
- *   q   dtype [B, nh, hd];  k_cache, v_cache dtype [num_slots, nkv, hd]
- *   context_lens, seq_base int32 [B];  max_context >= every context_lens[b]
+ *   q   dtype [B, nh, hd];  k_cache, v_cache dtype [num_slots, nkv, hd] (16-byte aligned)
+ *   context_lens, seq_base int32 [B];  max_context >= every context_lens[b];
+ *   every cache row read, seq_base[b] .. seq_base[b] + context_lens[b] - 1, < num_slots
  *   out dtype [B, nh, hd]
  *   workspace: device scratch of qw_attention_decode_workspace_size(...) bytes
  *   (split-KV partial results); may be NULL only when that size is 0.
  * Rules: nh % nkv == 0; hd == 128 with nh/nkv in {1, 2, 4, 8} (split-KV path),
  * or hd <= 64 (one warp per (sequence, q head), no workspace); bf16 or f32.
  */
-int qw_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+int qw_attention_decode(const void* q, const void* k_cache, const void* v_cache, int64_t num_slots,
                         const int32_t* context_lens, const int32_t* seq_base, int B, int max_context,
                         int n_heads, int n_kv_heads, int head_dim, float scale, void* out,
                         void* workspace, size_t workspace_bytes, int dtype, void* stream);
@@ -202,13 +209,15 @@ size_t qw_attention_decode_workspace_size(int B, int max_context, int n_heads, i
  * any stream capture.
  *
  * All calls share the one array and it keeps whatever the last call left in
- * it.  Nothing in it has to start at zero: every entry a call reads was
- * written earlier in the same call.  Calls that can run at the same time on
- * the GPU (on two streams, or from two host threads) race on the array and
- * give wrong results: keep them on one stream.  Each process has its own
- * copy of the array.
+ * it.  Its first 64 KiB are completion counters that must be zero when a
+ * call starts: the array is zero when the library is loaded and every call
+ * leaves its counters at zero; the rest of the array needs no clearing,
+ * because every value a call reads there was written earlier in the same
+ * call.  Calls that can run at the same time on the GPU (on two streams, or
+ * from two host threads) race on the array and give wrong results: keep
+ * them on one stream.  Each process has its own copy of the array.
  */
-int qw_attention_decode_static(const void* q, const void* k_cache, const void* v_cache,
+int qw_attention_decode_static(const void* q, const void* k_cache, const void* v_cache, int64_t num_slots,
                                const int32_t* context_lens, const int32_t* seq_base, int B, int max_context,
                                int n_heads, int n_kv_heads, int head_dim, float scale, void* out, int dtype,
                                void* stream);
@@ -225,7 +234,9 @@ size_t qw_attention_decode_static_scratch_bytes(void);
  *   QW_GEMM_ROW_REDUCE: W dtype [tp, N, K/tp] (shard r holds input columns
  *                       [r*K/tp, (r+1)*K/tp)); C[M, N] = sum_r A[:, shard r] W_r^T,
  *                       accumulated in fp32 across shards (the all_reduce), rounded once.
- *   workspace: qw_gemm_workspace_size(...) bytes (may be 0).
+ *   workspace: unused (pass NULL, 0); qw_gemm_workspace_size returns 0.  With
+ *   few tokens the K range is split over a thread-block cluster and the
+ *   partial sums are added in shared memory, in a fixed order.
  * Rules (bf16): K % 8 == 0, K/tp % 8 == 0 (row), N % 16 == 0 (N/2/tp % 8 == 0 for
  * SILU_MUL), A/W/C 16-byte aligned.  f32 runs on CUDA cores (exact fp32 FMA).
  */

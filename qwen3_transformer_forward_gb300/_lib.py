@@ -35,10 +35,11 @@ SIGNATURES = {
     "qw_qkv_norm_rope_store_kv": (C.c_int, [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _i64, _p, _p, _f32, _p, _p,
                                             _p, _i64, _p, _p, _i32, _p]),
     "qw_attention_prefill": (C.c_int, [_p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _i32, _p]),
-    "qw_attention_decode": (C.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _p, _sz, _i32,
-                                      _p]),
+    "qw_attention_decode": (C.c_int, [_p, _p, _p, _i64, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _p, _sz,
+                                      _i32, _p]),
     "qw_attention_decode_workspace_size": (C.c_size_t, [_i32, _i32, _i32, _i32]),
-    "qw_attention_decode_static": (C.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _i32, _p]),
+    "qw_attention_decode_static": (C.c_int, [_p, _p, _p, _i64, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _i32,
+                                             _p]),
     "qw_attention_decode_static_scratch_bytes": (C.c_size_t, []),
     "qw_gemm": (C.c_int, [_p, _p, _p, _i64, _i64, _i64, _i32, _i32, _i32, _p, _sz, _i32, _p]),
     "qw_gemm_workspace_size": (C.c_size_t, [_i64, _i64, _i64, _i32, _i32, _i32, _i32]),
@@ -176,7 +177,7 @@ def attention_decode(q, k_cache, v_cache, context_lens, seq_base, max_context, n
     B = q.shape[0]
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().qw_attention_decode(
-        _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"),
+        _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), k_cache.shape[0],
         _dev_ptr(context_lens, "context_lens"), _dev_ptr(seq_base, "seq_base"), B, max_context, n_heads, n_kv_heads,
         head_dim, scale, _dev_ptr(out, "out"), _dev_ptr(workspace, "workspace"), ws_bytes, dtype_code(q.dtype),
         _stream(stream)))
@@ -187,7 +188,7 @@ def attention_decode_static(q, k_cache, v_cache, context_lens, seq_base, max_con
     """Decode attention whose split-KV scratch is the library's fixed device array (no workspace)."""
     B = q.shape[0]
     _check(load().qw_attention_decode_static(
-        _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"),
+        _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), k_cache.shape[0],
         _dev_ptr(context_lens, "context_lens"), _dev_ptr(seq_base, "seq_base"), B, max_context, n_heads, n_kv_heads,
         head_dim, scale, _dev_ptr(out, "out"), dtype_code(q.dtype), _stream(stream)))
 

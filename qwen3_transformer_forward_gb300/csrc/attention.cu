@@ -11,12 +11,14 @@
 // (sequence, kv head, key chunk) and all q heads of that GQA group, so each
 // cached K/V byte is read once.  K/V tiles of 64 keys stream through shared
 // memory (cp.async double buffer); partial (m, l, o) per chunk go to the
-// caller's workspace and a combine kernel merges them.
+// caller's workspace and the last chunk of a (sequence, kv head) to finish
+// (an atomic completion counter) merges them and writes the output.
 #include <math.h>
 
 #include <mutex>
 
 #include "common.cuh"
+#include "tc_common.cuh"
 
 namespace qw {
 namespace attn {
@@ -319,11 +321,94 @@ __device__ __forceinline__ int dswz(int r, int e) {
   return r * DC_HD + ((c ^ (r & 7)) * EPC) + (e % EPC);
 }
 
+// Counts this chunk as done for its (sequence, kv head); the last chunk to
+// finish merges every chunk's (m, l, o) for the group's q heads, writes the
+// output and resets the counter.  All DC_THREADS threads call it.
+template <typename T, int G>
+__device__ __forceinline__ void decode_finish(const float* ws_o, const float* ws_ml, unsigned int* counters, int b,
+                                              int g, int nh, int nkv, int n_splits, T* out) {
+  constexpr int MAXS = 64;   // chunks per (sequence, kv head) merged through shared memory at a time
+  __shared__ int s_last;
+  __shared__ float s_w[G][MAXS];
+  __shared__ float s_scale[G];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0)
+    s_last = atomicAdd(counters + (int64_t(b) * nkv + g), 1u) == unsigned(n_splits - 1) ? 1 : 0;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int d = threadIdx.x;
+  const int64_t hrow0 = int64_t(b) * nh + int64_t(g) * G;
+  float acc[G];
+#pragma unroll
+  for (int j = 0; j < G; ++j) acc[j] = 0.0f;
+  float run_m[G], run_l[G];
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    run_m[j] = -INFINITY;
+    run_l[j] = 0.0f;
+  }
+  for (int s0 = 0; s0 < n_splits; s0 += MAXS) {
+    const int ns = min(MAXS, n_splits - s0);
+    // one warp per head: chunk maxima and weights relative to the running max
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int j = warp; j < G; j += DC_THREADS / 32) {
+      const int64_t hrow = hrow0 + j;
+      float ms[2], ls[2];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int sp = lane + 32 * u;
+        ms[u] = sp < ns ? __ldcg(ws_ml + 2 * (hrow * n_splits + s0 + sp)) : -INFINITY;
+        ls[u] = sp < ns ? __ldcg(ws_ml + 2 * (hrow * n_splits + s0 + sp) + 1) : 0.0f;
+        mx = fmaxf(mx, ms[u]);
+      }
+      mx = warp_max(mx);
+      const float m_new = fmaxf(run_m[j], mx);
+      const float m_use = m_new == -INFINITY ? 0.0f : m_new;
+      float lsum = 0.0f;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float w = ms[u] == -INFINITY ? 0.0f : exp2f(ms[u] - m_use);
+        if (lane + 32 * u < ns) s_w[j][lane + 32 * u] = w;
+        lsum += ls[u] * w;
+      }
+      lsum = warp_sum(lsum);
+      if (lane == 0) s_scale[j] = run_m[j] == -INFINITY ? 0.0f : exp2f(run_m[j] - m_use);
+      run_l[j] = run_l[j] * (run_m[j] == -INFINITY ? 0.0f : exp2f(run_m[j] - m_use)) + lsum;
+      run_m[j] = m_new;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int64_t hrow = hrow0 + j;
+      float o = acc[j] * s_scale[j];
+#pragma unroll 8
+      for (int sp = 0; sp < ns; ++sp) o += __ldcg(ws_o + (hrow * n_splits + s0 + sp) * DC_HD + d) * s_w[j][sp];
+      acc[j] = o;
+    }
+    __syncthreads();
+  }
+  // the warp that owned head j holds its running sum; publish it through shared memory
+  __shared__ float s_l[G];
+  {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int j = warp; j < G; j += DC_THREADS / 32)
+      if (lane == 0) s_l[j] = run_l[j];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < G; ++j) out[(hrow0 + j) * DC_HD + d] = from_f<T>(s_l[j] > 0.0f ? acc[j] / s_l[j] : 0.0f);
+  __syncthreads();
+  if (threadIdx.x == 0) counters[int64_t(b) * nkv + g] = 0u;
+}
+
 template <typename T, int G>
 __global__ void __launch_bounds__(DC_THREADS) attn_decode_kernel(
     const T* __restrict__ q, const T* __restrict__ kc, const T* __restrict__ vc, const int32_t* __restrict__ ctx_lens,
     const int32_t* __restrict__ seq_base, int nh, int nkv, float scale_log2, int chunk, int n_splits,
-    float* __restrict__ ws_o, float* __restrict__ ws_ml, T* __restrict__ out) {
+    float* __restrict__ ws_o, float* __restrict__ ws_ml, unsigned int* __restrict__ counters, T* __restrict__ out) {
   constexpr int EPC = 16 / sizeof(T);      // elements per 16-byte chunk
   constexpr int CPR = DC_HD / EPC;         // chunks per row
   extern __shared__ __align__(128) uint8_t smem[];
@@ -351,6 +436,7 @@ __global__ void __launch_bounds__(DC_THREADS) attn_decode_kernel(
         ws_ml[2 * idx] = -INFINITY;
         ws_ml[2 * idx + 1] = 0.0f;
       }
+      decode_finish<T, G>(ws_o, ws_ml, counters, b, g, nh, nkv, n_splits, out);
     } else {
       for (int i = tid; i < G * DC_HD; i += DC_THREADS)
         out[(int64_t(b) * nh + h0 + i / DC_HD) * DC_HD + i % DC_HD] = from_f<T>(0.0f);
@@ -478,28 +564,217 @@ __global__ void __launch_bounds__(DC_THREADS) attn_decode_kernel(
       }
     }
   }
+  if (n_splits > 1) decode_finish<T, G>(ws_o, ws_ml, counters, b, g, nh, nkv, n_splits, out);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(DC_HD) attn_decode_combine_kernel(const float* __restrict__ ws_o,
-                                                                    const float* __restrict__ ws_ml, int n_splits,
-                                                                    T* __restrict__ out) {
-  const int64_t hrow = blockIdx.x;
-  const int d = threadIdx.x;
-  float M = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, ws_ml[2 * (hrow * n_splits + s)]);
-  float L = 0.0f, o = 0.0f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < n_splits; ++s) {
-      const int64_t idx = hrow * n_splits + s;
-      const float ms = ws_ml[2 * idx];
-      if (ms == -INFINITY) continue;
-      const float w = exp2f(ms - M);
-      L += ws_ml[2 * idx + 1] * w;
-      o += ws_o[idx * DC_HD + d] * w;
+// ---------------------------------------------------------------------------
+// decode, bf16: tensor-core split-KV.  One CTA of 4 warps per (chunk of keys,
+// kv head, sequence).  K/V tiles of 64 keys arrive by TMA (3-D map over the
+// cache [slot][kv head][dim], two 64-dim boxes with 128-byte swizzle each)
+// through a 3-stage mbarrier ring.  Warp w owns keys 16w..16w+15 of every
+// tile and runs its own online softmax: S = Q K^T and O += P V with
+// mma.sync m16n8k16 (the group's G q heads padded to 16 rows).  The four
+// warps merge at the end; chunks merge through the workspace as above.
+// ---------------------------------------------------------------------------
+__device__ unsigned int g_attn_timeout = 0;
+
+constexpr int DT_KT = 64, DT_STAGES = 3, DT_THREADS = 128;
+constexpr uint32_t DT_BOX = 64 * 64 * 2;          // 64 keys x 64 dims of bf16
+constexpr uint32_t DT_STAGE = 4 * DT_BOX;         // K dims 0-63, K 64-127, V 0-63, V 64-127
+constexpr size_t DT_SMEM = 1024 + size_t(DT_STAGES) * DT_STAGE + 256;
+
+// byte offset of (key row r, 16-byte chunk c16 over the 128 dims) in a K or V region
+__device__ __forceinline__ uint32_t kv_off(int r, int c16) {
+  return uint32_t(c16 >> 3) * DT_BOX + uint32_t(r) * 128u + uint32_t(((c16 & 7) ^ (r & 7)) * 16);
+}
+
+template <int G>
+__global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
+    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const bf16* __restrict__ q,
+    const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ seq_base, int nh, int nkv, float scale_log2,
+    int chunk, int n_splits, float* __restrict__ ws_o, float* __restrict__ ws_ml, unsigned int* __restrict__ counters,
+    bf16* __restrict__ out) {
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + DT_STAGES * DT_STAGE);
+  const int b = blockIdx.z, g = blockIdx.y, split = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int L = ctx_lens[b];
+  const int start = split * chunk;
+  const int end = min(L, start + chunk);
+  const int h0 = g * G;
+  if (start >= end) {
+    if (n_splits > 1) {
+      if (tid < G) {
+        const int64_t idx = (int64_t(b) * nh + h0 + tid) * n_splits + split;
+        ws_ml[2 * idx] = -INFINITY;
+        ws_ml[2 * idx + 1] = 0.0f;
+      }
+      decode_finish<bf16, G>(ws_o, ws_ml, counters, b, g, nh, nkv, n_splits, out);
+    } else {
+      for (int i = tid; i < G * DC_HD; i += DT_THREADS)
+        out[(int64_t(b) * nh + h0 + i / DC_HD) * DC_HD + i % DC_HD] = __float2bfloat16_rn(0.0f);
+    }
+    return;
+  }
+  const int n_kt = (end - start + DT_KT - 1) / DT_KT;
+  const int zbase = seq_base[b] + start;
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + DT_STAGES + s); };
+  if (tid == 0) {
+    for (int s = 0; s < DT_STAGES; ++s) {
+      tcx::mbar_init(full(s), 1);
+      tcx::mbar_init(empty(s), DT_THREADS / 32);
+    }
+    tcx::fence_mbar_init();
+    tcx::prefetch_map(&tmK);
+    tcx::prefetch_map(&tmV);
+  }
+  __syncthreads();
+  auto issue = [&](int t) {
+    const int s = t % DT_STAGES;
+    const uint32_t dst = smem_u32(sm + s * DT_STAGE);
+    const int z = zbase + t * DT_KT;
+    tcx::mbar_expect_tx(full(s), DT_STAGE);
+    tcx::tma_load_3d(dst, &tmK, full(s), 0, g, z);
+    tcx::tma_load_3d(dst + DT_BOX, &tmK, full(s), 64, g, z);
+    tcx::tma_load_3d(dst + 2 * DT_BOX, &tmV, full(s), 0, g, z);
+    tcx::tma_load_3d(dst + 3 * DT_BOX, &tmV, full(s), 64, g, z);
+  };
+  if (tid == 0)
+    for (int t = 0; t < DT_STAGES && t < n_kt; ++t) issue(t);
+
+  const int gq = lane >> 2, tq = lane & 3;   // mma fragment row / column pair
+  const int mi = lane >> 3, ri = lane & 7;   // ldmatrix matrix / row
+  // q of this thread's row (head h0 + gq; rows >= G are zero)
+  uint32_t qa[8][2];
+  {
+    const bf16* qr = q + (int64_t(b) * nh + h0 + (gq < G ? gq : 0)) * DC_HD;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      qa[kk][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tq) : 0u;
+      qa[kk][1] = gq < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 8 + 2 * tq) : 0u;
     }
   }
-  out[hrow * DC_HD + d] = from_f<T>(L > 0.0f ? o / L : 0.0f);
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f;
+  const int key0 = warp * 16;
+  bool ok = true;
+  for (int t = 0; t < n_kt; ++t) {
+    const int s = t % DT_STAGES;
+    const uint32_t ph = (t / DT_STAGES) & 1;
+    if (ok && !tcx::mbar_wait(full(s), ph, &g_attn_timeout, 1u)) ok = false;
+    const uint32_t st = smem_u32(sm + s * DT_STAGE);
+    const int kbase = start + t * DT_KT + key0;          // key position of this warp's first row
+    if (kbase + 16 > end) {
+      // keys past the chunk: zero their V rows (whatever the cache holds there)
+      for (int i = 0; i < 16; ++i)
+        if (kbase + i >= end && lane < 16)
+          *reinterpret_cast<uint4*>(sm + s * DT_STAGE + 2 * DT_BOX + kv_off(key0 + i, lane)) = make_uint4(0, 0, 0, 0);
+      tcx::fence_proxy_async();
+      __syncwarp();
+    }
+    float sc[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(st + kv_off(key0 + ri + 8 * (mi >> 1), 2 * kk + (mi & 1)), b0, b1, b2, b3);
+      mma_bf16(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+      mma_bf16(sc[1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+    }
+    float x[4];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int kp = kbase + 8 * n + 2 * tq + e;
+        const float v = kp < end ? sc[n][e] * scale_log2 : -INFINITY;
+        x[2 * n + e] = v;
+        mx = fmaxf(mx, v);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run, mx);
+    const float m_use = m_new == -INFINITY ? 0.0f : m_new;
+    const float alpha = exp2f(m_run - m_use);
+    float p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = exp2f(x[i] - m_use);
+    l_run = l_run * alpha + (p[0] + p[1] + p[2] + p[3]);
+    m_run = m_new;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      o[i][0] *= alpha;
+      o[i][1] *= alpha;
+    }
+    const uint32_t a0 = pack_bf16(p[0], p[1]);
+    const uint32_t a2 = pack_bf16(p[2], p[3]);
+#pragma unroll
+    for (int dp = 0; dp < 8; ++dp) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(st + 2 * DT_BOX + kv_off(key0 + ri + 8 * (mi & 1), 2 * dp + (mi >> 1)), b0, b1, b2, b3);
+      mma_bf16(o[2 * dp], a0, 0u, a2, 0u, b0, b1);
+      mma_bf16(o[2 * dp + 1], a0, 0u, a2, 0u, b2, b3);
+    }
+    __syncwarp();
+    if (lane == 0) tcx::mbar_arrive(empty(s));
+    if (tid == 0 && t + DT_STAGES < n_kt) {
+      if (ok && !tcx::mbar_wait(empty(s), ph, &g_attn_timeout, 2u)) ok = false;
+      if (ok) issue(t + DT_STAGES);
+    }
+  }
+  // merge the four warps' softmax states
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  __syncthreads();   // every tile consumed: the ring is free
+  float* sO = reinterpret_cast<float*>(sm);                    // [4 warps][G][128]
+  float* sML = sO + (DT_THREADS / 32) * G * DC_HD;             // [4 warps][G][2]
+  if (gq < G) {
+#pragma unroll
+    for (int dn = 0; dn < 16; ++dn) {
+      sO[(warp * G + gq) * DC_HD + 8 * dn + 2 * tq] = o[dn][0];
+      sO[(warp * G + gq) * DC_HD + 8 * dn + 2 * tq + 1] = o[dn][1];
+    }
+    if (tq == 0) {
+      sML[(warp * G + gq) * 2] = m_run;
+      sML[(warp * G + gq) * 2 + 1] = l_run;
+    }
+  }
+  __syncthreads();
+  const int d = tid;
+  for (int j = 0; j < G; ++j) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < DT_THREADS / 32; ++w) M = fmaxf(M, sML[(w * G + j) * 2]);
+    float Lsum = 0.0f, O = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < DT_THREADS / 32; ++w) {
+        const float mw = sML[(w * G + j) * 2];
+        if (mw == -INFINITY) continue;
+        const float sc = exp2f(mw - M);
+        Lsum += sML[(w * G + j) * 2 + 1] * sc;
+        O += sO[(w * G + j) * DC_HD + d] * sc;
+      }
+    }
+    const int64_t hrow = int64_t(b) * nh + h0 + j;
+    if (n_splits > 1) {
+      const int64_t idx = hrow * n_splits + split;
+      ws_o[idx * DC_HD + d] = O;
+      if (d == 0) {
+        ws_ml[2 * idx] = M;
+        ws_ml[2 * idx + 1] = Lsum;
+      }
+    } else {
+      out[hrow * DC_HD + d] = __float2bfloat16_rn(Lsum > 0.0f ? O / Lsum : 0.0f);
+    }
+  }
+  if (n_splits > 1) decode_finish<bf16, G>(ws_o, ws_ml, counters, b, g, nh, nkv, n_splits, out);
 }
 
 struct DecodePlan {
@@ -568,13 +843,39 @@ extern "C" size_t qw_attention_decode_workspace_size(int B, int max_context, int
   if (B <= 0 || max_context <= 0 || n_heads <= 0 || head_dim != 128) return 0;
   const DecodePlan p = decode_plan(B, max_context, 0);
   if (p.splits <= 1) return 0;
-  return size_t(B) * n_heads * p.splits * (size_t(head_dim) + 2) * sizeof(float);
+  return kCounterBytes + size_t(B) * n_heads * p.splits * (size_t(head_dim) + 2) * sizeof(float);
+}
+
+template <int G>
+static int launch_decode_tc(const void* q, const void* kc, const void* vc, const int32_t* cl, const int32_t* sb,
+                            int B, int nh, int nkv, int64_t num_slots, float sl2, const DecodePlan& p, float* wo,
+                            float* wml, unsigned int* cnt, void* out, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(DT_SMEM));
+    if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    configured = true;
+  }
+  CUtensorMap mk, mv;
+  const uint64_t dims[3] = {uint64_t(DC_HD), uint64_t(nkv), uint64_t(num_slots)};
+  const uint64_t strides[2] = {uint64_t(DC_HD) * 2, uint64_t(nkv) * DC_HD * 2};
+  const uint32_t box[3] = {64u, 1u, uint32_t(DT_KT)};
+  int rc = make_tensor_map(&mk, kc, 3, dims, strides, box);
+  if (rc) return rc;
+  rc = make_tensor_map(&mv, vc, 3, dims, strides, box);
+  if (rc) return rc;
+  dim3 grid(unsigned(p.splits), unsigned(nkv), unsigned(B));
+  attn_decode_tc_kernel<G><<<grid, DT_THREADS, DT_SMEM, st>>>(mk, mv, static_cast<const bf16*>(q), cl, sb, nh, nkv,
+                                                              sl2, p.chunk, p.splits, wo, wml, cnt,
+                                                              static_cast<bf16*>(out));
+  return check_launch("attn_decode_tc_kernel");
 }
 
 template <typename T, int G>
 static int launch_decode(const void* q, const void* kc, const void* vc, const int32_t* cl, const int32_t* sb, int B,
-                         int nh, int nkv, float sl2, const DecodePlan& p, float* wo, float* wml, void* out,
-                         cudaStream_t st) {
+                         int nh, int nkv, float sl2, const DecodePlan& p, float* wo, float* wml, unsigned int* cnt,
+                         void* out, cudaStream_t st) {
   constexpr size_t sm = decode_smem<T>();
   static bool configured = false;
   if (!configured) {
@@ -585,19 +886,16 @@ static int launch_decode(const void* q, const void* kc, const void* vc, const in
   dim3 grid(unsigned(p.splits), unsigned(nkv), unsigned(B));
   attn_decode_kernel<T, G><<<grid, DC_THREADS, sm, st>>>(static_cast<const T*>(q), static_cast<const T*>(kc),
                                                          static_cast<const T*>(vc), cl, sb, nh, nkv, sl2, p.chunk,
-                                                         p.splits, wo, wml, static_cast<T*>(out));
-  int rc = check_launch("attn_decode_kernel");
-  if (rc || p.splits <= 1) return rc;
-  attn_decode_combine_kernel<T><<<unsigned(B * nh), DC_HD, 0, st>>>(wo, wml, p.splits, static_cast<T*>(out));
-  return check_launch("attn_decode_combine_kernel");
+                                                         p.splits, wo, wml, cnt, static_cast<T*>(out));
+  return check_launch("attn_decode_kernel");
 }
 
-extern "C" int qw_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+extern "C" int qw_attention_decode(const void* q, const void* k_cache, const void* v_cache, int64_t num_slots,
                                    const int32_t* context_lens, const int32_t* seq_base, int B, int max_context,
                                    int n_heads, int n_kv_heads, int head_dim, float scale, void* out, void* workspace,
                                    size_t workspace_bytes, int dtype, void* stream) {
   if (dtype != QW_BF16 && dtype != QW_F32) return set_error(QW_ERR_DTYPE, "qw_attention_decode: dtype %d", dtype);
-  if (B < 0 || max_context < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0)
+  if (B < 0 || max_context < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || num_slots < 0)
     return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode: bad sizes");
   if (n_heads % n_kv_heads || (head_dim != 128 && head_dim > 64))
     return set_error(QW_ERR_SHAPE, "qw_attention_decode: needs nh %% nkv == 0 and head_dim 128 or <= 64");
@@ -619,22 +917,39 @@ extern "C" int qw_attention_decode(const void* q, const void* k_cache, const voi
   const size_t need = qw_attention_decode_workspace_size(B, max_context, n_heads, head_dim);
   if (need && (!workspace || workspace_bytes < need))
     return set_error(QW_ERR_WORKSPACE, "qw_attention_decode: workspace of %zu bytes needed", need);
-  float* wml = static_cast<float*>(workspace);
+  if (need && size_t(B) * n_kv_heads * sizeof(unsigned int) > kCounterBytes)
+    return set_error(QW_ERR_SHAPE, "qw_attention_decode: %d sequences x %d kv heads exceed the counter area", B,
+                     n_kv_heads);
+  unsigned int* cnt = need ? static_cast<unsigned int*>(workspace) : nullptr;
+  float* wml = need ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kCounterBytes) : nullptr;
   float* wo = wml ? wml + size_t(B) * n_heads * p.splits * 2 : nullptr;
   const float sl2 = scale * kLog2e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == QW_BF16) {
+    if (reinterpret_cast<uintptr_t>(k_cache) % 16 || reinterpret_cast<uintptr_t>(v_cache) % 16)
+      return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode: caches must be 16-byte aligned");
+    switch (G) {
+      case 1: return launch_decode_tc<1>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, num_slots,
+                                         sl2, p, wo, wml, cnt, out, st);
+      case 2: return launch_decode_tc<2>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, num_slots,
+                                         sl2, p, wo, wml, cnt, out, st);
+      case 4: return launch_decode_tc<4>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, num_slots,
+                                         sl2, p, wo, wml, cnt, out, st);
+      default: return launch_decode_tc<8>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads,
+                                          num_slots, sl2, p, wo, wml, cnt, out, st);
+    }
+  }
 #define QW_DEC(TT)                                                                                                   \
   switch (G) {                                                                                                       \
     case 1: return launch_decode<TT, 1>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, sl2, p, \
-                                        wo, wml, out, st);                                                           \
+                                        wo, wml, cnt, out, st);                                                           \
     case 2: return launch_decode<TT, 2>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, sl2, p, \
-                                        wo, wml, out, st);                                                           \
+                                        wo, wml, cnt, out, st);                                                           \
     case 4: return launch_decode<TT, 4>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, sl2, p, \
-                                        wo, wml, out, st);                                                           \
+                                        wo, wml, cnt, out, st);                                                           \
     default: return launch_decode<TT, 8>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, sl2,  \
-                                         p, wo, wml, out, st);                                                       \
+                                         p, wo, wml, cnt, out, st);                                                       \
   }
-  if (dtype == QW_BF16) { QW_DEC(bf16) }
   QW_DEC(float)
 #undef QW_DEC
 }
@@ -683,7 +998,7 @@ static int decode_scratch_address(void** out) {
 extern "C" size_t qw_attention_decode_static_scratch_bytes(void) { return qw::attn::kStaticScratchBytes; }
 
 extern "C" int qw_attention_decode_static(const void* q, const void* k_cache, const void* v_cache,
-                                          const int32_t* context_lens, const int32_t* seq_base, int B,
+                                          int64_t num_slots, const int32_t* context_lens, const int32_t* seq_base, int B,
                                           int max_context, int n_heads, int n_kv_heads, int head_dim, float scale,
                                           void* out, int dtype, void* stream) {
   const size_t need = qw_attention_decode_workspace_size(B, max_context, n_heads, head_dim);
@@ -697,6 +1012,15 @@ extern "C" int qw_attention_decode_static(const void* q, const void* k_cache, co
     const int rc = qw::attn::decode_scratch_address(&ws);
     if (rc != QW_OK) return rc;
   }
-  return qw_attention_decode(q, k_cache, v_cache, context_lens, seq_base, B, max_context, n_heads, n_kv_heads,
+  return qw_attention_decode(q, k_cache, v_cache, num_slots, context_lens, seq_base, B, max_context, n_heads, n_kv_heads,
                              head_dim, scale, out, ws, need > 0 ? qw::attn::kStaticScratchBytes : 0, dtype, stream);
 }
+
+namespace qw {
+unsigned int take_attn_timeouts() {
+  unsigned int v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, attn::g_attn_timeout, sizeof(v));
+  if (v) cudaMemcpyToSymbol(attn::g_attn_timeout, &z, sizeof(z));
+  return v;
+}
+}  // namespace qw

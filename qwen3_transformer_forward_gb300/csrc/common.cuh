@@ -11,6 +11,10 @@ namespace qw {
 
 using bf16 = __nv_bfloat16;
 
+// Every workspace starts with this many bytes of completion counters; they
+// must be zero before the first call and each call leaves them zero.
+constexpr size_t kCounterBytes = 64 * 1024;
+
 // ---------------------------------------------------------------------------
 // element conversions
 // ---------------------------------------------------------------------------

@@ -17,7 +17,11 @@
 // Prefill (many tokens): MMA-A = activations, MMA-B = weights, BN = 256.
 // Decode (<= 64 tokens): operands swapped (MMA-A = 128 weight rows,
 // MMA-B = the tokens padded to 16/32/64) and split along K so that enough
-// CTAs stream the weights; a reduce kernel sums the fp32 partials.
+// CTAs stream the weights.  The K-splits of one weight tile form a thread-
+// block cluster (<= 8 CTAs): each leaves its fp32 partial tile in its own
+// shared memory and cluster rank 0 sums them in split order over distributed
+// shared memory, then applies the epilogue (bf16, or SiluAndMul with 64 gate
+// + 64 up rows per tile).  No global scratch, deterministic.
 //
 // Every mbarrier wait is bounded (2 s of %globaltimer); on timeout the kernel
 // records an error word, drains its own copies and frees TMEM.
@@ -32,6 +36,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "tc_common.cuh"
 
 namespace qw {
 
@@ -50,10 +55,11 @@ constexpr int BK = 64;
 constexpr int UMMA_K = 16;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int EPI_NONE = 0, EPI_SILU = 1;
+constexpr int kMaxCluster = 8;   // portable cluster size: K-splits per weight tile
 
 struct TcArgs {
   bf16* C;              // output (bf16)
-  float* partial;       // split-K fp32 partials [splits][M][Nfull] or nullptr
+  int splits;           // K-splits per weight tile (= cluster size along y; 1 = direct store)
   int64_t ldc;          // output row stride
   int64_t M;            // token rows
   int64_t N;            // output features (full width before SiluAndMul)
@@ -154,6 +160,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// thread-block cluster helpers (distributed shared memory)
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// address of the same shared-memory offset in cluster CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes grouped in 1024-byte (8-row) atoms.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -242,9 +269,10 @@ __global__ void __launch_bounds__(192, 1)
     // ---------------- TMA producer ----------------
     int r_s = 0;
     int64_t jl0 = 0;
-    if (EPI == EPI_SILU && !SWAP) {
-      r_s = tile_q / a.silu_tps;
-      jl0 = int64_t(tile_q % a.silu_tps) * (BN / 2);
+    if (EPI == EPI_SILU) {
+      const int t = SWAP ? tile_p : tile_q;
+      r_s = t / a.silu_tps;
+      jl0 = int64_t(t % a.silu_tps) * (SWAP ? BM / 2 : BN / 2);
     }
     for (int kb = kb0; kb < kb1; ++kb) {
       const int i = kb - kb0;
@@ -278,8 +306,16 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_2d(dB, &tmW, bar_full(s), xw, tile_q * BN);
         }
       } else {
-        if (WROW) tma_load_3d(dA, &tmW, bar_full(s), xw, tile_p * BM, rw);
-        else tma_load_2d(dA, &tmW, bar_full(s), xw, tile_p * BM);
+        if (EPI == EPI_SILU) {
+          // 64 gate rows then the 64 matching up rows of shard r_s
+          const int64_t g0 = int64_t(r_s) * 2 * a.i_l + jl0;
+          tma_load_2d(dA, &tmW, bar_full(s), xw, int(g0));
+          tma_load_2d(dA + A_BYTES / 2, &tmW, bar_full(s), xw, int(g0 + a.i_l));
+        } else if (WROW) {
+          tma_load_3d(dA, &tmW, bar_full(s), xw, tile_p * BM, rw);
+        } else {
+          tma_load_2d(dA, &tmW, bar_full(s), xw, tile_p * BM);
+        }
         tma_load_2d(dB, &tmAct, bar_full(s), xa, tile_q * BN);
       }
       issued = kb + 1;
@@ -381,8 +417,11 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     } else {
-      // swapped: TMEM lane = output feature, column = token
-      const int64_t p = int64_t(tile_p) * BM + quarter * 32 + lane;
+      // swapped: TMEM lane = weight row of the tile, column = token
+      const int pl = quarter * 32 + lane;
+      const int mv = int(a.M);   // tokens (<= BN)
+      const int64_t p = int64_t(tile_p) * BM + pl;
+      float* part_s = reinterpret_cast<float*>(sA);   // ring slots are free once the MMAs are done
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
@@ -392,20 +431,67 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = 0u;
         }
-        if (p < a.N) {
-          const int lim = BN - c < 32 ? BN - c : 32;
-          for (int e = 0; e < lim; ++e) {
-            const int64_t j = int64_t(tile_q) * BN + c + e;
-            if (j < a.M) {
-              if (a.partial != nullptr)
-                a.partial[(int64_t(split) * a.M + j) * a.N + p] = __uint_as_float(r[e]);
-              else
-                a.C[j * a.ldc + p] = __float2bfloat16_rn(__uint_as_float(r[e]));
-            }
-          }
+        const int lim = BN - c < 32 ? BN - c : 32;
+        if (a.splits == 1 && EPI == EPI_NONE) {
+          if (p < a.N)
+            for (int e = 0; e < lim; ++e)
+              if (c + e < mv) a.C[int64_t(c + e) * a.ldc + p] = __float2bfloat16_rn(__uint_as_float(r[e]));
+        } else {
+          for (int e = 0; e < lim; ++e) part_s[(c + e) * BM + pl] = __uint_as_float(r[e]);
         }
       }
     }
+  }
+
+  if (SWAP && (a.splits > 1 || EPI == EPI_SILU)) {
+    // every CTA of the cluster has its partial tile in shared memory (a lone
+    // CTA is a cluster of one)
+    __syncwarp();
+    cluster_sync_all();
+    if (warp >= 2) {
+      // reduce-scatter: rank r sums the splits for the tile rows f = r, r + S, ...
+      // (SiluAndMul: gate row f and up row f + 64) and writes those outputs
+      const int S = a.splits;
+      const uint32_t rank = cluster_rank();
+      const int mv = int(a.M);
+      const int te = threadIdx.x - 64;                 // 0..127 over the epilogue warps
+      constexpr int NF = EPI == EPI_SILU ? BM / 2 : BM;
+      const int nf_mine = (NF - int(rank) + S - 1) / S;
+      const uint32_t base = smem_u32(sA);
+      uint32_t peer[kMaxCluster];
+#pragma unroll
+      for (int sp = 0; sp < kMaxCluster; ++sp) peer[sp] = sp < S ? map_to_rank(base, uint32_t(sp)) : 0u;
+      const int total = nf_mine * mv;
+#pragma unroll 2
+      for (int idx = te; idx < total; idx += 128) {
+        const int fi = idx % nf_mine, j = idx / nf_mine;
+        const int f = int(rank) + S * fi;
+        const uint32_t off_g = uint32_t(j * BM + f) * 4u;
+        float vg[kMaxCluster], vu[kMaxCluster];
+#pragma unroll
+        for (int sp = 0; sp < kMaxCluster; ++sp) {
+          vg[sp] = sp < S ? ld_cluster_f32(peer[sp] + off_g) : 0.0f;
+          if (EPI == EPI_SILU) vu[sp] = sp < S ? ld_cluster_f32(peer[sp] + off_g + uint32_t(BM / 2) * 4u) : 0.0f;
+        }
+        float g = 0.0f, u = 0.0f;
+#pragma unroll
+        for (int sp = 0; sp < kMaxCluster; ++sp)
+          if (sp < S) {   // split order: deterministic
+            g += vg[sp];
+            if (EPI == EPI_SILU) u += vu[sp];
+          }
+        if (EPI == EPI_NONE) {
+          const int64_t pcol = int64_t(tile_p) * BM + f;
+          if (pcol < a.N) a.C[int64_t(j) * a.ldc + pcol] = __float2bfloat16_rn(g);
+        } else {
+          const int r_s = tile_p / a.silu_tps;
+          const int64_t jl = int64_t(tile_p % a.silu_tps) * (BM / 2) + f;
+          if (jl < a.i_l) a.C[int64_t(j) * a.ldc + int64_t(r_s) * a.i_l + jl] = __float2bfloat16_rn(silu_mul_bf16(g, u));
+        }
+      }
+    }
+    // keep every CTA's shared memory alive until all ranks have read it
+    cluster_sync_all();
   }
 
   __syncwarp();
@@ -423,34 +509,6 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::TMEM_COLS);
-  }
-}
-
-// fp32 split-K partials -> bf16 output, with an optional SiluAndMul on the
-// merged gate_up columns ([SK] §4)
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, int splits, int64_t M,
-                                                            int64_t N, bf16* __restrict__ C, int64_t ldc, int epi,
-                                                            int64_t i_l) {
-  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t stride = int64_t(splits) > 0 ? M * N : 0;
-  if (epi == EPI_NONE) {
-    if (idx >= M * N) return;
-    float s = 0.0f;
-    for (int k = 0; k < splits; ++k) s += part[k * stride + idx];
-    const int64_t m = idx / N, n = idx % N;
-    C[m * ldc + n] = __float2bfloat16_rn(s);
-  } else {
-    const int64_t I = N / 2;
-    if (idx >= M * I) return;
-    const int64_t m = idx / I, o = idx % I;
-    const int64_t r = o / i_l, j = o % i_l;
-    const int64_t gcol = r * 2 * i_l + j;
-    float g = 0.0f, u = 0.0f;
-    for (int k = 0; k < splits; ++k) {
-      g += part[k * stride + m * N + gcol];
-      u += part[k * stride + m * N + gcol + i_l];
-    }
-    C[m * ldc + o] = __float2bfloat16_rn(silu_mul_bf16(g, u));
   }
 }
 
@@ -524,17 +582,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 struct MapKey {
   uint64_t ptr;
-  uint64_t d0, d1, d2, s0, s1;
-  uint32_t b0, b1, rank;
+  uint64_t d[3], s[2];
+  uint32_t b[3], rank;
   bool operator==(const MapKey& o) const {
-    return ptr == o.ptr && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 && s0 == o.s0 && s1 == o.s1 && b0 == o.b0 &&
-           b1 == o.b1 && rank == o.rank;
+    return ptr == o.ptr && d[0] == o.d[0] && d[1] == o.d[1] && d[2] == o.d[2] && s[0] == o.s[0] && s[1] == o.s[1] &&
+           b[0] == o.b[0] && b[1] == o.b[1] && b[2] == o.b[2] && rank == o.rank;
   }
 };
 struct MapKeyHash {
   size_t operator()(const MapKey& k) const {
     uint64_t h = k.ptr * 0x9E3779B97F4A7C15ull;
-    for (uint64_t v : {k.d0, k.d1, k.d2, k.s0, k.s1, uint64_t(k.b0) << 32 | k.b1, uint64_t(k.rank)})
+    for (uint64_t v : {k.d[0], k.d[1], k.d[2], k.s[0], k.s[1], uint64_t(k.b[0]) << 32 | k.b[1],
+                       uint64_t(k.b[2]) << 32 | k.rank})
       h = (h ^ v) * 0x100000001B3ull;
     return size_t(h);
   }
@@ -542,11 +601,18 @@ struct MapKeyHash {
 std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
-// 2D (rank 2) or 3D (rank 3) bf16 map, innermost dim first, 128-byte swizzle,
-// box = 64 elements x box_rows (x 1)
-int make_map(CUtensorMap* out, const void* ptr, int rank, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s0_bytes,
-             uint64_t s1_bytes, uint32_t box_rows) {
-  MapKey key{reinterpret_cast<uint64_t>(ptr), d0, d1, d2, s0_bytes, s1_bytes, 64u, box_rows, uint32_t(rank)};
+}  // namespace
+
+int make_tensor_map(CUtensorMap* out, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
+                    const uint32_t* box) {
+  MapKey key{};
+  key.ptr = reinterpret_cast<uint64_t>(ptr);
+  key.rank = uint32_t(rank);
+  for (int i = 0; i < 3; ++i) {
+    key.d[i] = i < rank ? dims[i] : 1;
+    key.b[i] = i < rank ? box[i] : 1;
+  }
+  for (int i = 0; i < 2; ++i) key.s[i] = i < rank - 1 ? strides[i] : 0;
   {
     std::lock_guard<std::mutex> lk(g_map_mu);
     auto it = g_maps.find(key);
@@ -557,11 +623,11 @@ int make_map(CUtensorMap* out, const void* ptr, int rank, uint64_t d0, uint64_t 
   }
   auto fn = encode_fn();
   if (!fn) return set_error(QW_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {s0_bytes, s1_bytes};
-  cuuint32_t box[3] = {64u, box_rows, 1u};
+  cuuint64_t gd[3] = {key.d[0], key.d[1], key.d[2]};
+  cuuint64_t gs[2] = {key.s[0], key.s[1]};
+  cuuint32_t bx[3] = {key.b[0], key.b[1], key.b[2]};
   cuuint32_t es[3] = {1u, 1u, 1u};
-  CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
+  CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), gd, gs, bx, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_error(QW_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
@@ -571,18 +637,29 @@ int make_map(CUtensorMap* out, const void* ptr, int rank, uint64_t d0, uint64_t 
   return QW_OK;
 }
 
+namespace {
+
+// 2D (rank 2) or 3D (rank 3) map with box = 64 elements x box_rows (x 1)
+int make_map(CUtensorMap* out, const void* ptr, int rank, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s0_bytes,
+             uint64_t s1_bytes, uint32_t box_rows) {
+  const uint64_t dims[3] = {d0, d1, d2};
+  const uint64_t strides[2] = {s0_bytes, s1_bytes};
+  const uint32_t box[3] = {64u, box_rows, 1u};
+  return make_tensor_map(out, ptr, rank, dims, strides, box);
+}
+
 struct Plan {
   bool swap;
   int bn;
-  int splits;
+  int splits;         // swap: K-splits per weight tile = cluster size (<= 8)
   int kblocks_total;
   int kpb;
-  size_t ws_bytes;
+  int p_tiles;        // swap: weight-row tiles (SiluAndMul: 64 gate + 64 up rows per tile)
 };
 
 constexpr int kSms = 152;
 
-Plan plan_bf16(int64_t M, int64_t N, int64_t K, int tp, int mode) {
+Plan plan_bf16(int64_t M, int64_t N, int64_t K, int tp, int mode, int epi) {
   Plan p{};
   const int64_t Kl = mode == QW_GEMM_ROW_REDUCE ? K / tp : K;
   p.kpb = int((Kl + tc::BK - 1) / tc::BK);
@@ -591,15 +668,18 @@ Plan plan_bf16(int64_t M, int64_t N, int64_t K, int tp, int mode) {
   p.splits = 1;
   if (p.swap) {
     p.bn = M <= 16 ? 16 : M <= 32 ? 32 : 64;
-    const int p_tiles = int((N + tc::BM - 1) / tc::BM);
-    int s = (2 * kSms + p_tiles - 1) / p_tiles;
-    s = s < 1 ? 1 : s;
-    const int smax = p.kblocks_total / 2 > 1 ? p.kblocks_total / 2 : 1;
-    p.splits = s < smax ? s : smax;
-    // even out the k-blocks per split
-    const int per = (p.kblocks_total + p.splits - 1) / p.splits;
+    if (epi == QW_EPI_SILU_MUL) {
+      const int64_t i_l = N / 2 / tp;
+      p.p_tiles = int(tp * ((i_l + tc::BM / 2 - 1) / (tc::BM / 2)));
+    } else {
+      p.p_tiles = int((N + tc::BM - 1) / tc::BM);
+    }
+    // about two resident CTAs per SM, at most one cluster of 8 per tile
+    int s = (2 * kSms + p.p_tiles - 1) / p.p_tiles;
+    s = s < 1 ? 1 : (s > tc::kMaxCluster ? tc::kMaxCluster : s);
+    s = s > p.kblocks_total ? p.kblocks_total : s;
+    const int per = (p.kblocks_total + s - 1) / s;
     p.splits = (p.kblocks_total + per - 1) / per;
-    p.ws_bytes = p.splits > 1 ? size_t(p.splits) * size_t(M) * size_t(N) * sizeof(float) : 0;
   } else {
     p.bn = 256;
   }
@@ -616,14 +696,26 @@ int launch_tc(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArgs& ar
     if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     configured = true;
   }
-  dim3 grid(unsigned(args.p_tiles * args.q_tiles), unsigned(splits));
-  kern<<<grid, 192, smem, st>>>(act, w, args);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(args.p_tiles * args.q_tiles), unsigned(splits), 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = unsigned(splits);
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = splits > 1 ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, act, w, args);
+  if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "gemm_tc_kernel launch: %s", cudaGetErrorString(e));
   return check_launch("gemm_tc_kernel");
 }
 
 int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64_t K, int tp, int mode, int epi,
-              void* ws, size_t ws_bytes, cudaStream_t st) {
-  const Plan p = plan_bf16(M, N, K, tp, mode);
+              cudaStream_t st) {
+  const Plan p = plan_bf16(M, N, K, tp, mode, epi);
   const int64_t Kl = mode == QW_GEMM_ROW_REDUCE ? K / tp : K;
   const bool wrow = mode == QW_GEMM_ROW_REDUCE;
   int rc;
@@ -637,6 +729,7 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
   a.kpb = p.kpb;
   a.k_shard = Kl;
   a.i_l = epi == QW_EPI_SILU_MUL ? N / 2 / tp : 0;
+  a.splits = 1;
   if (!p.swap) {
     rc = make_map(&mA, A, 2, uint64_t(K), uint64_t(M), 1, uint64_t(K) * 2, 0, tc::BM);
     if (rc) return rc;
@@ -654,7 +747,6 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
     }
     a.p_fastest = (M * K * 2) <= (int64_t(48) << 20) ? 1 : 0;
     a.kblocks = p.kblocks_total;
-    a.partial = nullptr;
     if (epi == QW_EPI_SILU_MUL) return launch_tc<256, 4, false, tc::EPI_SILU, false>(mA, mW, a, 1, st);
     if (wrow) return launch_tc<256, 4, false, tc::EPI_NONE, true>(mA, mW, a, 1, st);
     return launch_tc<256, 4, false, tc::EPI_NONE, false>(mA, mW, a, 1, st);
@@ -662,47 +754,25 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
   // swapped operands for few tokens
   rc = make_map(&mA, A, 2, uint64_t(K), uint64_t(M), 1, uint64_t(K) * 2, 0, uint32_t(p.bn));
   if (rc) return rc;
+  const uint32_t wrows = epi == QW_EPI_SILU_MUL ? uint32_t(tc::BM / 2) : uint32_t(tc::BM);
   if (wrow) rc = make_map(&mW, W, 3, uint64_t(Kl), uint64_t(N), uint64_t(tp), uint64_t(Kl) * 2,
-                          uint64_t(Kl) * 2 * uint64_t(N), tc::BM);
-  else rc = make_map(&mW, W, 2, uint64_t(K), uint64_t(N), 1, uint64_t(K) * 2, 0, tc::BM);
+                          uint64_t(Kl) * 2 * uint64_t(N), wrows);
+  else rc = make_map(&mW, W, 2, uint64_t(K), uint64_t(N), 1, uint64_t(K) * 2, 0, wrows);
   if (rc) return rc;
-  a.p_tiles = int((N + tc::BM - 1) / tc::BM);
+  a.p_tiles = p.p_tiles;
   a.q_tiles = 1;
   a.p_fastest = 1;
   a.kblocks = (p.kblocks_total + p.splits - 1) / p.splits;
-  const bool need_reduce = p.splits > 1 || epi == QW_EPI_SILU_MUL;
-  float* part = nullptr;
-  if (need_reduce) {
-    const size_t need = size_t(p.splits) * size_t(M) * size_t(N) * sizeof(float);
-    if (!ws || ws_bytes < need)
-      return set_error(QW_ERR_WORKSPACE, "qw_gemm: workspace of %zu bytes needed", need);
-    part = static_cast<float*>(ws);
-  }
-  a.partial = part;
-  int r;
-#define QW_SWAP_LAUNCH(BNV)                                                                        \
-  r = wrow ? launch_tc<BNV, 8, true, tc::EPI_NONE, true>(mA, mW, a, p.splits, st)                  \
-           : launch_tc<BNV, 8, true, tc::EPI_NONE, false>(mA, mW, a, p.splits, st);
+  a.splits = p.splits;
+  if (epi == QW_EPI_SILU_MUL) a.silu_tps = p.p_tiles / tp;
+#define QW_SWAP_LAUNCH(BNV)                                                                                \
+  if (epi == QW_EPI_SILU_MUL) return launch_tc<BNV, 4, true, tc::EPI_SILU, false>(mA, mW, a, p.splits, st); \
+  if (wrow) return launch_tc<BNV, 4, true, tc::EPI_NONE, true>(mA, mW, a, p.splits, st);                    \
+  return launch_tc<BNV, 4, true, tc::EPI_NONE, false>(mA, mW, a, p.splits, st);
   if (p.bn == 16) { QW_SWAP_LAUNCH(16) }
-  else if (p.bn == 32) { QW_SWAP_LAUNCH(32) }
-  else { QW_SWAP_LAUNCH(64) }
+  if (p.bn == 32) { QW_SWAP_LAUNCH(32) }
+  QW_SWAP_LAUNCH(64)
 #undef QW_SWAP_LAUNCH
-  if (r) return r;
-  if (need_reduce) {
-    const int64_t outs = epi == QW_EPI_SILU_MUL ? M * (N / 2) : M * N;
-    tc::splitk_reduce_kernel<<<unsigned((outs + 255) / 256), 256, 0, st>>>(
-        part, p.splits, M, N, C, a.ldc, epi == QW_EPI_SILU_MUL ? tc::EPI_SILU : tc::EPI_NONE, a.i_l);
-    return check_launch("splitk_reduce_kernel");
-  }
-  return QW_OK;
-}
-
-size_t gemm_ws(int64_t M, int64_t N, int64_t K, int tp, int mode, int epi, int dtype) {
-  if (dtype != QW_BF16) return 0;
-  const Plan p = plan_bf16(M, N, K, tp, mode);
-  if (!p.swap) return 0;
-  if (p.splits > 1 || epi == QW_EPI_SILU_MUL) return size_t(p.splits) * size_t(M) * size_t(N) * sizeof(float);
-  return 0;
 }
 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -749,12 +819,13 @@ static int gemm_check(const void* A, const void* W, void* C, int64_t M, int64_t 
 }
 
 extern "C" size_t qw_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int tp, int mode, int epilogue, int dtype) {
-  if (M <= 0 || N <= 0 || K <= 0 || tp <= 0) return 0;
-  return gemm_ws(M, N, K, tp, mode, epilogue, dtype);
+  (void)M, (void)N, (void)K, (void)tp, (void)mode, (void)epilogue, (void)dtype;
+  return 0;   // split-K partials stay on chip (cluster shared memory)
 }
 
 extern "C" int qw_gemm(const void* A, const void* W, void* C, int64_t M, int64_t N, int64_t K, int tp, int mode,
                        int epilogue, void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+  (void)workspace, (void)workspace_bytes;
   int rc = gemm_check(A, W, C, M, N, K, tp, mode, epilogue, dtype, "qw_gemm");
   if (rc >= 0) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -768,14 +839,18 @@ extern "C" int qw_gemm(const void* A, const void* W, void* C, int64_t M, int64_t
     return check_launch("gemm_f32_kernel");
   }
   return gemm_bf16(static_cast<const bf16*>(A), static_cast<const bf16*>(W), static_cast<bf16*>(C), M, N, K, tp,
-                   mode, epilogue, workspace, workspace_bytes, st);
+                   mode, epilogue, st);
+}
+
+static size_t lm_rows_bytes(int64_t n_out, int64_t H, int dtype) {
+  const size_t es = dtype == QW_BF16 ? 2 : 4;
+  return (size_t(n_out) * size_t(H) * es + 255) / 256 * 256;
 }
 
 extern "C" size_t qw_lm_head_workspace_size(int64_t n_out, int64_t V, int64_t H, int tp, int dtype) {
   if (n_out <= 0 || V <= 0 || H <= 0) return 0;
-  const size_t es = dtype == QW_BF16 ? 2 : 4;
-  const size_t rows = (size_t(n_out) * size_t(H) * es + 255) / 256 * 256;
-  return rows + gemm_ws(n_out, V, H, tp > 0 ? tp : 1, QW_GEMM_COLUMN, QW_EPI_NONE, dtype);
+  (void)tp;
+  return kCounterBytes + lm_rows_bytes(n_out, H, dtype);
 }
 
 extern "C" int qw_lm_head(const void* hidden, int64_t T, const int32_t* last_idx, int64_t n_out, const void* table,
@@ -788,25 +863,26 @@ extern "C" int qw_lm_head(const void* hidden, int64_t T, const int32_t* last_idx
   if (!hidden || !table || !logits) return set_error(QW_ERR_INVALID_ARG, "qw_lm_head: null pointer");
   if (!last_idx && n_out > T) return set_error(QW_ERR_SHAPE, "qw_lm_head: n_out > T without last_idx");
   const size_t es = dtype == QW_BF16 ? 2 : 4;
-  const size_t need = qw_lm_head_workspace_size(n_out, V, H, tp, dtype);
-  const void* x = hidden;
+  int rc = gemm_check(hidden, table, logits, n_out, V, H, 1, QW_GEMM_COLUMN, QW_EPI_NONE, dtype, "qw_lm_head");
+  if (rc >= 0) return rc;
+  if ((H * int64_t(es)) % 16 || !al16(hidden)) return set_error(QW_ERR_INVALID_ARG, "qw_lm_head: H rows must be 16-byte");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  size_t rows = 0;
+  const void* x = hidden;
   if (last_idx) {
-    if (!ws || workspace_bytes < need) return set_error(QW_ERR_WORKSPACE, "qw_lm_head: workspace of %zu bytes needed", need);
-    if ((H * int64_t(es)) % 16 || !al16(hidden)) return set_error(QW_ERR_INVALID_ARG, "qw_lm_head: H rows must be 16-byte");
-    rows = (size_t(n_out) * size_t(H) * es + 255) / 256 * 256;
-    int rc = dtype == QW_BF16 ? launch_gather_rows<bf16>(hidden, T, last_idx, n_out, H, ws, st)
-                              : launch_gather_rows<float>(hidden, T, last_idx, n_out, H, ws, st);
+    const size_t need = qw_lm_head_workspace_size(n_out, V, H, tp, dtype);
+    if (!workspace || workspace_bytes < need)
+      return set_error(QW_ERR_WORKSPACE, "qw_lm_head: workspace of %zu bytes needed", need);
+    // the selected rows go after the counter area that other calls may share
+    uint8_t* rows = static_cast<uint8_t*>(workspace) + kCounterBytes;
+    rc = dtype == QW_BF16 ? launch_gather_rows<bf16>(hidden, T, last_idx, n_out, H, rows, st)
+                          : launch_gather_rows<float>(hidden, T, last_idx, n_out, H, rows, st);
     if (rc) return rc;
-    x = ws;
+    x = rows;
   }
   // each vocab shard r projects onto its rows [r*V/tp, (r+1)*V/tp) and writes
   // logit columns [r*V/tp, (r+1)*V/tp): with the shards stacked in one table
   // that is a single column-split GEMM over the whole vocab
-  int rc = qw_gemm(x, table, logits, n_out, V, H, 1, QW_GEMM_COLUMN, QW_EPI_NONE, ws ? ws + rows : nullptr,
-                   workspace_bytes > rows ? workspace_bytes - rows : 0, dtype, stream);
+  rc = qw_gemm(x, table, logits, n_out, V, H, 1, QW_GEMM_COLUMN, QW_EPI_NONE, nullptr, 0, dtype, stream);
   if (rc) return rc;
   if (next_tokens) return qw_argmax(logits, n_out, V, next_tokens, dtype, stream);
   return QW_OK;

@@ -175,7 +175,8 @@ class Qwen3Forward:
             ws = max(ws, L.gemm_workspace_size(M, N, K, tp, mode, epi, dt))
         ws = max(ws, L.attention_decode_workspace_size(max(max_seqs, 1), max_context, shape.n_heads, hd))
         ws = max(ws, L.lm_head_workspace_size(max(max_seqs, 1), shape.vocab, H, tp, dt))
-        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
+        # completion counters at its start must be zero before the first call
+        self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=device)
         self.scale = hd ** -0.5
         self.probe = None      # optional timing hook: probe(name, layer) -> context manager
 

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.qw_abi_version() == 1
+    assert lib.qw_abi_version() == 2
 
 
 def test_argument_errors_are_reported_before_launch(lib):
@@ -73,12 +73,12 @@ def test_argument_errors_are_reported_before_launch(lib):
                                     None) == L.QW_ERR_SHAPE
     assert lib.qw_attention_prefill(fake, fake, fake, fake, fake, None, 2, 8, 16, 8, 128, 0.1, fake, L.QW_F32,
                                     None) == L.QW_ERR_SHAPE
-    assert lib.qw_attention_decode(fake, fake, fake, fake, fake, 2, 8, 12, 4, 128, 0.1, fake, None, 0, L.QW_BF16,
-                                   None) == L.QW_ERR_SHAPE
+    assert lib.qw_attention_decode(fake, fake, fake, 100, fake, fake, 2, 8, 12, 4, 128, 0.1, fake, None, 0,
+                                   L.QW_BF16, None) == L.QW_ERR_SHAPE
     # decode without the workspace it needs
     need = lib.qw_attention_decode_workspace_size(8, 4096, 16, 128)
     assert need > 0
-    assert lib.qw_attention_decode(fake, fake, fake, fake, fake, 8, 4096, 16, 8, 128, 0.1, fake, None, 0,
+    assert lib.qw_attention_decode(fake, fake, fake, 100, fake, fake, 8, 4096, 16, 8, 128, 0.1, fake, None, 0,
                                    L.QW_BF16, None) == L.QW_ERR_WORKSPACE
     # lm_head: V not divisible by tp
     assert lib.qw_lm_head(fake, 4, None, 4, fake, 10, 64, 4, fake, None, None, 0, L.QW_BF16,
@@ -94,8 +94,8 @@ def test_rope_table_equals_oracle(lib, max_pos, d, theta):
 
 
 def test_workspace_sizes(lib):
-    # prefill-sized GEMMs need no workspace; decode-sized ones split K and do
+    # GEMMs keep split-K partials on chip: no workspace at any size
     assert L.gemm_workspace_size(2048, 4096, 1024, 2, L.QW_GEMM_COLUMN, 0, torch.bfloat16) == 0
-    assert L.gemm_workspace_size(8, 1024, 3072, 2, L.QW_GEMM_ROW_REDUCE, 0, torch.bfloat16) > 0
-    assert L.gemm_workspace_size(8, 1024, 3072, 2, L.QW_GEMM_ROW_REDUCE, 0, torch.float32) == 0
+    assert L.gemm_workspace_size(8, 1024, 3072, 2, L.QW_GEMM_ROW_REDUCE, 0, torch.bfloat16) == 0
+    assert L.lm_head_workspace_size(8, 151936, 1024, 2, torch.bfloat16) >= 64 * 1024 + 8 * 1024 * 2
     assert L.attention_decode_workspace_size(64, 2048, 16, 128) > 0

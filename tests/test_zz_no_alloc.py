@@ -53,7 +53,7 @@ def test_static_scratch_matches_workspace_version_twice(L):
         q, kc, vc, cl, sb, mc, nh, nkv, hd = _case(name, ctx)
         assert 0 < L.attention_decode_workspace_size(len(ctx), mc, nh, hd) <= L.attention_decode_static_scratch_bytes()
         ref = torch.empty(len(ctx), nh * hd, dtype=q.dtype, device="cuda")
-        ws = torch.empty(L.attention_decode_workspace_size(len(ctx), mc, nh, hd), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(L.attention_decode_workspace_size(len(ctx), mc, nh, hd), dtype=torch.uint8, device="cuda")
         L.attention_decode(q, kc, vc, cl, sb, mc, nh, nkv, hd, hd ** -0.5, ref, ws)
         got = torch.empty_like(ref)
         L.attention_decode_static(q, kc, vc, cl, sb, mc, nh, nkv, hd, hd ** -0.5, got)
