@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16_kernel(
     const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
     const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, const int32_t* __restrict__ seq_base,
     int nh, int nkv, float scale_log2, bf16* __restrict__ out) {
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // inputs of this kernel are complete and visible
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* sQ = smem;
   uint8_t* sK = smem + PF_BR * 256;
@@ -238,6 +240,8 @@ __global__ void __launch_bounds__(128) attn_small_kernel(
     const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, const int32_t* __restrict__ seq_base,
     const int32_t* __restrict__ ctx_lens, int n_seqs, int max_q, int nh, int nkv, int hd, float scale,
     T* __restrict__ out) {
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // inputs of this kernel are complete and visible
   const int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= int64_t(n_seqs) * max_q * nh) return;
@@ -297,7 +301,7 @@ int launch_attn_small(const void* q, const void* k, const void* v, const int32_t
                       const int32_t* seq_base, const int32_t* ctx_lens, int n_seqs, int max_q, int nh, int nkv,
                       int hd, float scale, void* out, cudaStream_t st) {
   const int64_t threads = int64_t(n_seqs) * max_q * nh * 32;
-  attn_small_kernel<T><<<unsigned((threads + 127) / 128), 128, 0, st>>>(
+  launch_pdl(attn_small_kernel<T>, unsigned((threads + 127) / 128), 128, 0, st, 
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), cu_q, cu_k, seq_base, ctx_lens,
       n_seqs, max_q, nh, nkv, hd, scale, static_cast<T*>(out));
   return check_launch("attn_small_kernel");
@@ -409,6 +413,8 @@ __global__ void __launch_bounds__(DC_THREADS) attn_decode_kernel(
     const T* __restrict__ q, const T* __restrict__ kc, const T* __restrict__ vc, const int32_t* __restrict__ ctx_lens,
     const int32_t* __restrict__ seq_base, int nh, int nkv, float scale_log2, int chunk, int n_splits,
     float* __restrict__ ws_o, float* __restrict__ ws_ml, unsigned int* __restrict__ counters, T* __restrict__ out) {
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // inputs of this kernel are complete and visible
   constexpr int EPC = 16 / sizeof(T);      // elements per 16-byte chunk
   constexpr int CPR = DC_HD / EPC;         // chunks per row
   extern __shared__ __align__(128) uint8_t smem[];
@@ -594,6 +600,8 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
     const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ seq_base, int nh, int nkv, float scale_log2,
     int chunk, int n_splits, float* __restrict__ ws_o, float* __restrict__ ws_ml, unsigned int* __restrict__ counters,
     bf16* __restrict__ out) {
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // inputs of this kernel are complete and visible
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + DT_STAGES * DT_STAGE);
@@ -827,7 +835,7 @@ extern "C" int qw_attention_prefill(const void* q, const void* k, const void* v,
       configured = true;
     }
     dim3 grid(unsigned((max_seqlen_q + PF_BR - 1) / PF_BR), unsigned(n_heads), unsigned(n_seqs));
-    attn_prefill_bf16_kernel<<<grid, PF_THREADS, PF_SMEM, st>>>(
+    launch_pdl(attn_prefill_bf16_kernel, grid, PF_THREADS, PF_SMEM, st, 
         static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v), cu_seqlens_q,
         cu_seqlens_k, seq_base, n_heads, n_kv_heads, scale * kLog2e, static_cast<bf16*>(out));
     return check_launch("attn_prefill_bf16_kernel");
@@ -866,7 +874,7 @@ static int launch_decode_tc(const void* q, const void* kc, const void* vc, const
   rc = make_tensor_map(&mv, vc, 3, dims, strides, box);
   if (rc) return rc;
   dim3 grid(unsigned(p.splits), unsigned(nkv), unsigned(B));
-  attn_decode_tc_kernel<G><<<grid, DT_THREADS, DT_SMEM, st>>>(mk, mv, static_cast<const bf16*>(q), cl, sb, nh, nkv,
+  launch_pdl(attn_decode_tc_kernel<G>, grid, DT_THREADS, DT_SMEM, st, mk, mv, static_cast<const bf16*>(q), cl, sb, nh, nkv,
                                                               sl2, p.chunk, p.splits, wo, wml, cnt,
                                                               static_cast<bf16*>(out));
   return check_launch("attn_decode_tc_kernel");
@@ -884,7 +892,7 @@ static int launch_decode(const void* q, const void* kc, const void* vc, const in
     configured = true;
   }
   dim3 grid(unsigned(p.splits), unsigned(nkv), unsigned(B));
-  attn_decode_kernel<T, G><<<grid, DC_THREADS, sm, st>>>(static_cast<const T*>(q), static_cast<const T*>(kc),
+  launch_pdl(attn_decode_kernel<T, G>, grid, DC_THREADS, sm, st, static_cast<const T*>(q), static_cast<const T*>(kc),
                                                          static_cast<const T*>(vc), cl, sb, nh, nkv, sl2, p.chunk,
                                                          p.splits, wo, wml, cnt, static_cast<T*>(out));
   return check_launch("attn_decode_kernel");

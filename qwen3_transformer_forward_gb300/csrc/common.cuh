@@ -92,9 +92,38 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
 }  // namespace qw
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel lets the next kernel on the stream
+// start early (pdl_trigger) and waits for the previous one to finish and
+// publish its memory (pdl_wait) before touching anything it produced.  Both
+// are no-ops when the kernel was launched without the attribute.
+// ---------------------------------------------------------------------------
+namespace qw {
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+}  // namespace qw
+
+// ---------------------------------------------------------------------------
 // host-side error reporting shared by every entry point (defined in qw_api.cu)
 // ---------------------------------------------------------------------------
 namespace qw {
 int set_error(int code, const char* fmt, ...);
 int check_launch(const char* what);
+bool pdl_enabled();   // programmatic dependent launch on (default) unless QW_NO_PDL=1
+
+// Launches `kern` on `st` with programmatic stream serialization (when enabled).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 }  // namespace qw

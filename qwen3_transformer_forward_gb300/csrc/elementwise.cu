@@ -19,6 +19,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) embed_vocab_kernel(const int64_t* __restrict__ ids, int64_t n_tok,
                                                           const T* __restrict__ table, int64_t V, int64_t H,
                                                           int tp, T* __restrict__ out, int32_t* err) {
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // inputs of this kernel are complete and visible
   constexpr int N = V16<T>::N;
   const int64_t tok = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -66,6 +68,8 @@ template <typename T, int NV>
 __global__ void __launch_bounds__(256) add_rmsnorm_kernel(const T* __restrict__ x, const T* res_in, T* res_out,
                                                           const T* __restrict__ gamma, float eps, int64_t rows,
                                                           int H, T* __restrict__ y) {
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // inputs of this kernel are complete and visible
   constexpr int N = V16<T>::N;
   const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -118,6 +122,8 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_kernel(
     const T* __restrict__ q_gamma, const T* __restrict__ k_gamma, float eps,
     const int64_t* __restrict__ slots, T* __restrict__ k_cache, T* __restrict__ v_cache, int64_t num_slots,
     T* __restrict__ q_out, int32_t* err) {
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // inputs of this kernel are complete and visible
   const int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int heads = nh + nkv;
@@ -213,6 +219,8 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_kernel(
 template <typename T>
 __global__ void __launch_bounds__(256) silu_mul_kernel(const T* __restrict__ x, T* __restrict__ out,
                                                        int64_t n_tok, int64_t I, int64_t I_l) {
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // inputs of this kernel are complete and visible
   constexpr int N = V16<T>::N;
   const int64_t vpr = I / N;
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -235,6 +243,8 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const T* __restrict__ x, 
 template <typename T>
 __global__ void __launch_bounds__(1024) argmax_kernel(const T* __restrict__ logits, int64_t V,
                                                       int64_t* __restrict__ out) {
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // inputs of this kernel are complete and visible
   constexpr int N = V16<T>::N;
   const T* p = logits + int64_t(blockIdx.x) * V;
   float best = -INFINITY;
@@ -283,6 +293,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const T* __restrict__ src, int64_t n_src,
                                                           const int32_t* __restrict__ idx, int64_t n,
                                                           int64_t H, T* __restrict__ out) {
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // inputs of this kernel are complete and visible
   constexpr int N = V16<T>::N;
   const int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -304,7 +316,7 @@ template <typename T>
 int launch_gather_rows(const void* src, int64_t n_src, const int32_t* idx, int64_t n, int64_t H, void* out,
                        cudaStream_t st) {
   const int64_t threads = n * 32;
-  gather_rows_kernel<T><<<unsigned((threads + 255) / 256), 256, 0, st>>>(
+  launch_pdl(gather_rows_kernel<T>, unsigned((threads + 255) / 256), 256, 0, st, 
       static_cast<const T*>(src), n_src, idx, n, H, static_cast<T*>(out));
   return check_launch("gather_rows");
 }
@@ -313,7 +325,7 @@ template int launch_gather_rows<float>(const void*, int64_t, const int32_t*, int
 
 template <typename T>
 int launch_argmax(const void* logits, int64_t M, int64_t V, int64_t* out, cudaStream_t st) {
-  argmax_kernel<T><<<unsigned(M), 1024, 0, st>>>(static_cast<const T*>(logits), V, out);
+  launch_pdl(argmax_kernel<T>, unsigned(M), 1024, 0, st, static_cast<const T*>(logits), V, out);
   return check_launch("argmax");
 }
 template int launch_argmax<bf16>(const void*, int64_t, int64_t, int64_t*, cudaStream_t);
@@ -342,10 +354,10 @@ extern "C" int qw_embed_vocab(const int64_t* ids, int64_t T, const void* table, 
   const int64_t threads = T * 32;
   const unsigned blocks = unsigned((threads + 255) / 256);
   if (dtype == QW_BF16)
-    embed_vocab_kernel<bf16><<<blocks, 256, 0, st>>>(ids, T, static_cast<const bf16*>(table), V, H, tp,
+    launch_pdl(embed_vocab_kernel<bf16>, blocks, 256, 0, st, ids, T, static_cast<const bf16*>(table), V, H, tp,
                                                      static_cast<bf16*>(out), err_count);
   else
-    embed_vocab_kernel<float><<<blocks, 256, 0, st>>>(ids, T, static_cast<const float*>(table), V, H, tp,
+    launch_pdl(embed_vocab_kernel<float>, blocks, 256, 0, st, ids, T, static_cast<const float*>(table), V, H, tp,
                                                       static_cast<float*>(out), err_count);
   return check_launch("qw_embed_vocab");
 }
@@ -360,11 +372,11 @@ static void launch_add_rmsnorm(int nv, const void* x, const void* ri, void* ro, 
   auto G = static_cast<const T*>(g);
   auto Y = static_cast<T*>(y);
   switch (nv) {
-    case 1: add_rmsnorm_kernel<T, 1><<<blocks, 256, 0, st>>>(X, RI, RO, G, eps, T_, H, Y); break;
-    case 2: add_rmsnorm_kernel<T, 2><<<blocks, 256, 0, st>>>(X, RI, RO, G, eps, T_, H, Y); break;
-    case 4: add_rmsnorm_kernel<T, 4><<<blocks, 256, 0, st>>>(X, RI, RO, G, eps, T_, H, Y); break;
-    case 8: add_rmsnorm_kernel<T, 8><<<blocks, 256, 0, st>>>(X, RI, RO, G, eps, T_, H, Y); break;
-    default: add_rmsnorm_kernel<T, 16><<<blocks, 256, 0, st>>>(X, RI, RO, G, eps, T_, H, Y); break;
+    case 1: launch_pdl(add_rmsnorm_kernel<T, 1>, blocks, 256, 0, st, X, RI, RO, G, eps, T_, H, Y); break;
+    case 2: launch_pdl(add_rmsnorm_kernel<T, 2>, blocks, 256, 0, st, X, RI, RO, G, eps, T_, H, Y); break;
+    case 4: launch_pdl(add_rmsnorm_kernel<T, 4>, blocks, 256, 0, st, X, RI, RO, G, eps, T_, H, Y); break;
+    case 8: launch_pdl(add_rmsnorm_kernel<T, 8>, blocks, 256, 0, st, X, RI, RO, G, eps, T_, H, Y); break;
+    default: launch_pdl(add_rmsnorm_kernel<T, 16>, blocks, 256, 0, st, X, RI, RO, G, eps, T_, H, Y); break;
   }
 }
 
@@ -419,10 +431,10 @@ static void launch_qkv_rope(int ppl, const void* qkv, int64_t T_, int nh, int nk
   auto v = static_cast<T*>(vc);
   auto q = static_cast<T*>(qo);
   switch (ppl) {
-    case 1: qkv_norm_rope_kernel<T, 1><<<blocks, 256, 0, st>>>(a, T_, nh, nkv, hd, tp, pos, cs, maxp, g1, g2, eps, slots, k, v, ns, q, err); break;
-    case 2: qkv_norm_rope_kernel<T, 2><<<blocks, 256, 0, st>>>(a, T_, nh, nkv, hd, tp, pos, cs, maxp, g1, g2, eps, slots, k, v, ns, q, err); break;
-    case 3: qkv_norm_rope_kernel<T, 3><<<blocks, 256, 0, st>>>(a, T_, nh, nkv, hd, tp, pos, cs, maxp, g1, g2, eps, slots, k, v, ns, q, err); break;
-    default: qkv_norm_rope_kernel<T, 4><<<blocks, 256, 0, st>>>(a, T_, nh, nkv, hd, tp, pos, cs, maxp, g1, g2, eps, slots, k, v, ns, q, err); break;
+    case 1: launch_pdl(qkv_norm_rope_kernel<T, 1>, blocks, 256, 0, st, a, T_, nh, nkv, hd, tp, pos, cs, maxp, g1, g2, eps, slots, k, v, ns, q, err); break;
+    case 2: launch_pdl(qkv_norm_rope_kernel<T, 2>, blocks, 256, 0, st, a, T_, nh, nkv, hd, tp, pos, cs, maxp, g1, g2, eps, slots, k, v, ns, q, err); break;
+    case 3: launch_pdl(qkv_norm_rope_kernel<T, 3>, blocks, 256, 0, st, a, T_, nh, nkv, hd, tp, pos, cs, maxp, g1, g2, eps, slots, k, v, ns, q, err); break;
+    default: launch_pdl(qkv_norm_rope_kernel<T, 4>, blocks, 256, 0, st, a, T_, nh, nkv, hd, tp, pos, cs, maxp, g1, g2, eps, slots, k, v, ns, q, err); break;
   }
 }
 
@@ -463,9 +475,9 @@ extern "C" int qw_silu_mul(const void* x, void* out, int64_t T, int64_t I, int t
   const int64_t n = T * (I / N);
   const unsigned blocks = unsigned((n + 255) / 256);
   if (dtype == QW_BF16)
-    silu_mul_kernel<bf16><<<blocks, 256, 0, st>>>(static_cast<const bf16*>(x), static_cast<bf16*>(out), T, I, I / tp);
+    launch_pdl(silu_mul_kernel<bf16>, blocks, 256, 0, st, static_cast<const bf16*>(x), static_cast<bf16*>(out), T, I, I / tp);
   else
-    silu_mul_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(x), static_cast<float*>(out), T, I,
+    launch_pdl(silu_mul_kernel<float>, blocks, 256, 0, st, static_cast<const float*>(x), static_cast<float*>(out), T, I,
                                                     I / tp);
   return check_launch("qw_silu_mul");
 }

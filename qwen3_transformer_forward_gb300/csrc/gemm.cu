@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  pdl_trigger();   // the next kernel may start its prologue
   int issued = kb0;
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
@@ -274,7 +275,45 @@ __global__ void __launch_bounds__(192, 1)
       r_s = t / a.silu_tps;
       jl0 = int64_t(t % a.silu_tps) * (SWAP ? BM / 2 : BN / 2);
     }
-    for (int kb = kb0; kb < kb1; ++kb) {
+    // weight slab of k-block kb into ring stage s (weights are constants)
+    auto load_w = [&](int kb, int s) {
+      int xw, rw = 0;
+      if (WROW) {
+        rw = kb / a.kpb;
+        xw = (kb % a.kpb) * BK;
+      } else {
+        xw = kb * BK;
+      }
+      const uint32_t dW = SWAP ? smem_u32(sA + s * A_BYTES) : smem_u32(sB + s * B_BYTES);
+      const uint32_t half = SWAP ? A_BYTES / 2 : B_BYTES / 2;
+      if (EPI == EPI_SILU) {
+        const int64_t g0 = int64_t(r_s) * 2 * a.i_l + jl0;
+        tma_load_2d(dW, &tmW, bar_full(s), xw, int(g0));
+        tma_load_2d(dW + half, &tmW, bar_full(s), xw, int(g0 + a.i_l));
+      } else if (WROW) {
+        tma_load_3d(dW, &tmW, bar_full(s), xw, SWAP ? tile_p * BM : tile_q * BN, rw);
+      } else {
+        tma_load_2d(dW, &tmW, bar_full(s), xw, SWAP ? tile_p * BM : tile_q * BN);
+      }
+    };
+    // activation slab of k-block kb (written by the previous kernel)
+    auto load_act = [&](int kb, int s) {
+      int xa;
+      if (WROW) xa = int((kb / a.kpb) * a.k_shard) + (kb % a.kpb) * BK;
+      else xa = kb * BK;
+      if (!SWAP) tma_load_2d(smem_u32(sA + s * A_BYTES), &tmAct, bar_full(s), xa, tile_p * BM);
+      else tma_load_2d(smem_u32(sB + s * B_BYTES), &tmAct, bar_full(s), xa, tile_q * BN);
+    };
+    // prologue: the first ring's weights stream in while the previous kernel finishes
+    const int npre = kb1 - kb0 < STAGES ? kb1 - kb0 : STAGES;
+    for (int i = 0; i < npre; ++i) {
+      mbar_expect_tx(bar_full(i), A_BYTES + B_BYTES);
+      load_w(kb0 + i, i);
+    }
+    pdl_wait();
+    for (int i = 0; i < npre; ++i) load_act(kb0 + i, i);
+    issued = kb0 + npre;
+    for (int kb = kb0 + npre; kb < kb1; ++kb) {
       const int i = kb - kb0;
       const int s = i % STAGES;
       const uint32_t ph = (i / STAGES) & 1;
@@ -284,40 +323,8 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (*abort_flag) break;
       mbar_expect_tx(bar_full(s), A_BYTES + B_BYTES);
-      int xa, xw, rw = 0;
-      if (WROW) {
-        rw = kb / a.kpb;
-        xw = (kb % a.kpb) * BK;
-        xa = int(rw * a.k_shard) + xw;
-      } else {
-        xa = xw = kb * BK;
-      }
-      const uint32_t dA = smem_u32(sA + s * A_BYTES);
-      const uint32_t dB = smem_u32(sB + s * B_BYTES);
-      if (!SWAP) {
-        tma_load_2d(dA, &tmAct, bar_full(s), xa, tile_p * BM);
-        if (EPI == EPI_SILU) {
-          const int64_t g0 = int64_t(r_s) * 2 * a.i_l + jl0;
-          tma_load_2d(dB, &tmW, bar_full(s), xw, int(g0));
-          tma_load_2d(dB + B_BYTES / 2, &tmW, bar_full(s), xw, int(g0 + a.i_l));
-        } else if (WROW) {
-          tma_load_3d(dB, &tmW, bar_full(s), xw, tile_q * BN, rw);
-        } else {
-          tma_load_2d(dB, &tmW, bar_full(s), xw, tile_q * BN);
-        }
-      } else {
-        if (EPI == EPI_SILU) {
-          // 64 gate rows then the 64 matching up rows of shard r_s
-          const int64_t g0 = int64_t(r_s) * 2 * a.i_l + jl0;
-          tma_load_2d(dA, &tmW, bar_full(s), xw, int(g0));
-          tma_load_2d(dA + A_BYTES / 2, &tmW, bar_full(s), xw, int(g0 + a.i_l));
-        } else if (WROW) {
-          tma_load_3d(dA, &tmW, bar_full(s), xw, tile_p * BM, rw);
-        } else {
-          tma_load_2d(dA, &tmW, bar_full(s), xw, tile_p * BM);
-        }
-        tma_load_2d(dB, &tmAct, bar_full(s), xa, tile_q * BN);
-      }
+      load_w(kb, s);
+      load_act(kb, s);
       issued = kb + 1;
     }
   } else if (warp == 1 && lane == 0) {
@@ -515,6 +522,141 @@ __global__ void __launch_bounds__(192, 1)
 }  // namespace tc
 
 // ===========================================================================
+// Few-token GEMM (decode): weight streaming with warp-level MMA.
+//
+// C[M, N] = A[M, K] W^T for M <= 64.  The weights are read once and dominate
+// the bytes, so the kernel is built for memory-level parallelism: a CTA owns
+// 16 weight rows (SiluAndMul: 8 gate rows and the matching 8 up rows) across
+// the whole K, split over its 8 warps; each warp issues all its weight loads
+// (16-byte, non-caching) up front into registers -- before the programmatic
+// dependency wait, since weights are constants -- then multiplies with
+// mma.sync m16n8k16.  Weights and tokens use the same permutation of the 32
+// k values of a chunk (thread t holds k 8t..8t+7: logical k 2t,2t+1 | 2t+8,2t+9
+// of two k-steps), so no shuffles are needed.  The 8 warps' partial tiles are
+// added in shared memory in warp order (deterministic) and the epilogue
+// writes bf16 (or silu(gate) * up).
+// ===========================================================================
+constexpr int GV_WARPS = 8;
+
+__device__ __forceinline__ uint4 ldg_stream(const bf16* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// RPC: weight rows per CTA (16, or 8 for small N to spread over more SMs);
+// MAXC: 32-wide k chunks per warp held in registers at once.
+template <int NT, int EPI, bool WROW, int RPC, int MAXC>
+__global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
+    gemv_mma_kernel(const bf16* __restrict__ A, const bf16* __restrict__ W, bf16* __restrict__ C, int M, int N, int K,
+                    int K_l, int64_t ldc, int64_t i_l) {
+  constexpr int GV_MAXC = MAXC;
+  __shared__ float red[GV_WARPS][16][NT * 8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  // the two weight rows of this thread (m16 tile rows g and g + 8)
+  int64_t rowA, rowB;
+  bool okA, okB;
+  if (EPI == tc::EPI_SILU) {
+    const int64_t o0 = int64_t(blockIdx.x) * 8;        // first output column
+    const int64_t r = o0 / i_l, j = o0 % i_l + g;
+    rowA = r * 2 * i_l + j;                            // gate row
+    rowB = rowA + i_l;                                 // matching up row
+    okA = okB = (o0 + g) < int64_t(N / 2) && j < i_l;
+  } else {
+    rowA = int64_t(blockIdx.x) * RPC + g;
+    rowB = rowA + 8;
+    okA = rowA < N;
+    okB = RPC == 16 && rowB < N;
+  }
+  const int kw = ((K + GV_WARPS * 32 - 1) / (GV_WARPS * 32)) * 32;   // k values per warp, whole chunks
+  const int k0 = warp * kw;
+  const int k1 = min(K, k0 + kw);
+  auto wptr = [&](int64_t row, int k) -> const bf16* {
+    if (WROW) {
+      const int r = k / K_l;
+      return W + (int64_t(r) * N + row) * K_l + (k - r * K_l);
+    }
+    return W + row * int64_t(K) + k;
+  };
+  float acc[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+  bool waited = false;
+  for (int kb = k0; kb < k1; kb += GV_MAXC * 32) {
+    uint4 wa[GV_MAXC], wb[GV_MAXC];
+#pragma unroll
+    for (int c = 0; c < GV_MAXC; ++c) {
+      const int k = kb + 32 * c + 8 * t;
+      const bool in = kb + 32 * c < k1;
+      wa[c] = (in && okA) ? ldg_stream(wptr(rowA, k)) : make_uint4(0, 0, 0, 0);
+      wb[c] = (RPC == 16 && in && okB) ? ldg_stream(wptr(rowB, k)) : make_uint4(0, 0, 0, 0);
+    }
+    if (!waited) {
+      pdl_trigger();   // the next kernel may start its prologue
+      pdl_wait();      // the activations are complete and visible
+      waited = true;
+    }
+#pragma unroll
+    for (int c = 0; c < GV_MAXC; ++c) {
+      if (kb + 32 * c >= k1) break;
+      const int k = kb + 32 * c + 8 * t;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const int tok = n * 8 + g;
+        const uint4 x = tok < M ? __ldg(reinterpret_cast<const uint4*>(A + int64_t(tok) * K + k)) : make_uint4(0, 0, 0, 0);
+        mma_16816(acc[n], wa[c].x, wb[c].x, wa[c].y, wb[c].y, x.x, x.y);
+        mma_16816(acc[n], wa[c].z, wb[c].z, wa[c].w, wb[c].w, x.z, x.w);
+      }
+    }
+  }
+  if (!waited) {
+    pdl_trigger();
+    pdl_wait();
+  }
+  // partial tiles to shared memory: rows g, g+8; tokens 2t, 2t+1 of each n-tile
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    red[warp][g][n * 8 + 2 * t] = acc[n][0];
+    red[warp][g][n * 8 + 2 * t + 1] = acc[n][1];
+    red[warp][g + 8][n * 8 + 2 * t] = acc[n][2];
+    red[warp][g + 8][n * 8 + 2 * t + 1] = acc[n][3];
+  }
+  __syncthreads();
+  if (EPI == tc::EPI_SILU) {
+    for (int e = threadIdx.x; e < 8 * M; e += GV_WARPS * 32) {
+      const int r = e & 7, tok = e >> 3;
+      float gs = 0.0f, us = 0.0f;
+#pragma unroll
+      for (int w = 0; w < GV_WARPS; ++w) {
+        gs += red[w][r][tok];
+        us += red[w][r + 8][tok];
+      }
+      const int64_t o = int64_t(blockIdx.x) * 8 + r;
+      if (o < N / 2) C[int64_t(tok) * ldc + o] = __float2bfloat16_rn(tc::silu_mul_bf16(gs, us));
+    }
+  } else {
+    for (int e = threadIdx.x; e < RPC * M; e += GV_WARPS * 32) {
+      const int r = e % RPC, tok = e / RPC;
+      float sum = 0.0f;
+#pragma unroll
+      for (int w = 0; w < GV_WARPS; ++w) sum += red[w][r][tok];
+      const int64_t row = int64_t(blockIdx.x) * RPC + r;
+      if (row < N) C[int64_t(tok) * ldc + row] = __float2bfloat16_rn(sum);
+    }
+  }
+}
+
+// ===========================================================================
 // fp32 GEMM on CUDA cores (exact fp32 FMA; the small fp32 model)
 // ===========================================================================
 __device__ __forceinline__ float w_at(const float* W, int64_t n, int64_t k, int64_t N, int64_t K, int64_t K_l,
@@ -527,6 +669,8 @@ __device__ __forceinline__ float w_at(const float* W, int64_t n, int64_t k, int6
 __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__ A, const float* __restrict__ W,
                                                        float* __restrict__ C, int64_t M, int64_t Nout, int64_t N,
                                                        int64_t K, int64_t K_l, int row, int silu, int64_t i_l) {
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // inputs of this kernel are complete and visible
   __shared__ float sa[16][17];
   __shared__ float sw[2][16][17];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -751,6 +895,36 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
     if (wrow) return launch_tc<256, 4, false, tc::EPI_NONE, true>(mA, mW, a, 1, st);
     return launch_tc<256, 4, false, tc::EPI_NONE, false>(mA, mW, a, 1, st);
   }
+  // few tokens, moderate N: weight streaming on warp-level MMA (see gemv_mma_kernel)
+  if (p.splits > 1 && Kl % 32 == 0) {
+    const int nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
+    const bool small_k = K <= GV_WARPS * 32 * 4;            // every warp's weights fit 4 chunks
+    const bool half = epi != QW_EPI_SILU_MUL && N <= 2048;  // 8 rows per CTA: twice the CTAs
+    const unsigned blocks =
+        unsigned(epi == QW_EPI_SILU_MUL ? (N / 2 + 7) / 8 : half ? (N + 7) / 8 : (N + 15) / 16);
+    cudaError_t e;
+#define QW_GV_ONE(NTV, EPIV, WR, RPCV, MC)                                                                     \
+  e = launch_pdl(gemv_mma_kernel<NTV, EPIV, WR, RPCV, MC>, dim3(blocks), dim3(GV_WARPS * 32), 0, st, A, W, C,   \
+                 int(M), int(N), int(K), int(Kl), a.ldc, a.i_l);
+#define QW_GV(NTV)                                                                                             \
+  if (epi == QW_EPI_SILU_MUL) {                                                                                \
+    if (small_k) { QW_GV_ONE(NTV, tc::EPI_SILU, false, 16, 4) } else { QW_GV_ONE(NTV, tc::EPI_SILU, false, 16, 12) } \
+  } else if (half) {                                                                                           \
+    if (wrow) { QW_GV_ONE(NTV, tc::EPI_NONE, true, 8, 12) } else { QW_GV_ONE(NTV, tc::EPI_NONE, false, 8, 12) } \
+  } else if (small_k) {                                                                                        \
+    if (wrow) { QW_GV_ONE(NTV, tc::EPI_NONE, true, 16, 4) } else { QW_GV_ONE(NTV, tc::EPI_NONE, false, 16, 4) } \
+  } else {                                                                                                     \
+    if (wrow) { QW_GV_ONE(NTV, tc::EPI_NONE, true, 16, 12) } else { QW_GV_ONE(NTV, tc::EPI_NONE, false, 16, 12) } \
+  }
+    if (nt == 1) { QW_GV(1) }
+    else if (nt == 2) { QW_GV(2) }
+    else if (nt == 4) { QW_GV(4) }
+    else { QW_GV(8) }
+#undef QW_GV
+#undef QW_GV_ONE
+    if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "gemv_mma_kernel launch: %s", cudaGetErrorString(e));
+    return check_launch("gemv_mma_kernel");
+  }
   // swapped operands for few tokens
   rc = make_map(&mA, A, 2, uint64_t(K), uint64_t(M), 1, uint64_t(K) * 2, 0, uint32_t(p.bn));
   if (rc) return rc;
@@ -833,7 +1007,7 @@ extern "C" int qw_gemm(const void* A, const void* W, void* C, int64_t M, int64_t
     const int64_t Nout = epilogue == QW_EPI_SILU_MUL ? N / 2 : N;
     const int64_t Kl = mode == QW_GEMM_ROW_REDUCE ? K / tp : K;
     dim3 grid(unsigned((Nout + 15) / 16), unsigned((M + 15) / 16));
-    gemm_f32_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(A), static_cast<const float*>(W),
+    launch_pdl(gemm_f32_kernel, grid, 256, 0, st, static_cast<const float*>(A), static_cast<const float*>(W),
                                           static_cast<float*>(C), M, Nout, N, K, Kl, mode == QW_GEMM_ROW_REDUCE,
                                           epilogue == QW_EPI_SILU_MUL, epilogue == QW_EPI_SILU_MUL ? N / 2 / tp : 0);
     return check_launch("gemm_f32_kernel");

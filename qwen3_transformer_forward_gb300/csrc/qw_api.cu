@@ -1,6 +1,7 @@
 // Error reporting, version and device-error query of the libqw C ABI.
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 
 #include <string>
 
@@ -24,6 +25,14 @@ int check_launch(const char* what) {
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   return QW_OK;
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("QW_NO_PDL");
+    return !(v && v[0] == '1');
+  }();
+  return on;
 }
 
 // defined next to the kernels that own a bounded-wait error word
