@@ -214,6 +214,94 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_kernel(
 }
 
 // ===========================================================================
+// QK-RMSNorm + RoPE + KV-cache store, bf16 with head_dim 128 (the model's
+// shape): eight lanes per head.  Lane j of a group moves elements
+// [8j, 8j+8) of the first half and [64+8j, 64+8j+8) of the second as 16-byte
+// vectors, so every RoPE pair (i, i + 64) lives in one lane; the head's sum of
+// squares is reduced over the eight lanes.  Same arithmetic as above.
+// ===========================================================================
+__global__ void __launch_bounds__(256) qkv_norm_rope_hd128_kernel(
+    const bf16* __restrict__ qkv, int64_t n_tok, int nh, int nkv, int tp, const int64_t* __restrict__ positions,
+    const float* __restrict__ cos_sin, int64_t max_pos, const bf16* __restrict__ q_gamma,
+    const bf16* __restrict__ k_gamma, float eps, const int64_t* __restrict__ slots, bf16* __restrict__ k_cache,
+    bf16* __restrict__ v_cache, int64_t num_slots, bf16* __restrict__ q_out, int32_t* err) {
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // inputs of this kernel are complete and visible
+  constexpr int HD = 128, HALF = 64;
+  const int heads = nh + nkv;
+  const int64_t task = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 3;   // one (token, head) per 8 lanes
+  const int sub = threadIdx.x & 7;
+  if (task >= n_tok * heads) return;   // whole 8-lane groups leave together
+  const int64_t tok = task / heads;
+  const int h = int(task % heads);
+  const int nh_l = nh / tp, nkv_l = nkv / tp;
+  const int64_t width_r = int64_t(nh_l + 2 * nkv_l) * HD;
+  const int64_t row_w = width_r * tp;
+  const bool is_q = h < nh;
+  const bf16* src;
+  const bf16* gamma;
+  int g = 0;
+  if (is_q) {
+    src = qkv + tok * row_w + (h / nh_l) * width_r + int64_t(h % nh_l) * HD;
+    gamma = q_gamma;
+  } else {
+    g = h - nh;
+    src = qkv + tok * row_w + (g / nkv_l) * width_r + int64_t(nh_l + g % nkv_l) * HD;
+    gamma = k_gamma;
+  }
+  const int i0 = 8 * sub;
+  float x1[8], x2[8];
+  load16(src + i0, x1);
+  load16(src + HALF + i0, x2);
+  float ss = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ss += x1[e] * x1[e] + x2[e] * x2[e];
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+  const float inv = rsqrtf(ss / float(HD) + eps);
+  const int64_t pos = positions[tok];
+  const bool pos_ok = pos >= 0 && pos < max_pos;
+  if (!pos_ok && sub == 0 && h == 0 && err != nullptr) atomicAdd(err, 1);
+  const float* cs = cos_sin + (pos_ok ? pos : 0) * HD;
+  float g1[8], g2[8];
+  load16(gamma + i0, g1);
+  load16(gamma + HALF + i0, g2);
+  float c[8], sn[8];
+  *reinterpret_cast<float4*>(c) = *reinterpret_cast<const float4*>(cs + i0);
+  *reinterpret_cast<float4*>(c + 4) = *reinterpret_cast<const float4*>(cs + i0 + 4);
+  *reinterpret_cast<float4*>(sn) = *reinterpret_cast<const float4*>(cs + HALF + i0);
+  *reinterpret_cast<float4*>(sn + 4) = *reinterpret_cast<const float4*>(cs + HALF + i0 + 4);
+  float y1[8], y2[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float n1 = round_t<bf16>((x1[e] * inv) * g1[e]);   // q_norm / k_norm output
+    const float n2 = round_t<bf16>((x2[e] * inv) * g2[e]);
+    y1[e] = pos_ok ? n1 * c[e] - n2 * sn[e] : 0.0f;          // RoPE on the halves
+    y2[e] = pos_ok ? n2 * c[e] + n1 * sn[e] : 0.0f;
+  }
+  if (is_q) {
+    bf16* o = q_out + (tok * nh + h) * int64_t(HD);
+    store16(o + i0, y1);
+    store16(o + HALF + i0, y2);
+    return;
+  }
+  const int64_t slot = slots[tok];
+  if (slot == -1) return;                                                    // padding: not stored
+  if (slot < 0 || slot >= num_slots || !pos_ok) {
+    if (sub == 0 && g == 0 && err != nullptr && (slot < 0 || slot >= num_slots)) atomicAdd(err, 1);
+    return;
+  }
+  bf16* kd = k_cache + (slot * nkv + g) * int64_t(HD);
+  bf16* vd = v_cache + (slot * nkv + g) * int64_t(HD);
+  store16(kd + i0, y1);
+  store16(kd + HALF + i0, y2);
+  const bf16* vs = src + int64_t(nkv_l) * HD;                                // v: bit copy
+  *reinterpret_cast<uint4*>(vd + 2 * i0) = *reinterpret_cast<const uint4*>(vs + 2 * i0);
+  *reinterpret_cast<uint4*>(vd + 2 * i0 + 8) = *reinterpret_cast<const uint4*>(vs + 2 * i0 + 8);
+}
+
+// ===========================================================================
 // SiluAndMul  ([SK] §4): out[:, r*I_l + j] = silu(gate_r[j]) * up_r[j]
 // ===========================================================================
 template <typename T>
@@ -455,6 +543,19 @@ extern "C" int qw_qkv_norm_rope_store_kv(const void* qkv, int64_t T, int n_heads
     return set_error(QW_ERR_INVALID_ARG, "qw_qkv_norm_rope_store_kv: null pointer");
   const int ppl = (head_dim / 2 + 31) / 32;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool aligned = (reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(q_out) |
+                        reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+                        reinterpret_cast<uintptr_t>(cos_sin) | reinterpret_cast<uintptr_t>(q_gamma) |
+                        reinterpret_cast<uintptr_t>(k_gamma)) % 16 == 0;
+  if (dtype == QW_BF16 && head_dim == 128 && aligned) {
+    const int64_t threads = T * (n_heads + n_kv_heads) * 8;
+    launch_pdl(qkv_norm_rope_hd128_kernel, unsigned((threads + 255) / 256), 256, 0, st,
+               static_cast<const bf16*>(qkv), T, n_heads, n_kv_heads, tp, positions, cos_sin, max_position,
+               static_cast<const bf16*>(q_gamma), static_cast<const bf16*>(k_gamma), eps, slot_mapping,
+               static_cast<bf16*>(k_cache), static_cast<bf16*>(v_cache), num_slots, static_cast<bf16*>(q_out),
+               err_count);
+    return check_launch("qw_qkv_norm_rope_store_kv");
+  }
   if (dtype == QW_BF16)
     launch_qkv_rope<bf16>(ppl, qkv, T, n_heads, n_kv_heads, head_dim, tp, positions, cos_sin, max_position, q_gamma,
                           k_gamma, eps, slot_mapping, k_cache, v_cache, num_slots, q_out, err_count, st);
