@@ -152,9 +152,11 @@ int qw_qkv_norm_rope_store_kv(const void* qkv, int64_t T, int n_heads, int n_kv_
  * Causal varlen GQA attention for prefill (flash_attn_varlen_func with
  * causal=True, [SK] §7.2).
  *   q   dtype [Tq, nh, hd], sequences packed by cu_seqlens_q (int32 [n_seqs+1])
- *   k,v dtype [rows, nkv, hd]: key j of sequence s is row seq_base[s] + j when
- *       seq_base (int32 [n_seqs]) is given (keys read from the KV cache),
- *       else row cu_seqlens_k[s] + j (packed keys).
+ *   k,v dtype [kv_rows, nkv, hd] (16-byte aligned): key j of sequence s is row
+ *       seq_base[s] + j when seq_base (int32 [n_seqs]) is given (keys read
+ *       from the KV cache), else row cu_seqlens_k[s] + j (packed keys); every
+ *       row read must be < kv_rows (the bf16 head_dim-128 path reads k and v
+ *       through TMA tensor maps bounded by kv_rows).
  *   cu_seqlens_k int32 [n_seqs+1]: Lk_s = cu_seqlens_k[s+1] - cu_seqlens_k[s] >= Lq_s;
  *       query i of sequence s sits at key position Lk_s - Lq_s + i and sees
  *       keys 0 .. that position.
@@ -163,9 +165,9 @@ int qw_qkv_norm_rope_store_kv(const void* qkv, int64_t T, int n_heads, int n_kv_
  * Rules: nh % nkv == 0; hd == 128 (bf16, tensor-core path) or hd <= 64 (bf16 or
  * f32, CUDA-core path).
  */
-int qw_attention_prefill(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
-                         const int32_t* cu_seqlens_k, const int32_t* seq_base, int n_seqs,
-                         int max_seqlen_q, int n_heads, int n_kv_heads, int head_dim, float scale,
+int qw_attention_prefill(const void* q, const void* k, const void* v, int64_t kv_rows,
+                         const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* seq_base,
+                         int n_seqs, int max_seqlen_q, int n_heads, int n_kv_heads, int head_dim, float scale,
                          void* out, int dtype, void* stream);
 
 /*

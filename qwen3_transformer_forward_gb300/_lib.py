@@ -34,7 +34,7 @@ SIGNATURES = {
     "qw_rope_cos_sin_table": (C.c_int, [_p, _i64, _i32, _f64]),
     "qw_qkv_norm_rope_store_kv": (C.c_int, [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _i64, _p, _p, _f32, _p, _p,
                                             _p, _i64, _p, _p, _i32, _p]),
-    "qw_attention_prefill": (C.c_int, [_p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _i32, _p]),
+    "qw_attention_prefill": (C.c_int, [_p, _p, _p, _i64, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _i32, _p]),
     "qw_attention_decode": (C.c_int, [_p, _p, _p, _i64, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _p, _sz,
                                       _i32, _p]),
     "qw_attention_decode_workspace_size": (C.c_size_t, [_i32, _i32, _i32, _i32]),
@@ -163,7 +163,7 @@ def attention_prefill(q, k, v, cu_seqlens_q, cu_seqlens_k, seq_base, max_seqlen_
                       scale, out, stream=None):
     n_seqs = cu_seqlens_q.shape[0] - 1
     _check(load().qw_attention_prefill(
-        _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(cu_seqlens_q, "cu_seqlens_q"),
+        _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), k.shape[0], _dev_ptr(cu_seqlens_q, "cu_seqlens_q"),
         _dev_ptr(cu_seqlens_k, "cu_seqlens_k"), _dev_ptr(seq_base, "seq_base"), n_seqs, max_seqlen_q, n_heads,
         n_kv_heads, head_dim, scale, _dev_ptr(out, "out"), dtype_code(q.dtype), _stream(stream)))
 

@@ -1,18 +1,14 @@
-// Causal GQA attention of the Qwen3 forward pass ([SK] §7.2): prefill over
-// packed variable-length sequences and decode over the KV cache.
-//
-// Prefill (bf16, head_dim 128): flash-attention style online softmax.  One
-// CTA of 8 warps owns 128 queries of one (sequence, q head); K/V tiles of 64
-// keys are double-buffered in XOR-swizzled shared memory with cp.async; QK^T
-// and PV run on the tensor cores (mma.sync m16n8k16, fp32 accumulate); the
-// softmax is fp32 in registers (exp2 with the scale folded in).
+// Causal GQA attention of the Qwen3 forward pass ([SK] §7.2): the CUDA-core
+// path for small head_dim (prefill and decode) and decode over the KV cache.
+// (Prefill with head_dim 128 runs on tcgen05 tensor cores: attention_prefill.cu.)
 //
 // Decode (head_dim 128): split-KV.  One CTA of 128 threads owns one
 // (sequence, kv head, key chunk) and all q heads of that GQA group, so each
-// cached K/V byte is read once.  K/V tiles of 64 keys stream through shared
-// memory (cp.async double buffer); partial (m, l, o) per chunk go to the
-// caller's workspace and the last chunk of a (sequence, kv head) to finish
-// (an atomic completion counter) merges them and writes the output.
+// cached K/V byte is read once.  K/V tiles stream through shared memory (a
+// TMA ring for bf16, cp.async double buffer for f32); partial (m, l, o) per
+// chunk go to the caller's workspace and the last chunk of a (sequence, kv
+// head) to finish (an atomic completion counter) merges them and writes the
+// output.
 #include <math.h>
 
 #include <mutex>
@@ -45,188 +41,6 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// rows of 128 bf16 (256 B = 16 chunks of 16 B); chunk c of row r is stored at
-// chunk c ^ (r & 7) so that 8 consecutive rows at one chunk hit 8 bank groups
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return uint32_t(row) * 256u + uint32_t(chunk ^ (row & 7)) * 16u;
-}
-
-constexpr int PF_BR = 128, PF_BC = 64, PF_HD = 128, PF_THREADS = 256;
-constexpr size_t PF_SMEM = size_t(PF_BR) * 256 + 2 * 2 * size_t(PF_BC) * 256;   // Q + 2 x (K, V)
-
-__global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16_kernel(
-    const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
-    const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, const int32_t* __restrict__ seq_base,
-    int nh, int nkv, float scale_log2, bf16* __restrict__ out) {
-  pdl_trigger();   // the next kernel may start its prologue
-  pdl_wait();      // inputs of this kernel are complete and visible
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* sQ = smem;
-  uint8_t* sK = smem + PF_BR * 256;
-  uint8_t* sV = sK + 2 * PF_BC * 256;
-  const int s = blockIdx.z, h = blockIdx.y;
-  const int qs = cu_q[s];
-  const int Lq = cu_q[s + 1] - qs;
-  const int Lk = cu_k[s + 1] - cu_k[s];
-  const int n_qt = (Lq + PF_BR - 1) / PF_BR;
-  const int qt = int(gridDim.x) - 1 - int(blockIdx.x);   // longest (causal) tiles first
-  if (qt >= n_qt) return;
-  const int g = h / (nh / nkv);
-  const int64_t kbase = seq_base != nullptr ? int64_t(seq_base[s]) : int64_t(cu_k[s]);
-  const int offset = Lk - Lq;
-  const int q_lo = qt * PF_BR;
-  const int q_hi = min(Lq, q_lo + PF_BR);
-  const int kv_end = min(Lk, offset + q_hi);
-  const int n_kt = (kv_end + PF_BC - 1) / PF_BC;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t qrow_stride = int64_t(nh) * PF_HD;
-  const int64_t krow_stride = int64_t(nkv) * PF_HD;
-
-  // Q tile (rows past the sequence end are zero)
-  for (int i = tid; i < PF_BR * 16; i += PF_THREADS) {
-    const int r = i >> 4, c = i & 15;
-    const int qi = q_lo + r;
-    const bool ok = qi < Lq;
-    const bf16* src = q + (int64_t(qs) + (ok ? qi : 0)) * qrow_stride + int64_t(h) * PF_HD + c * 8;
-    cp_async16_zfill(smem_u32(sQ) + swz(r, c), src, ok);
-  }
-  auto load_kv = [&](int kt, int buf) {
-    for (int i = tid; i < PF_BC * 16; i += PF_THREADS) {
-      const int r = i >> 4, c = i & 15;
-      const int kj = kt * PF_BC + r;
-      const bool ok = kj < kv_end;
-      const int64_t row = kbase + (ok ? kj : 0);
-      const int64_t off = row * krow_stride + int64_t(g) * PF_HD + c * 8;
-      cp_async16_zfill(smem_u32(sK + buf * PF_BC * 256) + swz(r, c), k + off, ok);
-      cp_async16_zfill(smem_u32(sV + buf * PF_BC * 256) + swz(r, c), v + off, ok);
-    }
-  };
-  if (n_kt > 0) load_kv(0, 0);
-  cp_async_commit();
-
-  const int gq = lane >> 2, tq = lane & 3;       // mma fragment coordinates
-  const int mi = lane >> 3, ri = lane & 7;       // ldmatrix matrix / row index
-  float o[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.0f, 0.0f};
-  uint32_t qf[8][4];
-  const int row0 = warp * 16;
-  const int qpos0 = offset + q_lo + row0 + gq;   // key position of this thread's first row (second: +8)
-
-  for (int kt = 0; kt < n_kt; ++kt) {
-    const int buf = kt & 1;
-    if (kt + 1 < n_kt) load_kv(kt + 1, buf ^ 1);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    if (kt == 0) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        ldsm_x4(smem_u32(sQ) + swz(row0 + ri + 8 * (mi & 1), 2 * kk + (mi >> 1)), qf[kk][0], qf[kk][1], qf[kk][2],
-                qf[kk][3]);
-    }
-    const uint32_t kb = smem_u32(sK + buf * PF_BC * 256);
-    const uint32_t vb = smem_u32(sV + buf * PF_BC * 256);
-    // S = Q K^T : 16 x 64 per warp
-    float sc[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.0f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int jp = 0; jp < 4; ++jp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + swz(16 * jp + ri + 8 * (mi >> 1), 2 * kk + (mi & 1)), b0, b1, b2, b3);
-        mma_bf16(sc[2 * jp], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
-        mma_bf16(sc[2 * jp + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
-      }
-    }
-    // scale, causal mask, online softmax
-    const int kpos0 = kt * PF_BC;
-    const bool need_mask = (kpos0 + PF_BC > offset + q_lo + row0) || (kpos0 + PF_BC > kv_end);
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float x = sc[j][e] * scale_log2;
-        if (need_mask) {
-          const int kp = kpos0 + 8 * j + 2 * tq + (e & 1);
-          const int qp = qpos0 + (e >> 1) * 8;
-          if (kp > qp || kp >= kv_end) x = -INFINITY;
-        }
-        sc[j][e] = x;
-        mx[e >> 1] = fmaxf(mx[e >> 1], x);
-      }
-    }
-    float alpha[2], m_use[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      const float m_new = fmaxf(m_run[r], mx[r]);
-      m_use[r] = m_new == -INFINITY ? 0.0f : m_new;
-      alpha[r] = exp2f(m_run[r] - m_use[r]);
-      m_run[r] = m_new;
-      l_run[r] *= alpha[r];
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p = exp2f(sc[j][e] - m_use[e >> 1]);
-        sc[j][e] = p;
-        l_run[e >> 1] += p;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i][0] *= alpha[0];
-      o[i][1] *= alpha[0];
-      o[i][2] *= alpha[1];
-      o[i][3] *= alpha[1];
-    }
-    // O += P V
-#pragma unroll
-    for (int kc = 0; kc < 4; ++kc) {
-      const uint32_t a0 = pack_bf16(sc[2 * kc][0], sc[2 * kc][1]);
-      const uint32_t a1 = pack_bf16(sc[2 * kc][2], sc[2 * kc][3]);
-      const uint32_t a2 = pack_bf16(sc[2 * kc + 1][0], sc[2 * kc + 1][1]);
-      const uint32_t a3 = pack_bf16(sc[2 * kc + 1][2], sc[2 * kc + 1][3]);
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb + swz(16 * kc + ri + 8 * (mi & 1), 2 * dp + (mi >> 1)), b0, b1, b2, b3);
-        mma_bf16(o[2 * dp], a0, a1, a2, a3, b0, b1);
-        mma_bf16(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
-      }
-    }
-    __syncthreads();
-  }
-  cp_async_wait<0>();
-  // normalise and store
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
-  }
-  const float inv0 = l_run[0] > 0.0f ? 1.0f / l_run[0] : 0.0f;
-  const float inv1 = l_run[1] > 0.0f ? 1.0f / l_run[1] : 0.0f;
-  const int qi0 = q_lo + row0 + gq, qi1 = qi0 + 8;
-#pragma unroll
-  for (int dn = 0; dn < 16; ++dn) {
-    const int d = 8 * dn + 2 * tq;
-    if (qi0 < Lq)
-      *reinterpret_cast<uint32_t*>(out + (int64_t(qs) + qi0) * qrow_stride + int64_t(h) * PF_HD + d) =
-          pack_bf16(o[dn][0] * inv0, o[dn][1] * inv0);
-    if (qi1 < Lq)
-      *reinterpret_cast<uint32_t*>(out + (int64_t(qs) + qi1) * qrow_stride + int64_t(h) * PF_HD + d) =
-          pack_bf16(o[dn][2] * inv1, o[dn][3] * inv1);
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -812,10 +626,16 @@ inline DecodePlan decode_plan(int B, int max_context, int nkv_unused) {
 using namespace qw;
 using namespace qw::attn;
 
-extern "C" int qw_attention_prefill(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
-                                    const int32_t* cu_seqlens_k, const int32_t* seq_base, int n_seqs,
-                                    int max_seqlen_q, int n_heads, int n_kv_heads, int head_dim, float scale,
-                                    void* out, int dtype, void* stream) {
+namespace qw {
+int launch_attention_prefill_tc(const void* q, const void* k, const void* v, int64_t kv_rows, const int32_t* cu_q,
+                                const int32_t* cu_k, const int32_t* seq_base, int n_seqs, int max_seqlen_q, int nh,
+                                int nkv, float scale, void* out, cudaStream_t st);
+}  // namespace qw
+
+extern "C" int qw_attention_prefill(const void* q, const void* k, const void* v, int64_t kv_rows,
+                                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* seq_base,
+                                    int n_seqs, int max_seqlen_q, int n_heads, int n_kv_heads, int head_dim,
+                                    float scale, void* out, int dtype, void* stream) {
   if (dtype != QW_BF16 && dtype != QW_F32) return set_error(QW_ERR_DTYPE, "qw_attention_prefill: dtype %d", dtype);
   if (n_seqs < 0 || max_seqlen_q < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0)
     return set_error(QW_ERR_INVALID_ARG, "qw_attention_prefill: bad sizes");
@@ -827,18 +647,10 @@ extern "C" int qw_attention_prefill(const void* q, const void* k, const void* v,
     return set_error(QW_ERR_INVALID_ARG, "qw_attention_prefill: null pointer");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == QW_BF16 && head_dim == 128) {
-    static bool configured = false;
-    if (!configured) {
-      cudaError_t e = cudaFuncSetAttribute(attn_prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           int(PF_SMEM));
-      if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-      configured = true;
-    }
-    dim3 grid(unsigned((max_seqlen_q + PF_BR - 1) / PF_BR), unsigned(n_heads), unsigned(n_seqs));
-    launch_pdl(attn_prefill_bf16_kernel, grid, PF_THREADS, PF_SMEM, st, 
-        static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v), cu_seqlens_q,
-        cu_seqlens_k, seq_base, n_heads, n_kv_heads, scale * kLog2e, static_cast<bf16*>(out));
-    return check_launch("attn_prefill_bf16_kernel");
+    if (kv_rows <= 0 || (reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16)
+      return set_error(QW_ERR_INVALID_ARG, "qw_attention_prefill: kv_rows must be > 0 and k, v 16-byte aligned");
+    return launch_attention_prefill_tc(q, k, v, kv_rows, cu_seqlens_q, cu_seqlens_k, seq_base, n_seqs, max_seqlen_q,
+                                       n_heads, n_kv_heads, scale, out, st);
   }
   if (dtype == QW_BF16)
     return launch_attn_small<bf16>(q, k, v, cu_seqlens_q, cu_seqlens_k, seq_base, nullptr, n_seqs, max_seqlen_q,

@@ -38,17 +38,19 @@ bool pdl_enabled() {
 // defined next to the kernels that own a bounded-wait error word
 unsigned int take_tc_timeouts();
 unsigned int take_attn_timeouts();
+unsigned int take_prefill_timeouts();
 
 }  // namespace qw
 
-extern "C" int qw_abi_version(void) { return 2; }
+extern "C" int qw_abi_version(void) { return 3; }
 
 extern "C" const char* qw_last_error_string(void) { return qw::g_last_error.c_str(); }
 
 extern "C" int qw_device_error(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return qw::set_error(QW_ERR_CUDA, "qw_device_error: %s", cudaGetErrorString(e));
-  const unsigned int t = qw::take_tc_timeouts() | (qw::take_attn_timeouts() << 8);
+  const unsigned int t =
+      qw::take_tc_timeouts() | (qw::take_attn_timeouts() << 8) | (qw::take_prefill_timeouts() << 16);
   if (t) return qw::set_error(QW_ERR_TIMEOUT, "a tensor-core pipeline wait timed out (code 0x%x)", t);
   return QW_OK;
 }

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.qw_abi_version() == 2
+    assert lib.qw_abi_version() == 3
 
 
 def test_argument_errors_are_reported_before_launch(lib):
@@ -69,9 +69,9 @@ def test_argument_errors_are_reported_before_launch(lib):
     assert lib.qw_gemm(fake, fake, fake, 4, 60, 64, 1, L.QW_GEMM_COLUMN, 0, None, 0, L.QW_BF16,
                        None) == L.QW_ERR_SHAPE
     # attention: head_dim must be 128 (bf16) or <= 64; decode group must be 1/2/4/8
-    assert lib.qw_attention_prefill(fake, fake, fake, fake, fake, None, 2, 8, 16, 8, 96, 0.1, fake, L.QW_BF16,
+    assert lib.qw_attention_prefill(fake, fake, fake, 64, fake, fake, None, 2, 8, 16, 8, 96, 0.1, fake, L.QW_BF16,
                                     None) == L.QW_ERR_SHAPE
-    assert lib.qw_attention_prefill(fake, fake, fake, fake, fake, None, 2, 8, 16, 8, 128, 0.1, fake, L.QW_F32,
+    assert lib.qw_attention_prefill(fake, fake, fake, 64, fake, fake, None, 2, 8, 16, 8, 128, 0.1, fake, L.QW_F32,
                                     None) == L.QW_ERR_SHAPE
     assert lib.qw_attention_decode(fake, fake, fake, 100, fake, fake, 2, 8, 12, 4, 128, 0.1, fake, None, 0,
                                    L.QW_BF16, None) == L.QW_ERR_SHAPE

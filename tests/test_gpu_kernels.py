@@ -285,16 +285,25 @@ def _attn_tol(ref, v):
     return 2.0 * bf16_ulp(ref) + 2.0 ** -9 * np.max(np.abs(v)) + 1e-6
 
 
-@pytest.mark.parametrize("seq_lens", [[1, 77, 200, 129], [512, 512], [3]])
-def test_attention_prefill_bf16_from_cache(L, seq_lens):
-    nh, nkv, hd = 16, 8, 128
+@pytest.mark.parametrize("seq_lens,nh,nkv,poison", [
+    ([1, 77, 200, 129], 16, 8, False),
+    ([512, 512], 16, 8, False),
+    ([3], 16, 8, False),
+    ([1, 77, 200, 129], 16, 8, True),     # cache rows outside the sequences hold NaN
+    ([300, 1000, 5], 8, 8, True),         # group size 1: two query tiles of one head per CTA
+    ([129, 384], 6, 2, False),            # odd group size 3
+    ([640, 33], 16, 4, False),            # group size 4
+])
+def test_attention_prefill_bf16_from_cache(L, seq_lens, nh, nkv, poison):
+    hd = 128
     b = si.prefill_batch(si.QWEN3_0_6B, seq_lens, extra_capacity=5)
     T = sum(seq_lens)
     q = si.normal(0, "a.q", (T, nh, hd), 1.0, "bf16")
     k = si.normal(0, "a.k", (T, nkv, hd), 1.0, "bf16")
     v = si.normal(0, "a.v", (T, nkv, hd), 1.0, "bf16")
-    kc = torch.zeros(b.num_slots, nkv, hd, dtype=torch.bfloat16)
-    vc = torch.zeros(b.num_slots, nkv, hd, dtype=torch.bfloat16)
+    fill = float("nan") if poison else 0.0
+    kc = torch.full((b.num_slots, nkv, hd), fill, dtype=torch.bfloat16)
+    vc = torch.full((b.num_slots, nkv, hd), fill, dtype=torch.bfloat16)
     kc[b.slot_mapping] = k
     vc[b.slot_mapping] = v
     out = torch.empty(T, nh * hd, dtype=torch.bfloat16, device="cuda")
@@ -306,8 +315,31 @@ def test_attention_prefill_bf16_from_cache(L, seq_lens):
                               hd ** -0.5, "bf16")
     got = to_np(out).reshape(T, nh, hd)
     err = np.abs(got - ref)
-    assert np.all(err <= _attn_tol(ref, v.double().numpy())), float(err.max())
+    assert np.all(err <= _attn_tol(ref, v.double().numpy())), float(np.nanmax(err))
     assert float(np.mean(err)) < 2e-3
+
+
+def test_attention_prefill_growing_scores(L):
+    """Keys whose norm grows along the sequence: each query's running max keeps
+    rising from one key tile to the next, so the kernel's output must not
+    depend on when (or whether) it re-bases its softmax accumulators."""
+    nh, nkv, hd = 16, 8, 128
+    seq_lens = [900, 260]
+    b = si.prefill_batch(si.QWEN3_0_6B, seq_lens)
+    T = sum(seq_lens)
+    q = si.normal(0, "ag.q", (T, nh, hd), 2.0, "bf16")
+    k = si.normal(0, "ag.k", (T, nkv, hd), 1.0, "f32")
+    pos = b.positions.to(torch.float32)
+    k = (k * (1.0 + pos / 64.0)[:, None, None]).to(torch.bfloat16)
+    v = si.normal(0, "ag.v", (T, nkv, hd), 1.0, "bf16")
+    out = torch.empty(T, nh * hd, dtype=torch.bfloat16, device="cuda")
+    cu = dev(b.cu_seqlens)
+    L.attention_prefill(dev(q), dev(k), dev(v), cu, cu, None, max(seq_lens), nh, nkv, hd, hd ** -0.5, out)
+    sync_ok(L)
+    ref = O.attention_prefill(q.double().numpy(), k.double().numpy(), v.double().numpy(), b.cu_seqlens.numpy(),
+                              hd ** -0.5, "bf16")
+    got = to_np(out).reshape(T, nh, hd)
+    assert np.all(np.abs(got - ref) <= _attn_tol(ref, v.double().numpy()))
 
 
 def test_attention_prefill_packed_and_prefix(L):
