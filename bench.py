@@ -288,6 +288,11 @@ class Workload:
             "decode.attention": ("hbm", 2.0 * 2 * nkv * hd * B * mean_ctx + 2.0 * 2 * B * nh * hd),
             "decode.add_rmsnorm": ("hbm", 2.0 * B * H * 4),
             "decode.qkv_norm_rope_store_kv": ("hbm", 2.0 * B * (qkvw + nh * hd + 2 * nkv * hd) + 16.0 * B),
+            # one persistent kernel per decode step: every layer's weights, the K/V
+            # rows each sequence attends to, the new K/V rows, the activations
+            "decode.layers": ("hbm", m.n_layers * (2.0 * (qkvw * H + H * nh * hd + 2 * I * H + H * I)
+                                                   + 2.0 * 2 * nkv * hd * B * mean_ctx + 2.0 * 2 * nkv * hd * B
+                                                   + 2.0 * B * (4 * H + qkvw + nh * hd + I))),
             "lm_head": ("hbm", 2.0 * V * H + 2.0 * B * V),
             "embed_vocab": ("hbm", 2.0 * 2 * T * H + 8.0 * T),
         }
@@ -298,6 +303,8 @@ class Workload:
         base = kind.split(".", 1)[-1]
         if kind in ("lm_head", "embed_vocab"):
             return 1 + self.S
+        if kind == "decode.layers":
+            return self.S
         n = per_layer.get(base, 1) * nl
         return n * (self.S if kind.startswith("decode.") else 1)
 
@@ -436,7 +443,10 @@ def count_launches(wl):
     # split-K sums and the split-KV merge happen inside the GEMM and attention kernels
     prefill = 1 + m.n_layers * per_layer + 1 + 3     # embed, layers, final norm, gather + gemm + argmax
     lm_dec = 2                                       # gemm + argmax
-    decode = 1 + m.n_layers * per_layer + 1 + lm_dec
+    if wl.fwd.fused_decode_ok(wl.B):
+        decode = 1 + 1 + lm_dec                      # embed, all layers in one kernel, lm_head
+    else:
+        decode = 1 + m.n_layers * per_layer + 1 + lm_dec
     return prefill + wl.S * decode
 
 

@@ -275,6 +275,61 @@ size_t qw_lm_head_workspace_size(int64_t n_out, int64_t V, int64_t H, int tp, in
 /* Greedy argmax over rows of logits dtype [M, V] -> int64 [M], lowest index on ties. */
 int qw_argmax(const void* logits, int64_t M, int64_t V, int64_t* out, int dtype, void* stream);
 
+/*
+ * One decode step of every decoder layer in one persistent kernel: for each
+ * layer, in the order of Qwen3DecoderLayer.forward ([SK] §1, §8):
+ *   add + RMSNorm (input_layernorm) -> QKV (column layout) -> QK-RMSNorm,
+ *   RoPE, KV-cache store -> decode attention over the cache -> o_proj (row
+ *   layout, shard sums) -> add + RMSNorm (post_attention_layernorm) ->
+ *   gate_up (column) + SiluAndMul -> down (row)
+ * and then the final add + RMSNorm.  Same arithmetic, layouts and rounding
+ * points as the per-operation entry points above; it exists because a
+ * decode batch of a few tokens leaves each operation far too small to fill
+ * the GPU on its own.
+ *   layers   host array of n_layers qw_decode_layer records (pointers into
+ *            device memory; the layouts of qw_gemm / qw_qkv_norm_rope_store_kv),
+ *            read during the call; the K/V caches 16-byte aligned
+ *   x        bf16 [B, H]: the embedding of the B new tokens (layer 0 input)
+ *   positions, slot_mapping int64 [B]; context_lens, seq_base int32 [B]:
+ *            as for qw_qkv_norm_rope_store_kv and qw_attention_decode (the new
+ *            token's k/v go to slot_mapping[b], which must be
+ *            seq_base[b] + context_lens[b] - 1; max_context >= every
+ *            context_lens[b])
+ *   cos_sin  fp32 [max_position, head_dim] (qw_rope_cos_sin_table)
+ *   final_norm bf16 [H];  out bf16 [B, H]: final normed hidden (lm_head input)
+ *   err_count int32 [1] or NULL: +1 per position or slot out of range
+ *   workspace: qw_decode_layers_workspace_size(...) bytes, 16-byte aligned,
+ *            zero when first used.  Every call leaves its first 64 KiB (grid
+ *            barrier, counters) as a following call needs them; after a call
+ *            that qw_device_error reports as timed out, zero it again.
+ * Rules: bf16; 1 <= B <= 16; head_dim 128; nh/nkv in {1, 2, 4, 8}; nh, nkv
+ * and I divisible by tp; H, nh*128/tp and I/tp multiples of 256;
+ * n_layers <= 64.  Launched cooperatively with one CTA per SM: calls on
+ * different streams must not overlap.  Errors: QW_ERR_SHAPE,
+ * QW_ERR_INVALID_ARG, QW_ERR_WORKSPACE, QW_ERR_CUDA.
+ */
+typedef struct qw_decode_layer {
+  const void* input_layernorm;           /* bf16 [H] */
+  const void* qkv;                       /* bf16 [tp * (nh/tp + 2*nkv/tp) * hd, H] */
+  const void* q_norm;                    /* bf16 [hd] */
+  const void* k_norm;                    /* bf16 [hd] */
+  const void* o_proj;                    /* bf16 [tp, H, nh/tp * hd] */
+  const void* post_attention_layernorm;  /* bf16 [H] */
+  const void* gate_up;                   /* bf16 [tp * 2*I/tp, H] */
+  const void* down;                      /* bf16 [tp, H, I/tp] */
+  void* k_cache;                         /* bf16 [num_slots, nkv, hd] */
+  void* v_cache;                         /* bf16 [num_slots, nkv, hd] */
+} qw_decode_layer;
+
+int qw_decode_layers(const qw_decode_layer* layers, int n_layers, const void* x, const int64_t* positions,
+                     const int64_t* slot_mapping, const int32_t* context_lens, const int32_t* seq_base, int B,
+                     int max_context, int H, int n_heads, int n_kv_heads, int head_dim, int intermediate, int tp,
+                     const float* cos_sin, int64_t max_position, int64_t num_slots, float eps, float scale,
+                     const void* final_norm, void* out, int32_t* err_count, void* workspace,
+                     size_t workspace_bytes, void* stream);
+size_t qw_decode_layers_workspace_size(int n_layers, int B, int H, int n_heads, int n_kv_heads, int head_dim,
+                                       int intermediate, int tp, int max_context);
+
 #ifdef __cplusplus
 }
 #endif

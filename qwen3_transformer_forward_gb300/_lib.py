@@ -47,7 +47,14 @@ SIGNATURES = {
     "qw_lm_head": (C.c_int, [_p, _i64, _p, _i64, _p, _i64, _i64, _i32, _p, _p, _p, _sz, _i32, _p]),
     "qw_lm_head_workspace_size": (C.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
     "qw_argmax": (C.c_int, [_p, _i64, _i64, _p, _i32, _p]),
+    "qw_decode_layers": (C.c_int, [_p, _i32, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _p,
+                                   _i64, _i64, _f32, _f32, _p, _p, _p, _p, _sz, _p]),
+    "qw_decode_layers_workspace_size": (C.c_size_t, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
 }
+
+# field order of qw_decode_layer (include/qw.h)
+DECODE_LAYER_FIELDS = ("input_layernorm", "qkv", "q_norm", "k_norm", "o_proj", "post_attention_layernorm", "gate_up",
+                       "down", "k_cache", "v_cache")
 
 
 class QwError(RuntimeError):
@@ -231,3 +238,36 @@ def argmax(logits, out, stream=None):
     M, V = logits.shape
     _check(load().qw_argmax(_dev_ptr(logits, "logits"), M, V, _dev_ptr(out, "out"), dtype_code(logits.dtype),
                             _stream(stream)))
+
+
+class DecodeLayer(C.Structure):
+    """qw_decode_layer (include/qw.h): one layer's device pointers."""
+    _fields_ = [(f, C.c_void_p) for f in DECODE_LAYER_FIELDS]
+
+
+def decode_layer_table(layers):
+    """Host array of qw_decode_layer records: one dict of CUDA tensors per
+    layer (keys DECODE_LAYER_FIELDS).  The tensors must outlive its use."""
+    arr = (DecodeLayer * len(layers))()
+    for i, lw in enumerate(layers):
+        for f in DECODE_LAYER_FIELDS:
+            setattr(arr[i], f, _dev_ptr(lw[f], f))
+    return arr
+
+
+def decode_layers_workspace_size(n_layers, B, H, n_heads, n_kv_heads, head_dim, intermediate, tp, max_context) -> int:
+    return load().qw_decode_layers_workspace_size(n_layers, B, H, n_heads, n_kv_heads, head_dim, intermediate, tp,
+                                                  max_context)
+
+
+def decode_layers(table, n_layers, x, positions, slot_mapping, context_lens, seq_base, max_context, n_heads,
+                  n_kv_heads, head_dim, intermediate, tp, cos_sin, num_slots, eps, scale, final_norm, out,
+                  workspace, err_count=None, stream=None):
+    B, H = x.shape
+    _check(load().qw_decode_layers(
+        C.cast(table, C.c_void_p), n_layers, _dev_ptr(x, "x"), _dev_ptr(positions, "positions"),
+        _dev_ptr(slot_mapping, "slot_mapping"), _dev_ptr(context_lens, "context_lens"), _dev_ptr(seq_base, "seq_base"),
+        B, max_context, H, n_heads, n_kv_heads, head_dim, intermediate, tp, _dev_ptr(cos_sin, "cos_sin"),
+        cos_sin.shape[0], num_slots, eps, scale, _dev_ptr(final_norm, "final_norm"), _dev_ptr(out, "out"),
+        _dev_ptr(err_count, "err_count"), _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))

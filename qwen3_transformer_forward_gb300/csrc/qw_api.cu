@@ -39,6 +39,7 @@ bool pdl_enabled() {
 unsigned int take_tc_timeouts();
 unsigned int take_attn_timeouts();
 unsigned int take_prefill_timeouts();
+unsigned int take_dstep_errors();
 
 }  // namespace qw
 
@@ -49,8 +50,12 @@ extern "C" const char* qw_last_error_string(void) { return qw::g_last_error.c_st
 extern "C" int qw_device_error(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return qw::set_error(QW_ERR_CUDA, "qw_device_error: %s", cudaGetErrorString(e));
-  const unsigned int t =
-      qw::take_tc_timeouts() | (qw::take_attn_timeouts() << 8) | (qw::take_prefill_timeouts() << 16);
-  if (t) return qw::set_error(QW_ERR_TIMEOUT, "a tensor-core pipeline wait timed out (code 0x%x)", t);
+  const unsigned int gemm = qw::take_tc_timeouts(), dec = qw::take_attn_timeouts(),
+                     pre = qw::take_prefill_timeouts(), step = qw::take_dstep_errors();
+  if (gemm | dec | pre | step)
+    return qw::set_error(QW_ERR_TIMEOUT,
+                         "a bounded device-side wait timed out (gemm 0x%x, decode attention 0x%x, prefill attention "
+                         "0x%x, decode step 0x%x)",
+                         gemm, dec, pre, step);
   return QW_OK;
 }

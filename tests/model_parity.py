@@ -30,7 +30,8 @@ def decode_meta(seq_lens, step: int, extra: int):
     return pos, (pos + 1).astype(np.int32), base + pos, base.astype(np.int32)
 
 
-def run_gpu(m, seq_lens, decode_steps: int, params=None, forced=None, device="cuda") -> Trace:
+def run_gpu(m, seq_lens, decode_steps: int, params=None, forced=None, device="cuda", fused_decode=False,
+            fwd_out=None) -> Trace:
     from qwen3_transformer_forward_gb300 import model as M
     from qwen3_transformer_forward_gb300 import _lib as L
     params = params or M.load_params(m, device=device)
@@ -38,6 +39,9 @@ def run_gpu(m, seq_lens, decode_steps: int, params=None, forced=None, device="cu
     B = len(seq_lens)
     fwd = M.Qwen3Forward(m, params, max_tokens=sum(seq_lens), num_slots=b.num_slots, max_seqs=B,
                          max_context=max(seq_lens) + decode_steps)
+    fwd.fused_decode = fused_decode
+    if fwd_out is not None:
+        fwd_out.append(fwd)
     ctx = M.to_device_prefill(b, device)
     hid, log, tok = [], [], []
     h = fwd.run_layers(ctx, decode=False)

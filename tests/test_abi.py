@@ -80,6 +80,13 @@ def test_argument_errors_are_reported_before_launch(lib):
     assert need > 0
     assert lib.qw_attention_decode(fake, fake, fake, 100, fake, fake, 8, 4096, 16, 8, 128, 0.1, fake, None, 0,
                                    L.QW_BF16, None) == L.QW_ERR_WORKSPACE
+    # one-kernel decode step: at most 16 tokens, head_dim 128, group size 1/2/4/8
+    args = lambda B, hd, nh, nkv: (fake, 28, fake, fake, fake, fake, fake, B, 100, 1024, nh, nkv, hd, 3072, 2, fake,  # noqa: E731
+                                   4096, 100, 1e-6, 0.1, fake, fake, None, fake, 1 << 30, None)
+    assert lib.qw_decode_layers(*args(17, 128, 16, 8)) == L.QW_ERR_SHAPE
+    assert lib.qw_decode_layers(*args(8, 64, 16, 8)) == L.QW_ERR_SHAPE
+    assert lib.qw_decode_layers(*args(8, 128, 12, 4)) == L.QW_ERR_SHAPE
+    assert lib.qw_decode_layers_workspace_size(28, 17, 1024, 16, 8, 128, 3072, 2, 2048) == 0
     # lm_head: V not divisible by tp
     assert lib.qw_lm_head(fake, 4, None, 4, fake, 10, 64, 4, fake, None, None, 0, L.QW_BF16,
                           None) == L.QW_ERR_SHAPE

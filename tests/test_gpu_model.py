@@ -77,13 +77,15 @@ def test_tiny_fp32_model_prefill_and_decode():
 SMALL_BF16 = si.QWEN3_0_6B.replace(vocab=8192, n_layers=3, tp=2, gamma_sigma=0.1)
 
 
-@pytest.mark.parametrize("tp", [1, 2])
-def test_small_bf16_model_prefill_and_decode(tp):
+@pytest.mark.parametrize("tp,fused", [(1, True), (2, True), (2, False)])
+def test_small_bf16_model_prefill_and_decode(tp, fused):
+    """fused: decode steps through the one-kernel decode step (qw_decode_layers),
+    else through the per-operation entry points."""
     m = SMALL_BF16.replace(tp=tp)
     seq_lens = [37, 130, 1, 64]
     steps = 3
     forced = forced_tokens(m, steps, len(seq_lens))
-    g = run_gpu(m, seq_lens, steps, forced=forced)
+    g = run_gpu(m, seq_lens, steps, forced=forced, fused_decode=fused)
     w = O.load_weights(m)
     o = run_oracle(m, seq_lens, steps, forced=forced, weights=w)
     with bf16_softmax_weights():
