@@ -282,6 +282,7 @@ class Workload:
             "prefill.add_rmsnorm": ("hbm", 2.0 * T * H * 4),
             "prefill.qkv_norm_rope_store_kv": ("hbm", 2.0 * T * (qkvw + nh * hd + 2 * nkv * hd) + 16.0 * T),
             "decode.gemm_qkv": ("hbm", gemm_b(B, qkvw, H)),
+            "decode.add_rmsnorm_gemm_qkv": ("hbm", gemm_b(B, qkvw, H) + 2.0 * 3 * B * H),
             "decode.gemm_o": ("hbm", gemm_b(B, H, nh * hd)),
             "decode.gemm_gate_up_silu": ("hbm", 2.0 * (2 * I * H + B * H + B * I)),
             "decode.gemm_down": ("hbm", gemm_b(B, H, I)),
@@ -299,7 +300,8 @@ class Workload:
 
     def launches_per_step(self, kind):
         nl = self.m.n_layers
-        per_layer = {"add_rmsnorm": 2}
+        fused_norm = self.fwd.norm_fusion_ok(self.B)
+        per_layer = {"add_rmsnorm": 1 if fused_norm and kind.startswith("decode.") else 2}
         base = kind.split(".", 1)[-1]
         if kind in ("lm_head", "embed_vocab"):
             return 1 + self.S
@@ -440,13 +442,15 @@ def count_launches(wl):
     from qwen3_transformer_forward_gb300 import _lib as L
     m = wl.m
     per_layer = 2 + 1 + 1 + 1 + 1 + 1 + 1   # 2 norms, qkv gemm, rope/kv, attention, o, gate_up, down
+    # decode with few tokens: the input norm runs inside the QKV GEMM
+    dec_layer = per_layer - 1 if wl.fwd.norm_fusion_ok(wl.B) else per_layer
     # split-K sums and the split-KV merge happen inside the GEMM and attention kernels
     prefill = 1 + m.n_layers * per_layer + 1 + 3     # embed, layers, final norm, gather + gemm + argmax
     lm_dec = 2                                       # gemm + argmax
     if wl.fwd.fused_decode_ok(wl.B):
         decode = 1 + 1 + lm_dec                      # embed, all layers in one kernel, lm_head
     else:
-        decode = 1 + m.n_layers * per_layer + 1 + lm_dec
+        decode = 1 + m.n_layers * dec_layer + 1 + lm_dec
     return prefill + wl.S * decode
 
 

@@ -255,6 +255,24 @@ size_t qw_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int tp, int mode,
 int qw_silu_mul(const void* x, void* out, int64_t T, int64_t I, int tp, int dtype, void* stream);
 
 /*
+ * Fused add + RMSNorm and Linear for few tokens (decode): the
+ * input_layernorm / post_attention_layernorm of Qwen3DecoderLayer feeding
+ * the QKV or gate_up projection ([SK] §1, §2, §5).  Same arithmetic and
+ * rounding points as qw_add_rmsnorm followed by qw_gemm (column layout):
+ *   s = x + residual_in (rounded to bf16; s = x when residual_in is NULL)
+ *   residual_out = s (if not NULL); y = RMSNorm(s) * gamma (rounded); C = y W^T
+ *   x, residual_in, residual_out bf16 [M, K];  gamma bf16 [K]
+ *   W bf16 [N, K] (column layout: tp shards stacked along N);  C bf16 [M, N],
+ *   or [M, N/2] with QW_EPI_SILU_MUL (gate_up, as qw_gemm)
+ * Rules: bf16; 0 <= M <= 16; K % 32 == 0, N % 16 == 0 and qw_gemm's shard
+ * rules; 16-byte aligned pointers; residual_out must not alias x or
+ * residual_in (every CTA reads them while one writes it).
+ */
+int qw_add_rmsnorm_gemm(const void* x, const void* residual_in, void* residual_out, const void* gamma, float eps,
+                        const void* W, void* C, int64_t M, int64_t N, int64_t K, int tp, int epilogue, int dtype,
+                        void* stream);
+
+/*
  * Vocab-parallel lm_head with the tied table ([VH] §4, [SK] §6, §8) and greedy
  * sampling.
  *   hidden    dtype [T, H]

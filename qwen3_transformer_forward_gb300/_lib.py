@@ -47,6 +47,7 @@ SIGNATURES = {
     "qw_lm_head": (C.c_int, [_p, _i64, _p, _i64, _p, _i64, _i64, _i32, _p, _p, _p, _sz, _i32, _p]),
     "qw_lm_head_workspace_size": (C.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
     "qw_argmax": (C.c_int, [_p, _i64, _i64, _p, _i32, _p]),
+    "qw_add_rmsnorm_gemm": (C.c_int, [_p, _p, _p, _p, _f32, _p, _p, _i64, _i64, _i64, _i32, _i32, _i32, _p]),
     "qw_decode_layers": (C.c_int, [_p, _i32, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _p,
                                    _i64, _i64, _f32, _f32, _p, _p, _p, _p, _sz, _p]),
     "qw_decode_layers_workspace_size": (C.c_size_t, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
@@ -271,3 +272,12 @@ def decode_layers(table, n_layers, x, positions, slot_mapping, context_lens, seq
         cos_sin.shape[0], num_slots, eps, scale, _dev_ptr(final_norm, "final_norm"), _dev_ptr(out, "out"),
         _dev_ptr(err_count, "err_count"), _dev_ptr(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def add_rmsnorm_gemm(x, residual_in, residual_out, gamma, eps, W, C, N, tp, epilogue=QW_EPI_NONE, stream=None):
+    """C = RMSNorm(x + residual_in) * gamma @ W^T for few tokens; residual_out = x + residual_in."""
+    M, K = x.shape
+    _check(load().qw_add_rmsnorm_gemm(
+        _dev_ptr(x, "x"), _dev_ptr(residual_in, "residual_in"), _dev_ptr(residual_out, "residual_out"),
+        _dev_ptr(gamma, "gamma"), eps, _dev_ptr(W, "W"), _dev_ptr(C, "C"), M, N, K, tp, epilogue,
+        dtype_code(x.dtype), _stream(stream)))

@@ -547,6 +547,11 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
     if (lane == 0) tcx::mbar_arrive(empty(s));
     if (tid == 0 && t + DT_STAGES < n_kt) {
       if (ok && !tcx::mbar_wait(empty(s), ph, &g_attn_timeout, 2u)) ok = false;
+      // The warps read this stage with ldmatrix (generic proxy) and the copy
+      // below overwrites it through the async proxy: the barrier alone does
+      // not order the two proxies.  Without this fence a copy was seen to land
+      // while a warp's last ldmatrix (V dims 112-127) was still pending.
+      tcx::fence_proxy_async();
       if (ok) issue(t + DT_STAGES);
     }
   }

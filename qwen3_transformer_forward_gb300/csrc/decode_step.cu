@@ -286,6 +286,8 @@ __device__ void producer(const Params& p, uint8_t* wring, uint64_t* wfull, uint6
         const int n = min(gm.R, gm.o1 - gm.o0 - t * gm.R);   // outputs of this unit
         const int reqs = which == G_GU ? 2 * n : n;
         const uint32_t dst = smem_u32(wring + size_t(slot) * SLOT);
+        // the consumers' generic reads of this slot before the async-proxy copies refill it
+        tcx::fence_proxy_async();
         if (lane == 0) tcx::mbar_expect_tx(smem_u32(wfull + slot), uint32_t(reqs) * gm.kseg * 2u);
         __syncwarp();
         for (int r = lane; r < reqs; r += 32) {
@@ -655,6 +657,9 @@ __device__ void att_produce(const Params& p, int l, uint8_t* aring, AttShared& a
         }
       }
       if (lane == 0) {
+        // generic reads of this stage (the consumers' ldmatrix, or the norm and
+        // GEMV stages that share the region) before the async-proxy copies
+        tcx::fence_proxy_async();
         const uint32_t dst = smem_u32(aring + size_t(stg) * ATT_STAGE);
         const uint32_t fb = smem_u32(&as.full[stg]);
         const int z = as.base[it.b] + it.start + st.cur_t * ATT_KT;

@@ -515,12 +515,26 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
 
 // RPC: weight rows per CTA (16, or 8 for small N to spread over more SMs);
 // MAXC: 32-wide k chunks per warp held in registers at once.
-template <int NT, int EPI, bool WROW, int RPC, int MAXC>
+// NORM: A is a sublayer output h; the GEMM input is y = RMSNorm(h + res_in)
+// * gamma (h alone when res_in is null), computed by every CTA for all M
+// tokens into shared memory; CTA 0 writes res_out = h + res_in (the new
+// residual, a buffer distinct from h and res_in).
+struct NormArgs {
+  const bf16* res_in;
+  bf16* res_out;
+  const bf16* gamma;
+  float eps;
+};
+constexpr int GV_YPAD = 8;   // y row padding (elements): 16-byte rows at distinct bank groups
+
+template <int NT, int EPI, bool WROW, int RPC, int MAXC, bool NORM = false>
 __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
     gemv_mma_kernel(const bf16* __restrict__ A, const bf16* __restrict__ W, bf16* __restrict__ C, int M, int N, int K,
-                    int K_l, int64_t ldc, int64_t i_l) {
+                    int K_l, int64_t ldc, int64_t i_l, NormArgs na) {
   constexpr int GV_MAXC = MAXC;
   __shared__ float red[GV_WARPS][16][NT * 8];
+  extern __shared__ __align__(16) uint8_t gv_dyn[];
+  bf16* ys = reinterpret_cast<bf16*>(gv_dyn);   // NORM: [M][K + GV_YPAD]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   // the two weight rows of this thread (m16 tile rows g and g + 8)
   int64_t rowA, rowB;
@@ -550,9 +564,8 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
   float acc[NT][4];
 #pragma unroll
   for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
-  bool waited = false;
-  for (int kb = k0; kb < k1; kb += GV_MAXC * 32) {
-    uint4 wa[GV_MAXC], wb[GV_MAXC];
+  uint4 wa[GV_MAXC], wb[GV_MAXC];
+  auto load_w = [&](int kb) {
 #pragma unroll
     for (int c = 0; c < GV_MAXC; ++c) {
       const int k = kb + 32 * c + 8 * t;
@@ -560,11 +573,61 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
       wa[c] = (in && okA) ? ldg_stream(wptr(rowA, k)) : make_uint4(0, 0, 0, 0);
       wb[c] = (RPC == 16 && in && okB) ? ldg_stream(wptr(rowB, k)) : make_uint4(0, 0, 0, 0);
     }
-    if (!waited) {
-      pdl_trigger();   // the next kernel may start its prologue
-      pdl_wait();      // the activations are complete and visible
-      waited = true;
+  };
+  // the first weights are constants: load them before the dependency wait
+  if (k0 < k1) load_w(k0);
+  pdl_trigger();   // the next kernel may start its prologue
+  pdl_wait();      // the activations are complete and visible
+  const int ys_stride = K + GV_YPAD;
+  if (NORM) {
+    // y = RMSNorm(h + res_in) * gamma for every token, into shared memory
+    for (int tk = warp; tk < M; tk += GV_WARPS) {
+      const bf16* hr = A + int64_t(tk) * K;
+      const bf16* rr = na.res_in != nullptr ? na.res_in + int64_t(tk) * K : nullptr;
+      float ss = 0.0f;
+      for (int k0v = lane * 8; k0v < K; k0v += 4 * 256) {
+        uint4 hv[4], rv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {   // a pass's loads all in flight before use
+          const int k = k0v + i * 256;
+          if (k < K) {
+            hv[i] = __ldcg(reinterpret_cast<const uint4*>(hr + k));
+            if (rr != nullptr) rv[i] = __ldcg(reinterpret_cast<const uint4*>(rr + k));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int k = k0v + i * 256;
+          if (k >= K) continue;
+          float v[8];
+          const bf16* hb = reinterpret_cast<const bf16*>(&hv[i]);
+          const bf16* rb = reinterpret_cast<const bf16*>(&rv[i]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            v[e] = rr != nullptr ? round_t<bf16>(__bfloat162float(hb[e]) + __bfloat162float(rb[e]))
+                                 : __bfloat162float(hb[e]);   // x + residual, in the model dtype
+          if (na.res_out != nullptr && blockIdx.x == 0) store16(na.res_out + int64_t(tk) * K + k, v);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ss += v[e] * v[e];
+          store16(ys + tk * ys_stride + k, v);   // the sum, normalised below
+        }
+      }
+      ss = warp_sum(ss);
+      const float inv = rsqrtf(ss / float(K) + na.eps);
+      __syncwarp();
+      for (int k = lane * 8; k < K; k += 256) {
+        float v[8], gm[8];
+        load16(ys + tk * ys_stride + k, v);
+        load16(na.gamma + k, gm);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = (v[e] * inv) * gm[e];
+        store16(ys + tk * ys_stride + k, v);
+      }
     }
+    __syncthreads();
+  }
+  for (int kb = k0; kb < k1; kb += GV_MAXC * 32) {
+    if (kb != k0) load_w(kb);
 #pragma unroll
     for (int c = 0; c < GV_MAXC; ++c) {
       if (kb + 32 * c >= k1) break;
@@ -572,15 +635,14 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         const int tok = n * 8 + g;
-        const uint4 x = tok < M ? __ldg(reinterpret_cast<const uint4*>(A + int64_t(tok) * K + k)) : make_uint4(0, 0, 0, 0);
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (tok < M)
+          x = NORM ? *reinterpret_cast<const uint4*>(ys + tok * ys_stride + k)
+                   : __ldg(reinterpret_cast<const uint4*>(A + int64_t(tok) * K + k));
         mma_16816(acc[n], wa[c].x, wb[c].x, wa[c].y, wb[c].y, x.x, x.y);
         mma_16816(acc[n], wa[c].z, wb[c].z, wa[c].w, wb[c].w, x.z, x.w);
       }
     }
-  }
-  if (!waited) {
-    pdl_trigger();
-    pdl_wait();
   }
   // partial tiles to shared memory: rows g, g+8; tokens 2t, 2t+1 of each n-tile
 #pragma unroll
@@ -864,7 +926,7 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
     cudaError_t e;
 #define QW_GV_ONE(NTV, EPIV, WR, RPCV, MC)                                                                     \
   e = launch_pdl(gemv_mma_kernel<NTV, EPIV, WR, RPCV, MC>, dim3(blocks), dim3(GV_WARPS * 32), 0, st, A, W, C,   \
-                 int(M), int(N), int(K), int(Kl), a.ldc, a.i_l);
+                 int(M), int(N), int(K), int(Kl), a.ldc, a.i_l, NormArgs{nullptr, nullptr, nullptr, 0.0f});
 #define QW_GV(NTV)                                                                                             \
   if (epi == QW_EPI_SILU_MUL) {                                                                                \
     if (small_k) { QW_GV_ONE(NTV, tc::EPI_SILU, false, 16, 4) } else { QW_GV_ONE(NTV, tc::EPI_SILU, false, 16, 12) } \
@@ -906,6 +968,46 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
   if (p.bn == 32) { QW_SWAP_LAUNCH(32) }
   QW_SWAP_LAUNCH(64)
 #undef QW_SWAP_LAUNCH
+}
+
+// y = RMSNorm(x + res_in) * gamma (in every CTA's shared memory), C = y W^T,
+// for at most 16 tokens: the weight-streaming GEMV with a norm prologue.
+int norm_gemm_bf16(const bf16* x, const NormArgs& na, const bf16* W, bf16* C, int M, int N, int K, int tp, int epi,
+                   cudaStream_t st) {
+  const int nt = M <= 8 ? 1 : 2;
+  const bool small_k = K <= GV_WARPS * 32 * 4;
+  const bool half = epi != QW_EPI_SILU_MUL && N <= 2048;
+  const unsigned blocks = unsigned(epi == QW_EPI_SILU_MUL ? (N / 2 + 7) / 8 : half ? (N + 7) / 8 : (N + 15) / 16);
+  const int64_t ldc = epi == QW_EPI_SILU_MUL ? N / 2 : N;
+  const int64_t i_l = epi == QW_EPI_SILU_MUL ? N / 2 / tp : 0;
+  const size_t smem = size_t(M) * (K + GV_YPAD) * 2;
+  cudaError_t e = cudaSuccess;
+#define QW_NG_ONE(NTV, EPIV, RPCV, MC)                                                                            \
+  {                                                                                                              \
+    auto kern = gemv_mma_kernel<NTV, EPIV, false, RPCV, MC, true>;                                               \
+    static size_t allowed = 48 * 1024;                                                                           \
+    if (smem > allowed) {                                                                                        \
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));                    \
+      if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));    \
+      allowed = smem;                                                                                            \
+    }                                                                                                            \
+    e = launch_pdl(kern, dim3(blocks), dim3(GV_WARPS * 32), smem, st, x, W, C, M, N, K, K, ldc, i_l, na);        \
+  }
+#define QW_NG(NTV)                                                                                               \
+  if (epi == QW_EPI_SILU_MUL) {                                                                                  \
+    if (small_k) QW_NG_ONE(NTV, tc::EPI_SILU, 16, 4) else QW_NG_ONE(NTV, tc::EPI_SILU, 16, 12)                    \
+  } else if (half) {                                                                                             \
+    QW_NG_ONE(NTV, tc::EPI_NONE, 8, 12)                                                                          \
+  } else if (small_k) {                                                                                          \
+    QW_NG_ONE(NTV, tc::EPI_NONE, 16, 4)                                                                          \
+  } else {                                                                                                       \
+    QW_NG_ONE(NTV, tc::EPI_NONE, 16, 12)                                                                         \
+  }
+  if (nt == 1) { QW_NG(1) } else { QW_NG(2) }
+#undef QW_NG
+#undef QW_NG_ONE
+  if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "gemv_mma_kernel launch: %s", cudaGetErrorString(e));
+  return check_launch("gemv_mma_kernel (norm prologue)");
 }
 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -1019,4 +1121,28 @@ extern "C" int qw_lm_head(const void* hidden, int64_t T, const int32_t* last_idx
   if (rc) return rc;
   if (next_tokens) return qw_argmax(logits, n_out, V, next_tokens, dtype, stream);
   return QW_OK;
+}
+
+extern "C" int qw_add_rmsnorm_gemm(const void* x, const void* residual_in, void* residual_out, const void* gamma,
+                                   float eps, const void* W, void* C, int64_t M, int64_t N, int64_t K, int tp,
+                                   int epilogue, int dtype, void* stream) {
+  if (dtype != QW_BF16) return set_error(QW_ERR_DTYPE, "qw_add_rmsnorm_gemm: bf16 only");
+  if (M < 0 || M > 16 || N <= 0 || K <= 0 || tp <= 0)
+    return set_error(QW_ERR_SHAPE, "qw_add_rmsnorm_gemm: needs 0 <= M <= 16 tokens");
+  if (epilogue != QW_EPI_NONE && epilogue != QW_EPI_SILU_MUL)
+    return set_error(QW_ERR_INVALID_ARG, "qw_add_rmsnorm_gemm: epilogue %d", epilogue);
+  if (K % 32 || N % 16 || N % tp || (epilogue == QW_EPI_SILU_MUL && ((N % (2 * tp)) || (N / 2 / tp) % 8)))
+    return set_error(QW_ERR_SHAPE, "qw_add_rmsnorm_gemm: K %% 32, N %% 16 and the gate_up split rules");
+  if (K > 16384) return set_error(QW_ERR_SHAPE, "qw_add_rmsnorm_gemm: K too large");
+  if (M == 0) return QW_OK;
+  if (!x || !gamma || !W || !C) return set_error(QW_ERR_INVALID_ARG, "qw_add_rmsnorm_gemm: null pointer");
+  if (!al16(x) || !al16(W) || !al16(C) || !al16(gamma) || (residual_in && !al16(residual_in)) ||
+      (residual_out && !al16(residual_out)))
+    return set_error(QW_ERR_INVALID_ARG, "qw_add_rmsnorm_gemm: pointers must be 16-byte aligned");
+  if (residual_out != nullptr && (residual_out == x || residual_out == residual_in))
+    return set_error(QW_ERR_INVALID_ARG, "qw_add_rmsnorm_gemm: residual_out must not alias x or residual_in");
+  const NormArgs na{static_cast<const bf16*>(residual_in), static_cast<bf16*>(residual_out),
+                    static_cast<const bf16*>(gamma), eps};
+  return norm_gemm_bf16(static_cast<const bf16*>(x), na, static_cast<const bf16*>(W), static_cast<bf16*>(C), int(M),
+                        int(N), int(K), tp, epilogue, static_cast<cudaStream_t>(stream));
 }

@@ -155,6 +155,7 @@ class Qwen3Forward:
         z = lambda *s: torch.empty(*s, dtype=dt, device=device)  # noqa: E731
         self.h = z(T, H)
         self.res = z(T, H)
+        self.res2 = z(max(max_seqs, 1), H)   # decode: the residual alternates between res and res2
         self.y = z(T, H)
         self.qkv = z(T, self.qkv_width)
         self.q = z(T, shape.n_heads * hd)
@@ -200,17 +201,32 @@ class Qwen3Forward:
                 (M, 2 * m.intermediate, m.hidden, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL),
                 (M, m.hidden, m.intermediate, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE)]
 
+    def norm_fusion_ok(self, T: int) -> bool:
+        """Few bf16 tokens: each add+RMSNorm runs as the prologue of the GEMM it feeds."""
+        return self.dtype == torch.bfloat16 and T <= 16 and T <= self.res2.shape[0]
+
+    def _res(self, c: int, T: int):
+        """Residual after update c of a decode step (two per layer) when norms are fused."""
+        return (self.res if c % 2 == 0 else self.res2)[:T]
+
     # -- one decoder layer ([SK] §1) ------------------------------------------
     def _layer(self, l: int, T: int, ctx, first: bool, decode: bool, stream=None):
         m, p = self.m, self.p.layers[l]
         tp = m.tp
         h, res, y = self.h[:T], self.res[:T], self.y[:T]
         ph = "decode" if decode else "prefill"
-        with self._around(f"{ph}.add_rmsnorm", l):
-            L.add_rmsnorm(h, None if first else res, res, p.input_ln, m.eps, y, stream)
+        fused = decode and self.norm_fusion_ok(T)
         qkv = self.qkv[:T]
-        with self._around(f"{ph}.gemm_qkv", l):
-            L.gemm(y, p.qkv, qkv, self.qkv_width, tp, L.QW_GEMM_COLUMN, L.QW_EPI_NONE, self.workspace, stream)
+        if fused:
+            # residual update 2l here, 2l+1 before gate_up; the buffers alternate
+            with self._around(f"{ph}.add_rmsnorm_gemm_qkv", l):
+                L.add_rmsnorm_gemm(h, None if first else self._res(2 * l - 1, T), self._res(2 * l, T), p.input_ln,
+                                   m.eps, p.qkv, qkv, self.qkv_width, tp, L.QW_EPI_NONE, stream)
+        else:
+            with self._around(f"{ph}.add_rmsnorm", l):
+                L.add_rmsnorm(h, None if first else res, res, p.input_ln, m.eps, y, stream)
+            with self._around(f"{ph}.gemm_qkv", l):
+                L.gemm(y, p.qkv, qkv, self.qkv_width, tp, L.QW_GEMM_COLUMN, L.QW_EPI_NONE, self.workspace, stream)
         q = self.q[:T]
         with self._around(f"{ph}.qkv_norm_rope_store_kv", l):
             L.qkv_norm_rope_store_kv(qkv, m.n_heads, m.n_kv_heads, m.head_dim, tp, ctx.positions, self.cos_sin,
@@ -228,9 +244,14 @@ class Qwen3Forward:
                                     attn, stream)
         with self._around(f"{ph}.gemm_o", l):
             L.gemm(attn, p.o, h, m.hidden, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, self.workspace, stream)
-        with self._around(f"{ph}.add_rmsnorm", l):
-            L.add_rmsnorm(h, res, res, p.post_ln, m.eps, y, stream)
         act = self.act[:T]
+        # (gate_up keeps its own norm kernel: fused, its 3 * I / 8 CTAs need a
+        # second wave that repeats the norm prologue, which costs more than it saves)
+        with self._around(f"{ph}.add_rmsnorm", l):
+            if fused:
+                L.add_rmsnorm(h, self._res(2 * l, T), self._res(2 * l + 1, T), p.post_ln, m.eps, y, stream)
+            else:
+                L.add_rmsnorm(h, res, res, p.post_ln, m.eps, y, stream)
         with self._around(f"{ph}.gemm_gate_up_silu", l):
             L.gemm(y, p.gate_up, act, 2 * m.intermediate, tp, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL,
                    self.workspace, stream)
@@ -286,12 +307,12 @@ class Qwen3Forward:
             self.h[:T].copy_(hidden_in)
         for l in range(len(self.p.layers)):
             self._layer(l, T, ctx, l == 0, decode, stream)
+        nl = len(self.p.layers)
+        res = self._res(2 * nl - 1, T) if decode and self.norm_fusion_ok(T) and nl > 0 else self.res[:T]
         if not final_norm:
-            return self.h[:T], self.res[:T]
-        if len(self.p.layers) == 0:
-            L.add_rmsnorm(self.h[:T], None, None, self.p.final_norm, m.eps, self.y[:T], stream)
-        else:
-            L.add_rmsnorm(self.h[:T], self.res[:T], None, self.p.final_norm, m.eps, self.y[:T], stream)
+            return self.h[:T], res
+        with self._around("final_norm", -1):
+            L.add_rmsnorm(self.h[:T], None if nl == 0 else res, None, self.p.final_norm, m.eps, self.y[:T], stream)
         return self.y[:T]
 
     def compute_logits(self, hidden: torch.Tensor, last_idx: Optional[torch.Tensor], n_out: int, stream=None):

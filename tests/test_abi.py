@@ -87,6 +87,11 @@ def test_argument_errors_are_reported_before_launch(lib):
     assert lib.qw_decode_layers(*args(8, 64, 16, 8)) == L.QW_ERR_SHAPE
     assert lib.qw_decode_layers(*args(8, 128, 12, 4)) == L.QW_ERR_SHAPE
     assert lib.qw_decode_layers_workspace_size(28, 17, 1024, 16, 8, 128, 3072, 2, 2048) == 0
+    # fused add + RMSNorm + GEMM: at most 16 tokens, residual_out distinct from x
+    assert lib.qw_add_rmsnorm_gemm(fake, None, None, fake, 1e-6, fake, fake, 17, 64, 64, 1, 0, L.QW_BF16,
+                                   None) == L.QW_ERR_SHAPE
+    assert lib.qw_add_rmsnorm_gemm(fake, fake, fake, fake, 1e-6, fake, fake, 4, 64, 64, 1, 0, L.QW_BF16,
+                                   None) == L.QW_ERR_INVALID_ARG
     # lm_head: V not divisible by tp
     assert lib.qw_lm_head(fake, 4, None, 4, fake, 10, 64, 4, fake, None, None, 0, L.QW_BF16,
                           None) == L.QW_ERR_SHAPE

@@ -251,6 +251,39 @@ def test_gemm_bf16(L, M, N, K, tp, mode, epi):
                        atol=_gemm_abs_bound(A, W, mode, epi, tp))
 
 
+@pytest.mark.parametrize("M,N,K,tp,epi,with_res", [(8, 4096, 1024, 2, 0, True), (8, 6144, 1024, 2, 1, True),
+                                                    (1, 4096, 1024, 1, 0, False), (16, 6144, 1024, 2, 1, True),
+                                                    (13, 1024, 2048, 2, 0, True), (5, 512, 96, 2, 1, False)])
+def test_add_rmsnorm_gemm(L, M, N, K, tp, epi, with_res):
+    """Fused add + RMSNorm + column Linear (decode QKV / gate_up) against the
+    oracle's add_rms_norm followed by the oracle Linear."""
+    x = si.normal(0, f"ng.x{M}.{K}", (M, K), 1.0, "bf16")
+    r = si.normal(0, f"ng.r{M}.{K}", (M, K), 2.0, "bf16")
+    g = (si.normal(0, f"ng.g{K}", (K,), 0.2, "f32") + 1.0).to(torch.bfloat16)
+    W = si.normal(0, f"ng.W{N}.{K}", (N, K), 0.02, "bf16")
+    C = torch.full((M, N // 2 if epi == 1 else N), 123.0, dtype=torch.bfloat16, device="cuda")
+    res_out = torch.full((M, K), 7.0, dtype=torch.bfloat16, device="cuda")
+    L.add_rmsnorm_gemm(dev(x), dev(r) if with_res else None, res_out, dev(g), 1e-6, dev(W), C, N, tp, epi)
+    sync_ok(L)
+    if with_res:
+        ry, rres = O.add_rms_norm(x.double().numpy(), r.double().numpy(), g.double().numpy(), 1e-6, "bf16")
+    else:
+        ry = O.rms_norm(x.double().numpy(), g.double().numpy(), 1e-6, "bf16")
+        rres = x.double().numpy()
+    assert np.array_equal(to_np(res_out), rres)   # residual add: one rounding of an exact sum
+    y = torch.from_numpy(ry).to(torch.bfloat16)
+    ref = _gemm_ref(y, W, 0, epi, tp, "bf16")
+    # y itself may sit one bf16 step from the oracle's (rsqrt and summation
+    # order): that step times sum_k |w_k| on top of the GEMM's own bound
+    y_step = 2.0 ** -8 * (np.abs(ry) @ np.abs(W.double().numpy()).T)
+    if epi == 1:
+        i_l = N // 2 // tp
+        y_step = np.concatenate([y_step[:, r_ * 2 * i_l:r_ * 2 * i_l + i_l] + y_step[:, r_ * 2 * i_l + i_l:(r_ + 1) * 2 * i_l]
+                                 for r_ in range(tp)], -1) * 2.0
+    assert_within_ulps(to_np(C), ref, 2.0, 0.9, f"add_rmsnorm_gemm {M}x{N}x{K} epi{epi}",
+                       atol=_gemm_abs_bound(y, W, 0, epi, tp) + y_step)
+
+
 @pytest.mark.parametrize("M,N,K,tp,mode,epi", [(32, 128, 64, 2, 0, 0), (32, 64, 64, 2, 1, 0),
                                                (32, 256, 64, 2, 0, 1), (5, 512, 64, 1, 0, 0)])
 def test_gemm_f32(L, M, N, K, tp, mode, epi):
