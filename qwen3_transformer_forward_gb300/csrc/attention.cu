@@ -54,8 +54,8 @@ __global__ void __launch_bounds__(128) attn_small_kernel(
     const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, const int32_t* __restrict__ seq_base,
     const int32_t* __restrict__ ctx_lens, int n_seqs, int max_q, int nh, int nkv, int hd, float scale,
     T* __restrict__ out) {
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // inputs of this kernel are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   const int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= int64_t(n_seqs) * max_q * nh) return;
@@ -227,8 +227,8 @@ __global__ void __launch_bounds__(DC_THREADS) attn_decode_kernel(
     const T* __restrict__ q, const T* __restrict__ kc, const T* __restrict__ vc, const int32_t* __restrict__ ctx_lens,
     const int32_t* __restrict__ seq_base, int nh, int nkv, float scale_log2, int chunk, int n_splits,
     float* __restrict__ ws_o, float* __restrict__ ws_ml, unsigned int* __restrict__ counters, T* __restrict__ out) {
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // inputs of this kernel are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   constexpr int EPC = 16 / sizeof(T);      // elements per 16-byte chunk
   constexpr int CPR = DC_HD / EPC;         // chunks per row
   extern __shared__ __align__(128) uint8_t smem[];
@@ -414,8 +414,8 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
     const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ seq_base, int nh, int nkv, float scale_log2,
     int chunk, int n_splits, float* __restrict__ ws_o, float* __restrict__ ws_ml, unsigned int* __restrict__ counters,
     bf16* __restrict__ out) {
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // inputs of this kernel are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + DT_STAGES * DT_STAGE);

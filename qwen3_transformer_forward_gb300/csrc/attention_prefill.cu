@@ -90,8 +90,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_prefill_tc_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const bf16* __restrict__ q,
     const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, const int32_t* __restrict__ seq_base,
     int nh, int nkv, int pair_heads, float scale_log2, bf16* __restrict__ out) {
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // inputs of this kernel are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);

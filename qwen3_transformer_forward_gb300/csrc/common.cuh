@@ -92,10 +92,12 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
 }  // namespace qw
 
 // ---------------------------------------------------------------------------
-// programmatic dependent launch: a kernel lets the next kernel on the stream
-// start early (pdl_trigger) and waits for the previous one to finish and
-// publish its memory (pdl_wait) before touching anything it produced.  Both
-// are no-ops when the kernel was launched without the attribute.
+// programmatic dependent launch: a kernel waits for the previous one to finish
+// and publish its memory (pdl_wait) before touching anything it produced, and
+// then lets the next kernel on the stream start early (pdl_trigger).  Waiting
+// first keeps at most one kernel parked ahead: measured on the 28-layer
+// decode step, triggering before the wait let chains of waiting CTAs occupy
+// the SMs and cost about 5%.  Both are no-ops without the launch attribute.
 // ---------------------------------------------------------------------------
 namespace qw {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -19,8 +19,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) embed_vocab_kernel(const int64_t* __restrict__ ids, int64_t n_tok,
                                                           const T* __restrict__ table, int64_t V, int64_t H,
                                                           int tp, T* __restrict__ out, int32_t* err) {
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // inputs of this kernel are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   constexpr int N = V16<T>::N;
   const int64_t tok = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -68,8 +68,8 @@ template <typename T, int NV>
 __global__ void __launch_bounds__(256) add_rmsnorm_kernel(const T* __restrict__ x, const T* res_in, T* res_out,
                                                           const T* __restrict__ gamma, float eps, int64_t rows,
                                                           int H, T* __restrict__ y) {
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // inputs of this kernel are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   constexpr int N = V16<T>::N;
   const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -122,8 +122,8 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_kernel(
     const T* __restrict__ q_gamma, const T* __restrict__ k_gamma, float eps,
     const int64_t* __restrict__ slots, T* __restrict__ k_cache, T* __restrict__ v_cache, int64_t num_slots,
     T* __restrict__ q_out, int32_t* err) {
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // inputs of this kernel are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   const int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int heads = nh + nkv;
@@ -225,8 +225,8 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_hd128_kernel(
     const float* __restrict__ cos_sin, int64_t max_pos, const bf16* __restrict__ q_gamma,
     const bf16* __restrict__ k_gamma, float eps, const int64_t* __restrict__ slots, bf16* __restrict__ k_cache,
     bf16* __restrict__ v_cache, int64_t num_slots, bf16* __restrict__ q_out, int32_t* err) {
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // inputs of this kernel are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   constexpr int HD = 128, HALF = 64;
   const int heads = nh + nkv;
   const int64_t task = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 3;   // one (token, head) per 8 lanes
@@ -307,8 +307,8 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_hd128_kernel(
 template <typename T>
 __global__ void __launch_bounds__(256) silu_mul_kernel(const T* __restrict__ x, T* __restrict__ out,
                                                        int64_t n_tok, int64_t I, int64_t I_l) {
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // inputs of this kernel are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   constexpr int N = V16<T>::N;
   const int64_t vpr = I / N;
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -331,8 +331,8 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const T* __restrict__ x, 
 template <typename T>
 __global__ void __launch_bounds__(1024) argmax_kernel(const T* __restrict__ logits, int64_t V,
                                                       int64_t* __restrict__ out) {
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // inputs of this kernel are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   constexpr int N = V16<T>::N;
   const T* p = logits + int64_t(blockIdx.x) * V;
   float best = -INFINITY;
@@ -381,8 +381,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const T* __restrict__ src, int64_t n_src,
                                                           const int32_t* __restrict__ idx, int64_t n,
                                                           int64_t H, T* __restrict__ out) {
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // inputs of this kernel are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   constexpr int N = V16<T>::N;
   const int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;

@@ -576,8 +576,8 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
   };
   // the first weights are constants: load them before the dependency wait
   if (k0 < k1) load_w(k0);
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // the activations are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   const int ys_stride = K + GV_YPAD;
   if (NORM) {
     // y = RMSNorm(h + res_in) * gamma for every token, into shared memory
@@ -690,8 +690,8 @@ __device__ __forceinline__ float w_at(const float* W, int64_t n, int64_t k, int6
 __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__ A, const float* __restrict__ W,
                                                        float* __restrict__ C, int64_t M, int64_t Nout, int64_t N,
                                                        int64_t K, int64_t K_l, int row, int silu, int64_t i_l) {
-  pdl_trigger();   // the next kernel may start its prologue
   pdl_wait();      // inputs of this kernel are complete and visible
+  pdl_trigger();   // only now may the next kernel start its prologue
   __shared__ float sa[16][17];
   __shared__ float sw[2][16][17];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
