@@ -54,10 +54,14 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-layers", type=int, default=4)
-    ap.add_argument("--cpu-sample-tokens", type=int, default=256)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
     ap.add_argument("--profile-window", action="store_true",
                     help="after the timed region, run one more step between cudaProfilerStart/Stop "
                          "(for ncu --profile-from-start off)")
+    ap.add_argument("--profile-kernel", choices=["decode.attention"], default=None,
+                    help="launch only this kernel, --profile-reps times, on inputs of the workload's shape "
+                         "(random values, mean decode context) and exit: a small case for ncu section captures")
+    ap.add_argument("--profile-reps", type=int, default=3)
     return ap.parse_args(argv)
 
 
@@ -576,8 +580,36 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def profile_kernel(args):
+    """One kernel of the workload on inputs of its shape, for a small ncu capture."""
+    import seeded_inputs as si
+    from qwen3_transformer_forward_gb300 import build as B
+    from qwen3_transformer_forward_gb300 import _lib as L
+    B.build()
+    w = si.workload(WORKLOAD)
+    m = w.model
+    seqs, S = list(w.seq_lens), w.decode_steps
+    nb, nh, nkv, hd = len(seqs), m.n_heads, m.n_kv_heads, m.head_dim
+    cap = max(seqs) + S
+    g = torch.Generator(device="cuda").manual_seed(0)
+    rnd = lambda *shape: torch.randn(*shape, device="cuda", generator=g).to(torch.bfloat16)  # noqa: E731
+    if args.profile_kernel == "decode.attention":
+        kc, vc, q = rnd(nb * cap, nkv, hd), rnd(nb * cap, nkv, hd), rnd(nb, nh, hd)
+        ctx = torch.tensor([L0 + S // 2 for L0 in seqs], dtype=torch.int32, device="cuda")
+        base = torch.arange(nb, dtype=torch.int32, device="cuda") * cap
+        out = torch.empty(nb, nh * hd, dtype=torch.bfloat16, device="cuda")
+        ws = torch.zeros(L.attention_decode_workspace_size(nb, cap, nh, hd), dtype=torch.uint8, device="cuda")
+        for _ in range(args.profile_reps):
+            L.attention_decode(q, kc, vc, ctx, base, cap, nh, nkv, hd, hd ** -0.5, out, ws)
+    torch.cuda.synchronize()
+    L.device_error()
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.profile_kernel is not None:
+        profile_kernel(args)
+        return
     rank, world, local = dist_setup()
     if args.impl == "reference":
         out = run_reference(args, rank, world)
