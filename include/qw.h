@@ -80,7 +80,7 @@ typedef enum {
   QW_EPI_SILU_MUL = 1     /* fused SiluAndMul on a merged gate_up output ([SK] §4) */
 } qw_epilogue;
 
-/* Version of this ABI (increments on any signature change); this is version 2. */
+/* Version of this ABI (increments on any signature change); this is version 4. */
 int qw_abi_version(void);
 
 /* Description of the last failure on the calling thread ("" if none). */
@@ -179,14 +179,26 @@ int qw_attention_prefill(const void* q, const void* k, const void* v, int64_t kv
  *   every cache row read, seq_base[b] .. seq_base[b] + context_lens[b] - 1, < num_slots
  *   out dtype [B, nh, hd]
  *   workspace: device scratch of qw_attention_decode_workspace_size(...) bytes
- *   (split-KV partial results); may be NULL only when that size is 0.
+ *   (split-KV partial results); may be NULL only when that size is 0.  The
+ *   first 64 KiB are completion counters: zero before the first call, and
+ *   every call leaves them zero.
+ *   flags: 0, or QW_DECODE_HISTORY_READY (bf16, hd 128).  With that flag the
+ *   caller states that context_lens, seq_base and every cache row the call
+ *   reads except each sequence's last (position context_lens[b] - 1) were
+ *   complete before the kernel enqueued just before this call started, and
+ *   that this kernel writes at most q and those last rows (a decode step's
+ *   QK-norm + RoPE + KV store).  The kernel then reads the lengths and starts
+ *   copying the earlier rows before it waits for that kernel (programmatic
+ *   dependent launch).  Without it nothing is read before the wait.
  * Rules: nh % nkv == 0; hd == 128 with nh/nkv in {1, 2, 4, 8} (split-KV path),
- * or hd <= 64 (one warp per (sequence, q head), no workspace); bf16 or f32.
+ * or hd <= 64 (one warp per (sequence, q head), no workspace); bf16 or f32;
+ * unknown flags: QW_ERR_INVALID_ARG.
  */
+#define QW_DECODE_HISTORY_READY 1
 int qw_attention_decode(const void* q, const void* k_cache, const void* v_cache, int64_t num_slots,
                         const int32_t* context_lens, const int32_t* seq_base, int B, int max_context,
                         int n_heads, int n_kv_heads, int head_dim, float scale, void* out,
-                        void* workspace, size_t workspace_bytes, int dtype, void* stream);
+                        void* workspace, size_t workspace_bytes, int dtype, int flags, void* stream);
 size_t qw_attention_decode_workspace_size(int B, int max_context, int n_heads, int head_dim);
 
 /*

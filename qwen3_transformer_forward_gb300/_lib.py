@@ -36,7 +36,7 @@ SIGNATURES = {
                                             _p, _i64, _p, _p, _i32, _p]),
     "qw_attention_prefill": (C.c_int, [_p, _p, _p, _i64, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _i32, _p]),
     "qw_attention_decode": (C.c_int, [_p, _p, _p, _i64, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _p, _sz,
-                                      _i32, _p]),
+                                      _i32, _i32, _p]),
     "qw_attention_decode_workspace_size": (C.c_size_t, [_i32, _i32, _i32, _i32]),
     "qw_attention_decode_static": (C.c_int, [_p, _p, _p, _i64, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _i32,
                                              _p]),
@@ -180,15 +180,20 @@ def attention_decode_workspace_size(B, max_context, n_heads, head_dim) -> int:
     return load().qw_attention_decode_workspace_size(B, max_context, n_heads, head_dim)
 
 
+QW_DECODE_HISTORY_READY = 1
+
+
 def attention_decode(q, k_cache, v_cache, context_lens, seq_base, max_context, n_heads, n_kv_heads, head_dim, scale,
-                     out, workspace=None, stream=None):
+                     out, workspace=None, stream=None, history_ready=False):
+    """history_ready: the previous kernel on the stream writes only q and each sequence's last cache row
+    (see QW_DECODE_HISTORY_READY in qw.h)."""
     B = q.shape[0]
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().qw_attention_decode(
         _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), k_cache.shape[0],
         _dev_ptr(context_lens, "context_lens"), _dev_ptr(seq_base, "seq_base"), B, max_context, n_heads, n_kv_heads,
         head_dim, scale, _dev_ptr(out, "out"), _dev_ptr(workspace, "workspace"), ws_bytes, dtype_code(q.dtype),
-        _stream(stream)))
+        QW_DECODE_HISTORY_READY if history_ready else 0, _stream(stream)))
 
 
 def attention_decode_static(q, k_cache, v_cache, context_lens, seq_base, max_context, n_heads, n_kv_heads,

@@ -388,220 +388,329 @@ __global__ void __launch_bounds__(DC_THREADS) attn_decode_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// decode, bf16: tensor-core split-KV.  One CTA of 4 warps per (chunk of keys,
-// kv head, sequence).  K/V tiles of 64 keys arrive by TMA (3-D map over the
-// cache [slot][kv head][dim], two 64-dim boxes with 128-byte swizzle each)
-// through a 3-stage mbarrier ring.  Warp w owns keys 16w..16w+15 of every
-// tile and runs its own online softmax: S = Q K^T and O += P V with
-// mma.sync m16n8k16 (the group's G q heads padded to 16 rows).  The four
-// warps merge at the end; chunks merge through the workspace as above.
+// decode, bf16: tensor-core split-KV in one persistent wave.
+//
+// The work is laid out as a fixed grid of 64-key tiles: pair p = b * nkv + g
+// (sequence b, kv head g) owns tiles [p * T, (p + 1) * T), T = ceil(max
+// context / 64).  CTA c takes the contiguous range [c * per, (c + 1) * per)
+// of that grid (per = ceil(P * T / gridDim)), so the split depends only on
+// sizes the host knows and a CTA can start its copies at once; tiles at or
+// past a sequence's own length are skipped.  K/V tiles arrive by TMA (3-D map
+// over the cache [slot][kv head][dim], two 64-dim boxes with 128-byte swizzle
+// each) through a 3-stage mbarrier ring that runs on across pair boundaries.
+// Warp w owns keys 16w..16w+15 of every tile and runs its own online softmax:
+// S = Q K^T and O += P V with mma.sync m16n8k16 (the group's G q heads padded
+// to 16 rows).  At the end of each pair segment the four warps merge in
+// shared memory.  A pair inside one CTA's range is written out directly;
+// otherwise each of its CTAs c_first..c_last leaves (m, l, o) in workspace
+// slot c + p (distinct for every (CTA, pair) that occurs, since a later CTA
+// starts at or after the pair where an earlier one stopped), and the last to
+// finish, by the pair's completion counter, merges them in CTA order.
 // ---------------------------------------------------------------------------
 __device__ unsigned int g_attn_timeout = 0;
 
 constexpr int DT_KT = 64, DT_STAGES = 3, DT_THREADS = 128;
 constexpr uint32_t DT_BOX = 64 * 64 * 2;          // 64 keys x 64 dims of bf16
 constexpr uint32_t DT_STAGE = 4 * DT_BOX;         // K dims 0-63, K 64-127, V 0-63, V 64-127
-constexpr size_t DT_SMEM = 1024 + size_t(DT_STAGES) * DT_STAGE + 256;
+constexpr int DT_MERGE = 8;                       // segments whose partials one merge step loads at once
+
+// dynamic shared memory (after rounding the base up to 1024 B):
+// ring | sO [4 warps][G][128] f32 | sML [4][G][2] f32 | flag | barriers
+template <int G>
+constexpr size_t dt_smem() {
+  return 1024 + size_t(DT_STAGES) * DT_STAGE + size_t(4) * G * DC_HD * 4 + size_t(4) * G * 2 * 4 + 16 +
+         2 * DT_STAGES * 8;
+}
 
 // byte offset of (key row r, 16-byte chunk c16 over the 128 dims) in a K or V region
 __device__ __forceinline__ uint32_t kv_off(int r, int c16) {
   return uint32_t(c16 >> 3) * DT_BOX + uint32_t(r) * 128u + uint32_t(((c16 & 7) ^ (r & 7)) * 16);
 }
 
+__device__ __forceinline__ unsigned int atom_add_acq_rel_gpu(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 template <int G>
 __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const bf16* __restrict__ q,
-    const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ seq_base, int nh, int nkv, float scale_log2,
-    int chunk, int n_splits, float* __restrict__ ws_o, float* __restrict__ ws_ml, unsigned int* __restrict__ counters,
-    bf16* __restrict__ out) {
-  pdl_wait();      // inputs of this kernel are complete and visible
-  pdl_trigger();   // only now may the next kernel start its prologue
-  extern __shared__ uint8_t smem_dyn[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + DT_STAGES * DT_STAGE);
-  const int b = blockIdx.z, g = blockIdx.y, split = blockIdx.x;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int L = ctx_lens[b];
-  const int start = split * chunk;
-  const int end = min(L, start + chunk);
-  const int h0 = g * G;
-  if (start >= end) {
-    if (n_splits > 1) {
-      if (tid < G) {
-        const int64_t idx = (int64_t(b) * nh + h0 + tid) * n_splits + split;
-        ws_ml[2 * idx] = -INFINITY;
-        ws_ml[2 * idx + 1] = 0.0f;
-      }
-      decode_finish<bf16, G>(ws_o, ws_ml, counters, b, g, nh, nkv, n_splits, out);
-    } else {
-      for (int i = tid; i < G * DC_HD; i += DT_THREADS)
-        out[(int64_t(b) * nh + h0 + i / DC_HD) * DC_HD + i % DC_HD] = __float2bfloat16_rn(0.0f);
+    const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ seq_base, int nh, int nkv, int n_pairs,
+    int T, int per, float scale_log2, int history_ready, float* __restrict__ ws_o, float* __restrict__ ws_ml,
+    unsigned int* __restrict__ counters, bf16* __restrict__ out) {
+  // history_ready: context lengths, bases and every cached row but each
+  // sequence's last were complete before the previous kernel started, which
+  // writes only q and those last rows.  Then the lengths are read and the
+  // copies of tiles before each sequence's last start ahead of the wait.
+  if (!history_ready) {
+    pdl_wait();      // inputs of this kernel are complete and visible
+    pdl_trigger();   // only now may the next kernel start its prologue
+  }
+  const int64_t lo = int64_t(blockIdx.x) * per;
+  const int64_t hi = min(int64_t(n_pairs) * T, lo + per);
+  if (lo >= hi) {   // uniform over the CTA
+    if (history_ready) {
+      pdl_wait();
+      pdl_trigger();
     }
     return;
   }
-  const int n_kt = (end - start + DT_KT - 1) / DT_KT;
-  const int zbase = seq_base[b] + start;
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  float* sO = reinterpret_cast<float*>(sm + DT_STAGES * DT_STAGE);   // [4][G][128]
+  float* sML = sO + 4 * G * DC_HD;                                   // [4][G][2]
+  int* s_last = reinterpret_cast<int*>(sML + 4 * G * 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_last + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int p_first = int(lo / T), p_last = int((hi - 1) / T);
+  const int L_first = ctx_lens[p_first / nkv], base_first = seq_base[p_first / nkv];   // loaded together
+  // this CTA's tiles of pair p: the static range clipped to the sequence's own length (Tb tiles)
+  auto seg_range = [&](int p, int& ta, int& tb, int& Tb) {
+    const int ts = p == p_first ? int(lo - int64_t(p) * T) : 0;
+    const int te = p == p_last ? int(hi - int64_t(p) * T) : T;
+    const int L = p / nkv == p_first / nkv ? L_first : ctx_lens[p / nkv];
+    Tb = L > 0 ? (L + DT_KT - 1) / DT_KT : 0;
+    ta = ts;
+    tb = max(ts, min(te, Tb));
+  };
   auto full = [&](int s) { return smem_u32(bars + s); };
   auto empty = [&](int s) { return smem_u32(bars + DT_STAGES + s); };
+
+  // ---- producer state (thread 0): the next tile to load
+  int pp = p_first, pt = 0, pt_end = 0, pTb = 0;
+  auto prod_next = [&]() -> bool {   // moves to a pair with a tile left; false when none
+    while (pt >= pt_end) {
+      if (pp > p_last) return false;
+      seg_range(pp, pt, pt_end, pTb);
+      if (pt >= pt_end) ++pp;
+    }
+    return true;
+  };
+  int n_tiles = 0;   // tiles this CTA streams
+  for (int p = p_first; p <= p_last; ++p) {
+    int ta, tb, Tb;
+    seg_range(p, ta, tb, Tb);
+    n_tiles += tb - ta;
+  }
+  auto issue = [&](int j) {
+    const int s = j % DT_STAGES;
+    const uint32_t dst = smem_u32(sm + s * DT_STAGE);
+    const int b = pp / nkv, g = pp % nkv;
+    const int z = (b == p_first / nkv ? base_first : seq_base[b]) + pt * DT_KT;
+    tcx::mbar_expect_tx(full(s), DT_STAGE);
+    tcx::tma_load_3d(dst, &tmK, full(s), 0, g, z);
+    tcx::tma_load_3d(dst + DT_BOX, &tmK, full(s), 64, g, z);
+    tcx::tma_load_3d(dst + 2 * DT_BOX, &tmV, full(s), 0, g, z);
+    tcx::tma_load_3d(dst + 3 * DT_BOX, &tmV, full(s), 64, g, z);
+    if (++pt >= pt_end) ++pp;
+  };
+  int issued = 0;
   if (tid == 0) {
     for (int s = 0; s < DT_STAGES; ++s) {
       tcx::mbar_init(full(s), 1);
       tcx::mbar_init(empty(s), DT_THREADS / 32);
     }
     tcx::fence_mbar_init();
-    tcx::prefetch_map(&tmK);
-    tcx::prefetch_map(&tmV);
+    // ahead of the wait: tiles before each sequence's last (which may still be written)
+    if (history_ready)
+      for (; issued < DT_STAGES && issued < n_tiles; ++issued)
+        if (!prod_next() || pt == pTb - 1) break;
+        else issue(issued);
   }
-  __syncthreads();
-  auto issue = [&](int t) {
-    const int s = t % DT_STAGES;
-    const uint32_t dst = smem_u32(sm + s * DT_STAGE);
-    const int z = zbase + t * DT_KT;
-    tcx::mbar_expect_tx(full(s), DT_STAGE);
-    tcx::tma_load_3d(dst, &tmK, full(s), 0, g, z);
-    tcx::tma_load_3d(dst + DT_BOX, &tmK, full(s), 64, g, z);
-    tcx::tma_load_3d(dst + 2 * DT_BOX, &tmV, full(s), 0, g, z);
-    tcx::tma_load_3d(dst + 3 * DT_BOX, &tmV, full(s), 64, g, z);
-  };
+  if (history_ready) {
+    pdl_wait();      // q and the sequences' last rows are complete and visible
+    pdl_trigger();   // only now may the next kernel start its prologue
+  }
   if (tid == 0)
-    for (int t = 0; t < DT_STAGES && t < n_kt; ++t) issue(t);
+    for (int j = issued; j < DT_STAGES && j < n_tiles; ++j)
+      if (prod_next()) issue(j);
+  __syncthreads();
 
   const int gq = lane >> 2, tq = lane & 3;   // mma fragment row / column pair
   const int mi = lane >> 3, ri = lane & 7;   // ldmatrix matrix / row
-  // q of this thread's row (head h0 + gq; rows >= G are zero)
-  uint32_t qa[8][2];
-  {
-    const bf16* qr = q + (int64_t(b) * nh + h0 + (gq < G ? gq : 0)) * DC_HD;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      qa[kk][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tq) : 0u;
-      qa[kk][1] = gq < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 8 + 2 * tq) : 0u;
-    }
-  }
-  float o[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-  float m_run = -INFINITY, l_run = 0.0f;
   const int key0 = warp * 16;
   bool ok = true;
-  for (int t = 0; t < n_kt; ++t) {
-    const int s = t % DT_STAGES;
-    const uint32_t ph = (t / DT_STAGES) & 1;
-    if (ok && !tcx::mbar_wait(full(s), ph, &g_attn_timeout, 1u)) ok = false;
-    const uint32_t st = smem_u32(sm + s * DT_STAGE);
-    const int kbase = start + t * DT_KT + key0;          // key position of this warp's first row
-    if (kbase + 16 > end) {
-      // keys past the chunk: zero their V rows (whatever the cache holds there)
-      for (int i = 0; i < 16; ++i)
-        if (kbase + i >= end && lane < 16)
-          *reinterpret_cast<uint4*>(sm + s * DT_STAGE + 2 * DT_BOX + kv_off(key0 + i, lane)) = make_uint4(0, 0, 0, 0);
-      tcx::fence_proxy_async();
+  int j = 0;   // ring position
+  for (int p = p_first; p <= p_last; ++p) {
+    const int b = p / nkv, g = p % nkv;
+    int ta, tb, Tb;
+    seg_range(p, ta, tb, Tb);
+    const int L = b == p_first / nkv ? L_first : ctx_lens[b];
+    // q of this thread's row (head g * G + gq; rows >= G are zero)
+    uint32_t qa[8][2];
+    {
+      const bf16* qr = q + (int64_t(b) * nh + g * G + (gq < G ? gq : 0)) * DC_HD;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qa[kk][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tq) : 0u;
+        qa[kk][1] = gq < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 8 + 2 * tq) : 0u;
+      }
+    }
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+    float m_run = -INFINITY, l_run = 0.0f;
+    for (int t = ta; t < tb; ++t, ++j) {
+      const int s = j % DT_STAGES;
+      const uint32_t ph = (j / DT_STAGES) & 1;
+      if (ok && !tcx::mbar_wait(full(s), ph, &g_attn_timeout, 1u)) ok = false;
+      const uint32_t st = smem_u32(sm + s * DT_STAGE);
+      const int kbase = t * DT_KT + key0;   // key position of this warp's first row
+      if (kbase + 16 > L) {
+        // keys past the sequence: zero their V rows (whatever the cache holds there)
+        for (int i = 0; i < 16; ++i)
+          if (kbase + i >= L && lane < 16)
+            *reinterpret_cast<uint4*>(sm + s * DT_STAGE + 2 * DT_BOX + kv_off(key0 + i, lane)) =
+                make_uint4(0, 0, 0, 0);
+        tcx::fence_proxy_async();
+        __syncwarp();
+      }
+      float sc[2][4];
+#pragma unroll
+      for (int nn = 0; nn < 2; ++nn) sc[nn][0] = sc[nn][1] = sc[nn][2] = sc[nn][3] = 0.0f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(st + kv_off(key0 + ri + 8 * (mi >> 1), 2 * kk + (mi & 1)), b0, b1, b2, b3);
+        mma_bf16(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+        mma_bf16(sc[1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+      }
+      float x[4];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int kp = kbase + 8 * nn + 2 * tq + e;
+          const float v = kp < L ? sc[nn][e] * scale_log2 : -INFINITY;
+          x[2 * nn + e] = v;
+          mx = fmaxf(mx, v);
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      const float m_use = m_new == -INFINITY ? 0.0f : m_new;
+      const float alpha = exp2f(m_run - m_use);
+      float pr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pr[i] = exp2f(x[i] - m_use);
+      l_run = l_run * alpha + (pr[0] + pr[1] + pr[2] + pr[3]);
+      m_run = m_new;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        o[i][0] *= alpha;
+        o[i][1] *= alpha;
+      }
+      const uint32_t a0 = pack_bf16(pr[0], pr[1]);
+      const uint32_t a2 = pack_bf16(pr[2], pr[3]);
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(st + 2 * DT_BOX + kv_off(key0 + ri + 8 * (mi & 1), 2 * dp + (mi >> 1)), b0, b1, b2, b3);
+        mma_bf16(o[2 * dp], a0, 0u, a2, 0u, b0, b1);
+        mma_bf16(o[2 * dp + 1], a0, 0u, a2, 0u, b2, b3);
+      }
       __syncwarp();
-    }
-    float sc[2][4];
-#pragma unroll
-    for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.0f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(st + kv_off(key0 + ri + 8 * (mi >> 1), 2 * kk + (mi & 1)), b0, b1, b2, b3);
-      mma_bf16(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-      mma_bf16(sc[1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
-    }
-    float x[4];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int kp = kbase + 8 * n + 2 * tq + e;
-        const float v = kp < end ? sc[n][e] * scale_log2 : -INFINITY;
-        x[2 * n + e] = v;
-        mx = fmaxf(mx, v);
-      }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);
-    const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-    const float alpha = exp2f(m_run - m_use);
-    float p[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) p[i] = exp2f(x[i] - m_use);
-    l_run = l_run * alpha + (p[0] + p[1] + p[2] + p[3]);
-    m_run = m_new;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i][0] *= alpha;
-      o[i][1] *= alpha;
-    }
-    const uint32_t a0 = pack_bf16(p[0], p[1]);
-    const uint32_t a2 = pack_bf16(p[2], p[3]);
-#pragma unroll
-    for (int dp = 0; dp < 8; ++dp) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(st + 2 * DT_BOX + kv_off(key0 + ri + 8 * (mi & 1), 2 * dp + (mi >> 1)), b0, b1, b2, b3);
-      mma_bf16(o[2 * dp], a0, 0u, a2, 0u, b0, b1);
-      mma_bf16(o[2 * dp + 1], a0, 0u, a2, 0u, b2, b3);
-    }
-    __syncwarp();
-    if (lane == 0) tcx::mbar_arrive(empty(s));
-    if (tid == 0 && t + DT_STAGES < n_kt) {
-      if (ok && !tcx::mbar_wait(empty(s), ph, &g_attn_timeout, 2u)) ok = false;
-      // The warps read this stage with ldmatrix (generic proxy) and the copy
-      // below overwrites it through the async proxy: the barrier alone does
-      // not order the two proxies.  Without this fence a copy was seen to land
-      // while a warp's last ldmatrix (V dims 112-127) was still pending.
-      tcx::fence_proxy_async();
-      if (ok) issue(t + DT_STAGES);
-    }
-  }
-  // merge the four warps' softmax states
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-  __syncthreads();   // every tile consumed: the ring is free
-  float* sO = reinterpret_cast<float*>(sm);                    // [4 warps][G][128]
-  float* sML = sO + (DT_THREADS / 32) * G * DC_HD;             // [4 warps][G][2]
-  if (gq < G) {
-#pragma unroll
-    for (int dn = 0; dn < 16; ++dn) {
-      sO[(warp * G + gq) * DC_HD + 8 * dn + 2 * tq] = o[dn][0];
-      sO[(warp * G + gq) * DC_HD + 8 * dn + 2 * tq + 1] = o[dn][1];
-    }
-    if (tq == 0) {
-      sML[(warp * G + gq) * 2] = m_run;
-      sML[(warp * G + gq) * 2 + 1] = l_run;
-    }
-  }
-  __syncthreads();
-  const int d = tid;
-  for (int j = 0; j < G; ++j) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < DT_THREADS / 32; ++w) M = fmaxf(M, sML[(w * G + j) * 2]);
-    float Lsum = 0.0f, O = 0.0f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < DT_THREADS / 32; ++w) {
-        const float mw = sML[(w * G + j) * 2];
-        if (mw == -INFINITY) continue;
-        const float sc = exp2f(mw - M);
-        Lsum += sML[(w * G + j) * 2 + 1] * sc;
-        O += sO[(w * G + j) * DC_HD + d] * sc;
+      if (lane == 0) tcx::mbar_arrive(empty(s));
+      if (tid == 0 && j + DT_STAGES < n_tiles) {
+        if (ok && !tcx::mbar_wait(empty(s), ph, &g_attn_timeout, 2u)) ok = false;
+        // The warps read this stage with ldmatrix (generic proxy) and the copy
+        // below overwrites it through the async proxy: the barrier alone does
+        // not order the two proxies.  Without this fence a copy was seen to land
+        // while a warp's last ldmatrix (V dims 112-127) was still pending.
+        tcx::fence_proxy_async();
+        if (ok && prod_next()) issue(j + DT_STAGES);
       }
     }
-    const int64_t hrow = int64_t(b) * nh + h0 + j;
-    if (n_splits > 1) {
-      const int64_t idx = hrow * n_splits + split;
-      ws_o[idx * DC_HD + d] = O;
-      if (d == 0) {
-        ws_ml[2 * idx] = M;
-        ws_ml[2 * idx + 1] = Lsum;
+    // ---- end of this CTA's segment of pair p: merge the four warps' softmax states
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if (gq < G) {
+#pragma unroll
+      for (int dn = 0; dn < 16; ++dn) {
+        sO[(warp * G + gq) * DC_HD + 8 * dn + 2 * tq] = o[dn][0];
+        sO[(warp * G + gq) * DC_HD + 8 * dn + 2 * tq + 1] = o[dn][1];
       }
-    } else {
-      out[hrow * DC_HD + d] = __float2bfloat16_rn(Lsum > 0.0f ? O / Lsum : 0.0f);
+      if (tq == 0) {
+        sML[(warp * G + gq) * 2] = m_run;
+        sML[(warp * G + gq) * 2 + 1] = l_run;
+      }
     }
+    __syncthreads();
+    const int c_first = int(int64_t(p) * T / per), c_last = int((int64_t(p) * T + T - 1) / per);
+    const bool split = c_first != c_last;
+    const int d = tid;
+#pragma unroll
+    for (int jh = 0; jh < G; ++jh) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < DT_THREADS / 32; ++w) M = fmaxf(M, sML[(w * G + jh) * 2]);
+      float Lsum = 0.0f, O = 0.0f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < DT_THREADS / 32; ++w) {
+          const float mw = sML[(w * G + jh) * 2];
+          if (mw == -INFINITY) continue;
+          const float scw = exp2f(mw - M);
+          Lsum += sML[(w * G + jh) * 2 + 1] * scw;
+          O += sO[(w * G + jh) * DC_HD + d] * scw;
+        }
+      }
+      if (!split) {
+        out[(int64_t(b) * nh + g * G + jh) * DC_HD + d] = __float2bfloat16_rn(Lsum > 0.0f ? O / Lsum : 0.0f);
+      } else {
+        const int64_t idx = (int64_t(blockIdx.x) + p) * G + jh;
+        ws_o[idx * DC_HD + d] = O;
+        if (d == 0) {
+          ws_ml[2 * idx] = M;
+          ws_ml[2 * idx + 1] = Lsum;
+        }
+      }
+    }
+    if (split) {
+      // the CTA barrier orders every thread's partial before thread 0's
+      // release; its acquire and the next barrier order the merge's reads
+      __syncthreads();
+      if (tid == 0) *s_last = atom_add_acq_rel_gpu(counters + p, 1u) == unsigned(c_last - c_first) ? 1 : 0;
+      __syncthreads();
+      if (*s_last) {
+#pragma unroll
+        for (int jh = 0; jh < G; ++jh) {
+          float M = -INFINITY, Lsum = 0.0f, O = 0.0f;
+          for (int c0 = c_first; c0 <= c_last; c0 += DT_MERGE) {
+            float mc[DT_MERGE], lc[DT_MERGE], oc[DT_MERGE];
+#pragma unroll
+            for (int u = 0; u < DT_MERGE; ++u) {   // one batch of loads in flight together
+              const int64_t idx = (int64_t(c0 + u) + p) * G + jh;
+              const bool in = c0 + u <= c_last;
+              mc[u] = in ? __ldcg(ws_ml + 2 * idx) : -INFINITY;
+              lc[u] = in ? __ldcg(ws_ml + 2 * idx + 1) : 0.0f;
+              oc[u] = in ? __ldcg(ws_o + idx * DC_HD + d) : 0.0f;
+            }
+            float mb = M;
+#pragma unroll
+            for (int u = 0; u < DT_MERGE; ++u) mb = fmaxf(mb, mc[u]);
+            if (mb == -INFINITY) continue;
+            const float rs = M == -INFINITY ? 0.0f : exp2f(M - mb);
+            Lsum *= rs;
+            O *= rs;
+#pragma unroll
+            for (int u = 0; u < DT_MERGE; ++u) {
+              if (mc[u] == -INFINITY) continue;
+              const float w = exp2f(mc[u] - mb);
+              Lsum += lc[u] * w;
+              O += oc[u] * w;
+            }
+            M = mb;
+          }
+          out[(int64_t(b) * nh + g * G + jh) * DC_HD + d] = __float2bfloat16_rn(Lsum > 0.0f ? O / Lsum : 0.0f);
+        }
+        if (tid == 0) counters[p] = 0u;
+      }
+    }
+    __syncthreads();   // sO, sML and the flag are free for the next segment
   }
-  if (n_splits > 1) decode_finish<bf16, G>(ws_o, ws_ml, counters, b, g, nh, nkv, n_splits, out);
 }
 
 struct DecodePlan {
@@ -664,36 +773,116 @@ extern "C" int qw_attention_prefill(const void* q, const void* k, const void* v,
                                   n_heads, n_kv_heads, head_dim, scale, out, st);
 }
 
+// SM count of the current device; 152 (GB300) when no device can be queried,
+// which only happens on a host checking arguments without launching.
+static int device_sms() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 152;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 152;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// The persistent decode kernel's workspace: completion counters, then one
+// (m, l) and one o per (slot, q head of the group) for the W + B * nkv slots.
+// G * W never exceeds 8 * SMs (at most two CTAs per SM of the ~100 KB ring
+// for G <= 4, one for G = 8), which bounds it without knowing nkv.
+static size_t decode_tc_workspace_bound(int B, int n_heads) {
+  return kCounterBytes + (size_t(8) * device_sms() + size_t(B) * n_heads) * (DC_HD + 2) * sizeof(float);
+}
+
 extern "C" size_t qw_attention_decode_workspace_size(int B, int max_context, int n_heads, int head_dim) {
   if (B <= 0 || max_context <= 0 || n_heads <= 0 || head_dim != 128) return 0;
-  const DecodePlan p = decode_plan(B, max_context, 0);
-  if (p.splits <= 1) return 0;
-  return kCounterBytes + size_t(B) * n_heads * p.splits * (size_t(head_dim) + 2) * sizeof(float);
+  size_t need = decode_tc_workspace_bound(B, n_heads);   // bf16
+  const DecodePlan p = decode_plan(B, max_context, 0);   // f32 split plan
+  if (p.splits > 1) {
+    const size_t f32 = kCounterBytes + size_t(B) * n_heads * p.splits * (size_t(head_dim) + 2) * sizeof(float);
+    need = need > f32 ? need : f32;
+  }
+  return need;
+}
+
+// Resident CTAs per SM of attn_decode_tc_kernel<G> (its shared memory sets it); set up once.
+template <int G>
+static int decode_tc_ctas_per_sm(int* out) {
+  static std::mutex mu;
+  static int v = 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (v == 0) {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(dt_smem<G>()));
+    if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_tc_kernel<G>, DT_THREADS, dt_smem<G>());
+    if (e != cudaSuccess || n <= 0)
+      return set_error(QW_ERR_CUDA, "decode attention occupancy: %s", cudaGetErrorString(e));
+    v = n;
+  }
+  *out = v;
+  return QW_OK;
 }
 
 template <int G>
 static int launch_decode_tc(const void* q, const void* kc, const void* vc, const int32_t* cl, const int32_t* sb,
-                            int B, int nh, int nkv, int64_t num_slots, float sl2, const DecodePlan& p, float* wo,
-                            float* wml, unsigned int* cnt, void* out, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(DT_SMEM));
-    if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    configured = true;
+                            int B, int nh, int nkv, int64_t num_slots, int max_context, float sl2, void* ws,
+                            size_t ws_bytes, int history_ready, void* out, cudaStream_t st) {
+  int per_sm = 0;
+  int rc = decode_tc_ctas_per_sm<G>(&per_sm);
+  if (rc) return rc;
+  // One wave.  With fewer pairs than resident slots, each pair is cut into S
+  // equal key chunks (T padded to S * per), so the CTAs of one sequence's kv
+  // heads stream the same key rows side by side; otherwise the pairs' tiles
+  // are dealt out evenly.  Either way a CTA gets at least two tiles.
+  int T = (max_context + DT_KT - 1) / DT_KT;
+  const int64_t n_pairs = int64_t(B) * nkv;
+  int64_t slots_sm = int64_t(device_sms()) * per_sm;
+  if (slots_sm > 8 * device_sms() / G) slots_sm = 8 * device_sms() / G;   // keeps the workspace bound
+  int64_t per, W;
+  if (n_pairs <= slots_sm) {
+    int64_t S = slots_sm / n_pairs;
+    if (S > (T + 1) / 2) S = (T + 1) / 2;
+    if (S < 1) S = 1;
+    per = (T + S - 1) / S;
+    S = (T + per - 1) / per;
+    T = int(S * per);
+    W = n_pairs * S;
+  } else {
+    const int64_t tiles = n_pairs * T;
+    W = slots_sm;
+    if ((tiles + 1) / 2 < W) W = (tiles + 1) / 2;
+    if (W < 1) W = 1;
+    per = (tiles + W - 1) / W;
+    W = (tiles + per - 1) / per;   // CTAs that get tiles
   }
+  const size_t slots = size_t(W) + size_t(n_pairs);
+  const size_t need = kCounterBytes + slots * G * (DC_HD + 2) * sizeof(float);
+  if (!ws || ws_bytes < need) return set_error(QW_ERR_WORKSPACE, "qw_attention_decode: workspace of %zu bytes needed", need);
+  unsigned int* cnt = static_cast<unsigned int*>(ws);
+  float* wml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
+  float* wo = wml + slots * G * 2;
   CUtensorMap mk, mv;
   const uint64_t dims[3] = {uint64_t(DC_HD), uint64_t(nkv), uint64_t(num_slots)};
   const uint64_t strides[2] = {uint64_t(DC_HD) * 2, uint64_t(nkv) * DC_HD * 2};
   const uint32_t box[3] = {64u, 1u, uint32_t(DT_KT)};
-  int rc = make_tensor_map(&mk, kc, 3, dims, strides, box);
+  rc = make_tensor_map(&mk, kc, 3, dims, strides, box);
   if (rc) return rc;
   rc = make_tensor_map(&mv, vc, 3, dims, strides, box);
   if (rc) return rc;
-  dim3 grid(unsigned(p.splits), unsigned(nkv), unsigned(B));
-  launch_pdl(attn_decode_tc_kernel<G>, grid, DT_THREADS, DT_SMEM, st, mk, mv, static_cast<const bf16*>(q), cl, sb, nh, nkv,
-                                                              sl2, p.chunk, p.splits, wo, wml, cnt,
-                                                              static_cast<bf16*>(out));
+  launch_pdl(attn_decode_tc_kernel<G>, dim3(unsigned(W)), DT_THREADS, dt_smem<G>(), st, mk, mv,
+             static_cast<const bf16*>(q), cl, sb, nh, nkv, int(n_pairs), T, int(per), sl2, history_ready, wo, wml,
+             cnt, static_cast<bf16*>(out));
   return check_launch("attn_decode_tc_kernel");
 }
 
@@ -718,7 +907,8 @@ static int launch_decode(const void* q, const void* kc, const void* vc, const in
 extern "C" int qw_attention_decode(const void* q, const void* k_cache, const void* v_cache, int64_t num_slots,
                                    const int32_t* context_lens, const int32_t* seq_base, int B, int max_context,
                                    int n_heads, int n_kv_heads, int head_dim, float scale, void* out, void* workspace,
-                                   size_t workspace_bytes, int dtype, void* stream) {
+                                   size_t workspace_bytes, int dtype, int flags, void* stream) {
+  if (flags & ~QW_DECODE_HISTORY_READY) return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode: flags %d", flags);
   if (dtype != QW_BF16 && dtype != QW_F32) return set_error(QW_ERR_DTYPE, "qw_attention_decode: dtype %d", dtype);
   if (B < 0 || max_context < 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || num_slots < 0)
     return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode: bad sizes");
@@ -738,32 +928,39 @@ extern "C" int qw_attention_decode(const void* q, const void* k_cache, const voi
                : launch_attn_small<float>(q, k_cache, v_cache, nullptr, nullptr, seq_base, context_lens, B, 1,
                                           n_heads, n_kv_heads, head_dim, scale, out, st0);
   }
-  const DecodePlan p = decode_plan(B, max_context, n_kv_heads);
-  const size_t need = qw_attention_decode_workspace_size(B, max_context, n_heads, head_dim);
-  if (need && (!workspace || workspace_bytes < need))
-    return set_error(QW_ERR_WORKSPACE, "qw_attention_decode: workspace of %zu bytes needed", need);
-  if (need && size_t(B) * n_kv_heads * sizeof(unsigned int) > kCounterBytes)
+  if (size_t(B) * n_kv_heads * sizeof(unsigned int) > kCounterBytes)
     return set_error(QW_ERR_SHAPE, "qw_attention_decode: %d sequences x %d kv heads exceed the counter area", B,
                      n_kv_heads);
-  unsigned int* cnt = need ? static_cast<unsigned int*>(workspace) : nullptr;
-  float* wml = need ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kCounterBytes) : nullptr;
-  float* wo = wml ? wml + size_t(B) * n_heads * p.splits * 2 : nullptr;
   const float sl2 = scale * kLog2e;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == QW_BF16) {
+    const size_t bound = decode_tc_workspace_bound(B, n_heads);
+    if (!workspace || workspace_bytes < bound)
+      return set_error(QW_ERR_WORKSPACE, "qw_attention_decode: workspace of %zu bytes needed", bound);
     if (reinterpret_cast<uintptr_t>(k_cache) % 16 || reinterpret_cast<uintptr_t>(v_cache) % 16)
       return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode: caches must be 16-byte aligned");
     switch (G) {
       case 1: return launch_decode_tc<1>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, num_slots,
-                                         sl2, p, wo, wml, cnt, out, st);
+                                         max_context, sl2, workspace, workspace_bytes, flags & QW_DECODE_HISTORY_READY,
+                                         out, st);
       case 2: return launch_decode_tc<2>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, num_slots,
-                                         sl2, p, wo, wml, cnt, out, st);
+                                         max_context, sl2, workspace, workspace_bytes, flags & QW_DECODE_HISTORY_READY,
+                                         out, st);
       case 4: return launch_decode_tc<4>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, num_slots,
-                                         sl2, p, wo, wml, cnt, out, st);
+                                         max_context, sl2, workspace, workspace_bytes, flags & QW_DECODE_HISTORY_READY,
+                                         out, st);
       default: return launch_decode_tc<8>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads,
-                                          num_slots, sl2, p, wo, wml, cnt, out, st);
+                                          num_slots, max_context, sl2, workspace, workspace_bytes,
+                                          flags & QW_DECODE_HISTORY_READY, out, st);
     }
   }
+  const DecodePlan p = decode_plan(B, max_context, n_kv_heads);
+  const size_t need = p.splits > 1 ? kCounterBytes + size_t(B) * n_heads * p.splits * (DC_HD + 2) * sizeof(float) : 0;
+  if (need && (!workspace || workspace_bytes < need))
+    return set_error(QW_ERR_WORKSPACE, "qw_attention_decode: workspace of %zu bytes needed", need);
+  unsigned int* cnt = need ? static_cast<unsigned int*>(workspace) : nullptr;
+  float* wml = need ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kCounterBytes) : nullptr;
+  float* wo = wml ? wml + size_t(B) * n_heads * p.splits * 2 : nullptr;
 #define QW_DEC(TT)                                                                                                   \
   switch (G) {                                                                                                       \
     case 1: return launch_decode<TT, 1>(q, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads, sl2, p, \
@@ -838,7 +1035,7 @@ extern "C" int qw_attention_decode_static(const void* q, const void* k_cache, co
     if (rc != QW_OK) return rc;
   }
   return qw_attention_decode(q, k_cache, v_cache, num_slots, context_lens, seq_base, B, max_context, n_heads, n_kv_heads,
-                             head_dim, scale, out, ws, need > 0 ? qw::attn::kStaticScratchBytes : 0, dtype, stream);
+                             head_dim, scale, out, ws, need > 0 ? qw::attn::kStaticScratchBytes : 0, dtype, 0, stream);
 }
 
 namespace qw {

@@ -187,6 +187,9 @@ class Qwen3Forward:
         # slower today than the per-operation kernels chained with programmatic
         # dependent launch (2.4 vs 1.4 ms per 28-layer step of 8 tokens)
         self.fused_decode = False
+        # decode attention may stream cached history before the previous kernel ends
+        # (valid while slot_mapping[b] == seq_base[b] + context_lens[b] - 1)
+        self._history_ready = True
         self._fused = None     # (layer table, workspace), built on first use
 
     def _around(self, name: str, layer: int):
@@ -235,9 +238,12 @@ class Qwen3Forward:
         attn = self.attn[:T]
         with self._around(f"{ph}.attention", l):
             if decode:
+                # sequence b's cache is contiguous from seq_base[b], so the kernel just
+                # before (QK-norm + RoPE + KV store) writes only q and each sequence's
+                # last row: the history can stream in before that kernel finishes
                 L.attention_decode(q, self.k_cache[l], self.v_cache[l], ctx.context_lens, ctx.seq_base,
                                    ctx.max_context, m.n_heads, m.n_kv_heads, m.head_dim, self.scale, attn,
-                                   self.workspace, stream)
+                                   self.workspace, stream, history_ready=self._history_ready)
             else:
                 L.attention_prefill(q, self.k_cache[l], self.v_cache[l], ctx.cu_seqlens, ctx.cu_seqlens,
                                     ctx.seq_base, ctx.max_seqlen, m.n_heads, m.n_kv_heads, m.head_dim, self.scale,

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.qw_abi_version() == 3
+    assert lib.qw_abi_version() == 4
 
 
 def test_argument_errors_are_reported_before_launch(lib):
@@ -74,12 +74,15 @@ def test_argument_errors_are_reported_before_launch(lib):
     assert lib.qw_attention_prefill(fake, fake, fake, 64, fake, fake, None, 2, 8, 16, 8, 128, 0.1, fake, L.QW_F32,
                                     None) == L.QW_ERR_SHAPE
     assert lib.qw_attention_decode(fake, fake, fake, 100, fake, fake, 2, 8, 12, 4, 128, 0.1, fake, None, 0,
-                                   L.QW_BF16, None) == L.QW_ERR_SHAPE
+                                   L.QW_BF16, 0, None) == L.QW_ERR_SHAPE
     # decode without the workspace it needs
     need = lib.qw_attention_decode_workspace_size(8, 4096, 16, 128)
     assert need > 0
     assert lib.qw_attention_decode(fake, fake, fake, 100, fake, fake, 8, 4096, 16, 8, 128, 0.1, fake, None, 0,
-                                   L.QW_BF16, None) == L.QW_ERR_WORKSPACE
+                                   L.QW_BF16, 0, None) == L.QW_ERR_WORKSPACE
+    # unknown flags
+    assert lib.qw_attention_decode(fake, fake, fake, 100, fake, fake, 8, 4096, 16, 8, 128, 0.1, fake, None, 0,
+                                   L.QW_BF16, 2, None) == L.QW_ERR_INVALID_ARG
     # one-kernel decode step: at most 16 tokens, head_dim 128, group size 1/2/4/8
     args = lambda B, hd, nh, nkv: (fake, 28, fake, fake, fake, fake, fake, B, 100, 1024, nh, nkv, hd, 3072, 2, fake,  # noqa: E731
                                    4096, 100, 1e-6, 0.1, fake, fake, None, fake, 1 << 30, None)

@@ -450,6 +450,53 @@ def test_attention_decode(L, ctx, dtype):
         assert normwise_rel_err(got, ref) <= 1e-5
 
 
+DECODE_EDGE_CASES = {
+    # name: (context lengths, q heads, kv heads)
+    "empty_sequences": ([0, 5, 0, 300, 0], 16, 8),        # no keys: zero output
+    "many_sequences": ([17 + (7 * i) % 90 for i in range(200)], 16, 8),   # > 128 sequences per scan chunk
+    "one_long_many_short": ([4096, 1, 2, 64], 16, 8),      # one pair spans many CTAs
+    "group_1": ([130, 2049, 1], 8, 8),
+    "group_4": ([130, 2049, 65], 32, 8),
+    "group_8": ([700, 2049], 64, 8),
+    "single_key": ([1], 16, 8),
+}
+
+
+@pytest.mark.parametrize("case", sorted(DECODE_EDGE_CASES))
+def test_attention_decode_partition_edges(L, case):
+    """The bf16 decode kernel splits the (sequence, kv head, 64-key tile)
+    sequence into one contiguous range per CTA: empty sequences, more than
+    128 sequences, a pair spread over many CTAs and every GQA group size."""
+    ctx, nh, nkv = DECODE_EDGE_CASES[case]
+    hd = 128
+    B = len(ctx)
+    cap = [c + 3 for c in ctx]
+    base = np.concatenate([[0], np.cumsum(cap)[:-1]]).astype(np.int32)
+    S = int(sum(cap))
+    kc = si.normal(0, f"de.{case}.k", (S, nkv, hd), 1.0, "bf16")
+    vc = si.normal(0, f"de.{case}.v", (S, nkv, hd), 1.0, "bf16")
+    q = si.normal(0, f"de.{case}.q", (B, nh, hd), 1.0, "bf16")
+    out = torch.full((B, nh * hd), 7.0, dtype=torch.bfloat16, device="cuda")
+    mc = max(ctx)
+    ws = torch.zeros(L.attention_decode_workspace_size(B, mc, nh, hd), dtype=torch.uint8, device="cuda")
+    for _ in range(2):   # the completion counters must be left at zero for the next call
+        L.attention_decode(dev(q), dev(kc), dev(vc), dev(torch.tensor(ctx, dtype=torch.int32)),
+                           dev(torch.tensor(base)), mc, nh, nkv, hd, hd ** -0.5, out, ws)
+        sync_ok(L)
+        assert int(ws[:64 * 1024].view(torch.int32).abs().sum()) == 0
+    got = to_np(out).reshape(B, nh, hd)
+    kd, vd = kc.double().numpy(), vc.double().numpy()
+    live = [b for b in range(B) if ctx[b] > 0]
+    for b in range(B):
+        if ctx[b] == 0:
+            assert np.all(got[b] == 0.0), b
+    ref = O.attention_decode(q.double().numpy()[live], [kd[base[b]:base[b] + ctx[b]] for b in live],
+                             [vd[base[b]:base[b] + ctx[b]] for b in live], hd ** -0.5, "bf16")
+    err = np.abs(got[live] - ref)
+    assert np.all(err <= _attn_tol(ref, vd)), float(err.max())
+    assert float(np.mean(err)) < 2e-3
+
+
 # ----------------------------------------------------------------------------
 # lm_head and argmax
 # ----------------------------------------------------------------------------

@@ -23,7 +23,7 @@ CAP, CTX = 2176, 2049              # 2048 prompt keys + this step's key
 HIDDEN, LAYERS, COPIES, REPLAYS = 1024, 8, 16, 100
 
 
-def chain_mismatches(L, copies=COPIES, replays=REPLAYS, layers=LAYERS):
+def chain_mismatches(L, copies=COPIES, replays=REPLAYS, layers=LAYERS, history_ready=False):
     """Number of (replay, copy, layer) attention outputs that differ from replay 0."""
     g = torch.Generator(device="cuda").manual_seed(1234)
     bf = torch.bfloat16
@@ -44,7 +44,8 @@ def chain_mismatches(L, copies=COPIES, replays=REPLAYS, layers=LAYERS):
         for c in range(copies):
             for l in range(layers):
                 i = c * layers + l
-                L.attention_decode(q[l], kc[l], vc[l], cl, sb, CAP, NH, NKV, HD, HD ** -0.5, attn[i], ws[i])
+                L.attention_decode(q[l], kc[l], vc[l], cl, sb, CAP, NH, NKV, HD, HD ** -0.5, attn[i], ws[i],
+                                   history_ready=history_ready)
                 L.gemm(attn[i], wo[l], hout[i], HIDDEN, 2, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE)
 
     chain()
@@ -68,11 +69,14 @@ def chain_mismatches(L, copies=COPIES, replays=REPLAYS, layers=LAYERS):
     return bad
 
 
-def test_decode_chain_replays_bit_identical():
+@pytest.mark.parametrize("history_ready", [False, True])
+def test_decode_chain_replays_bit_identical(history_ready):
+    """history_ready: the kernel before each attention is a GEMV that writes
+    neither q nor the caches, so attention may stream its history early."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from qwen3_transformer_forward_gb300 import build
     build.build()
     from qwen3_transformer_forward_gb300 import _lib as L
     L.load()
-    assert chain_mismatches(L) == 0
+    assert chain_mismatches(L, history_ready=history_ready) == 0

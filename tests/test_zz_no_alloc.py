@@ -66,9 +66,10 @@ def test_static_scratch_matches_workspace_version_twice(L):
 
 def test_static_scratch_rejects_batches_beyond_its_size(L):
     from qwen3_transformer_forward_gb300._lib import QW_ERR_WORKSPACE, QwError
-    # one sequence, 64 q heads over 8 kv heads, up to 16384 keys: the split-KV
-    # plan needs 64 chunks x 64 heads x (128 + 2) floats, just over 2 MiB
-    B, mc, nh, nkv, hd = 1, 16384, 64, 8, 128
+    # 256 sequences of 16 q heads over 8 kv heads: one (m, l, o) slot per
+    # (CTA, pair) plus one per pair, (8 x SMs + 256 x 16) x (128 + 2) floats,
+    # is over 2 MiB
+    B, mc, nh, nkv, hd = 256, 64, 16, 8, 128
     assert L.attention_decode_workspace_size(B, mc, nh, hd) > L.attention_decode_static_scratch_bytes()
     q = torch.zeros(B, nh, hd, dtype=torch.bfloat16, device="cuda")
     kv = torch.zeros(8, nkv, hd, dtype=torch.bfloat16, device="cuda")
