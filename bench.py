@@ -326,6 +326,74 @@ def load_peaks():
         return {"hbm": 6800.0, "tensor": 1700.0, "tensor_burst": 1900.0, "source": "fallback"}
 
 
+def attention_traffic_from_profile():
+    """dram bytes per launch of the decode attention kernel from its committed ncu
+    summary, or None when attention.cu changed since that capture."""
+    import hashlib
+    import re
+    prof = os.path.join(ROOT, "profiles", "decode_attention_bench_shape.md")
+    src = os.path.join(ROOT, "qwen3_transformer_forward_gb300", "csrc", "attention.cu")
+    if not os.path.exists(prof):
+        return None
+    with open(prof) as f:
+        text = f.read()
+    with open(src, "rb") as f:
+        src_sha1 = hashlib.sha1(f.read()).hexdigest()
+    m_b = re.search(r"dram_bytes_per_launch = (\d+)", text)
+    m_h = re.search(r"attention\.cu sha1 = ([0-9a-f]{40})", text)
+    if not m_b or not m_h or src_sha1 != m_h.group(1):
+        return None
+    return int(m_b.group(1))
+
+
+def attention_roofline(wl, peaks, reps=5):
+    """Decode attention alone: one CUDA graph of 28 back-to-back launches, one per
+    layer's KV cache (2 GB together, larger than L2), on the decode step halfway
+    through the run.  Duration = graph time / launches (events on the replay stream)."""
+    from qwen3_transformer_forward_gb300 import _lib as L
+    fwd, m = wl.fwd, wl.m
+    s = wl.S // 2
+    B = wl.B
+    cl, base = wl.dcl[s], wl.dbase
+    q, out = fwd.q[:B], fwd.attn[:B]
+
+    def chain():
+        for l in range(m.n_layers):
+            L.attention_decode(q, fwd.k_cache[l], fwd.v_cache[l], cl, base, wl.max_context, m.n_heads, m.n_kv_heads,
+                               m.head_dim, fwd.scale, out, fwd.workspace, history_ready=True)
+
+    chain()
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        chain()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    L.device_error()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * m.n_layers)
+    ctx = [L0 + s + 1 for L0 in wl.seq_lens]
+    hd, nh, nkv = m.head_dim, m.n_heads, m.n_kv_heads
+    algo = 2.0 * 2 * nkv * hd * sum(ctx) + 2.0 * 2 * B * nh * hd
+    achieved = algo / (us * 1e-6) / 1e9
+    traffic = attention_traffic_from_profile()
+    if traffic is not None:   # the capture ran at the mean context: scale to this one
+        traffic = round(traffic * sum(ctx) / (B * (statistics.mean(wl.seq_lens) + wl.S // 2)))
+    return {"kernel": "decode.attention", "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 3), "traffic": traffic,
+            "algorithmic_bytes": round(algo), "us_per_launch": round(us, 2),
+            "peak_source": f"{peaks['source']} (HBM copy)",
+            "timing": f"{m.n_layers} back-to-back launches over the {m.n_layers} layers' KV caches (larger than L2), "
+                      f"decode step {s}, one CUDA graph replayed {reps} times, events on the replay stream"}
+
+
 def run_ours(args, rank, world, local):
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
@@ -407,6 +475,8 @@ def run_ours(args, rank, world, local):
                         "unit": kd["unit"], "frac": kd["frac"], "traffic": None,
                         "peak_source": f"{peaks['source']} ({'HBM copy' if kd['bound'] == 'hbm' else 'bf16 sustained'})",
                         "timing": probe_method}
+            if dom == "decode.attention":
+                roofline = attention_roofline(wl, peaks)
 
     if args.profile_window:
         torch.cuda.synchronize()
