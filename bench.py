@@ -290,7 +290,9 @@ class Workload:
             "decode.gemm_o": ("hbm", gemm_b(B, H, nh * hd)),
             "decode.gemm_gate_up_silu": ("hbm", 2.0 * (2 * I * H + B * H + B * I)),
             "decode.gemm_down": ("hbm", gemm_b(B, H, I)),
-            "decode.attention": ("hbm", 2.0 * 2 * nkv * hd * B * mean_ctx + 2.0 * 2 * B * nh * hd),
+            # with the QK-norm + RoPE + KV store folded in: the QKV rows in, the new k/v rows out
+            "decode.attention": ("hbm", 2.0 * 2 * nkv * hd * B * mean_ctx + 2.0 * B * nh * hd
+                                 + 2.0 * B * qkvw + 2.0 * 2 * B * nkv * hd + 16.0 * B),
             "decode.add_rmsnorm": ("hbm", 2.0 * B * H * 4),
             "decode.qkv_norm_rope_store_kv": ("hbm", 2.0 * B * (qkvw + nh * hd + 2 * nkv * hd) + 16.0 * B),
             # one persistent kernel per decode step: every layer's weights, the K/V
@@ -355,12 +357,16 @@ def attention_roofline(wl, peaks, reps=5):
     s = wl.S // 2
     B = wl.B
     cl, base = wl.dcl[s], wl.dbase
-    q, out = fwd.q[:B], fwd.attn[:B]
+    out = fwd.attn[:B]
 
-    def chain():
+    qkv, pos, slots = fwd.qkv[:B], wl.dpos[s], wl.dslots[s]
+
+    def chain():   # (stores k/v rows from the qkv buffer, the last decode step's, at step s's slots; the next replay of the step rewrites them)
         for l in range(m.n_layers):
-            L.attention_decode(q, fwd.k_cache[l], fwd.v_cache[l], cl, base, wl.max_context, m.n_heads, m.n_kv_heads,
-                               m.head_dim, fwd.scale, out, fwd.workspace, history_ready=True)
+            p = wl.params.layers[l]
+            L.attention_decode_rope(qkv, m.n_heads, m.n_kv_heads, m.head_dim, m.tp, pos, fwd.cos_sin, p.q_norm,
+                                    p.k_norm, m.eps, slots, fwd.k_cache[l], fwd.v_cache[l], fwd.err, cl, base,
+                                    wl.max_context, fwd.scale, out, fwd.workspace, history_ready=True)
 
     chain()
     torch.cuda.synchronize()
@@ -381,7 +387,8 @@ def attention_roofline(wl, peaks, reps=5):
     us = e0.elapsed_time(e1) * 1e3 / (reps * m.n_layers)
     ctx = [L0 + s + 1 for L0 in wl.seq_lens]
     hd, nh, nkv = m.head_dim, m.n_heads, m.n_kv_heads
-    algo = 2.0 * 2 * nkv * hd * sum(ctx) + 2.0 * 2 * B * nh * hd
+    qkvw = (nh + 2 * nkv) * hd
+    algo = 2.0 * 2 * nkv * hd * sum(ctx) + 2.0 * B * nh * hd + 2.0 * B * qkvw + 2.0 * 2 * B * nkv * hd + 16.0 * B
     achieved = algo / (us * 1e-6) / 1e9
     traffic = attention_traffic_from_profile()
     if traffic is not None:   # the capture ran at the mean context: scale to this one
@@ -516,8 +523,11 @@ def count_launches(wl):
     from qwen3_transformer_forward_gb300 import _lib as L
     m = wl.m
     per_layer = 2 + 1 + 1 + 1 + 1 + 1 + 1   # 2 norms, qkv gemm, rope/kv, attention, o, gate_up, down
-    # decode with few tokens: the input norm runs inside the QKV GEMM
+    # decode with few tokens: the input norm runs inside the QKV GEMM; in bf16 the
+    # QK-norm + RoPE + KV store runs inside decode attention
     dec_layer = per_layer - 1 if wl.fwd.norm_fusion_ok(wl.B) else per_layer
+    if wl.fwd.dtype == torch.bfloat16 and m.head_dim == 128:
+        dec_layer -= 1
     # split-K sums and the split-KV merge happen inside the GEMM and attention kernels
     prefill = 1 + m.n_layers * per_layer + 1 + 3     # embed, layers, final norm, gather + gemm + argmax
     lm_dec = 2                                       # gemm + argmax
@@ -663,14 +673,20 @@ def profile_kernel(args):
     cap = max(seqs) + S
     g = torch.Generator(device="cuda").manual_seed(0)
     rnd = lambda *shape: torch.randn(*shape, device="cuda", generator=g).to(torch.bfloat16)  # noqa: E731
-    if args.profile_kernel == "decode.attention":
-        kc, vc, q = rnd(nb * cap, nkv, hd), rnd(nb * cap, nkv, hd), rnd(nb, nh, hd)
+    if args.profile_kernel == "decode.attention":   # with the folded QK-norm + RoPE + KV store
+        kc, vc = rnd(nb * cap, nkv, hd), rnd(nb * cap, nkv, hd)
+        qkv = rnd(nb, (nh + 2 * nkv) * hd)
+        gamma = torch.ones(hd, dtype=torch.bfloat16, device="cuda")
         ctx = torch.tensor([L0 + S // 2 for L0 in seqs], dtype=torch.int32, device="cuda")
         base = torch.arange(nb, dtype=torch.int32, device="cuda") * cap
+        pos = (ctx - 1).to(torch.int64)
+        slots = base.to(torch.int64) + pos
+        cs = L.rope_cos_sin_table(m.max_position, hd, m.rope_theta).cuda()
         out = torch.empty(nb, nh * hd, dtype=torch.bfloat16, device="cuda")
         ws = torch.zeros(L.attention_decode_workspace_size(nb, cap, nh, hd), dtype=torch.uint8, device="cuda")
         for _ in range(args.profile_reps):
-            L.attention_decode(q, kc, vc, ctx, base, cap, nh, nkv, hd, hd ** -0.5, out, ws)
+            L.attention_decode_rope(qkv, nh, nkv, hd, m.tp, pos, cs, gamma, gamma, m.eps, slots, kc, vc, None, ctx,
+                                    base, cap, hd ** -0.5, out, ws)
     torch.cuda.synchronize()
     L.device_error()
 

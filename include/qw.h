@@ -202,6 +202,34 @@ int qw_attention_decode(const void* q, const void* k_cache, const void* v_cache,
 size_t qw_attention_decode_workspace_size(int B, int max_context, int n_heads, int head_dim);
 
 /*
+ * Decode step's QK-RMSNorm + RoPE + KV-cache store ([SK] §3, §7.1, §8) and
+ * decode attention ([SK] §7.2) in one launch: qw_qkv_norm_rope_store_kv on
+ * one token per sequence followed by qw_attention_decode, without the q_out
+ * round trip.
+ *   qkv bf16 [B, tp * (nh/tp + 2*nkv/tp) * 128]: the merged QKV output, shard r
+ *       holding [q_r; k_r; v_r] (as for qw_qkv_norm_rope_store_kv);
+ *   positions int64 [B], cos_sin, max_position, q_gamma, k_gamma, eps,
+ *       slot_mapping int64 [B], err_count: as for qw_qkv_norm_rope_store_kv;
+ *   k_cache, v_cache bf16 [num_slots, nkv, 128] (16-byte aligned);
+ *   context_lens, seq_base, max_context, scale, out, workspace, flags: as for
+ *       qw_attention_decode (workspace from qw_attention_decode_workspace_size).
+ * Sequence b's key positions 0 .. context_lens[b] - 1 sit at cache rows
+ * seq_base[b] + position, and this step's k and v are the ones at position
+ * context_lens[b] - 1: slot_mapping[b] must be seq_base[b] + context_lens[b]
+ * - 1, or -1 for a sequence whose k/v is not stored (then context_lens[b] must
+ * not count it).  A sequence with context_lens[b] = 0 stores nothing and gets
+ * a zero output.  Rules: bf16, head_dim 128, nh % nkv == 0 with group 1/2/4/8,
+ * tp divides nh and nkv.
+ */
+int qw_attention_decode_rope(const void* qkv, int n_heads, int n_kv_heads, int head_dim, int tp,
+                             const int64_t* positions, const float* cos_sin, int64_t max_position,
+                             const void* q_gamma, const void* k_gamma, float eps, const int64_t* slot_mapping,
+                             void* k_cache, void* v_cache, int64_t num_slots, int32_t* err_count,
+                             const int32_t* context_lens, const int32_t* seq_base, int B, int max_context,
+                             float scale, void* out, void* workspace, size_t workspace_bytes, int dtype, int flags,
+                             void* stream);
+
+/*
  * Decode attention that needs no workspace from the caller.  The pages have
  * no counterpart: this entry point exists for callers that cannot allocate
  * device memory themselves, such as a plugin that a host framework hands

@@ -38,6 +38,8 @@ SIGNATURES = {
     "qw_attention_decode": (C.c_int, [_p, _p, _p, _i64, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _p, _sz,
                                       _i32, _i32, _p]),
     "qw_attention_decode_workspace_size": (C.c_size_t, [_i32, _i32, _i32, _i32]),
+    "qw_attention_decode_rope": (C.c_int, [_p, _i32, _i32, _i32, _i32, _p, _p, _i64, _p, _p, _f32, _p, _p, _p, _i64,
+                                           _p, _p, _p, _i32, _i32, _f32, _p, _p, _sz, _i32, _i32, _p]),
     "qw_attention_decode_static": (C.c_int, [_p, _p, _p, _i64, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _i32,
                                              _p]),
     "qw_attention_decode_static_scratch_bytes": (C.c_size_t, []),
@@ -194,6 +196,21 @@ def attention_decode(q, k_cache, v_cache, context_lens, seq_base, max_context, n
         _dev_ptr(context_lens, "context_lens"), _dev_ptr(seq_base, "seq_base"), B, max_context, n_heads, n_kv_heads,
         head_dim, scale, _dev_ptr(out, "out"), _dev_ptr(workspace, "workspace"), ws_bytes, dtype_code(q.dtype),
         QW_DECODE_HISTORY_READY if history_ready else 0, _stream(stream)))
+
+
+def attention_decode_rope(qkv, n_heads, n_kv_heads, head_dim, tp, positions, cos_sin, q_gamma, k_gamma, eps,
+                          slot_mapping, k_cache, v_cache, err_count, context_lens, seq_base, max_context, scale, out,
+                          workspace, stream=None, history_ready=False):
+    """QK-norm + RoPE + KV store of one decode token per sequence, then decode attention, in one launch."""
+    B = qkv.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().qw_attention_decode_rope(
+        _dev_ptr(qkv, "qkv"), n_heads, n_kv_heads, head_dim, tp, _dev_ptr(positions, "positions"),
+        _dev_ptr(cos_sin, "cos_sin"), cos_sin.shape[0], _dev_ptr(q_gamma, "q_gamma"), _dev_ptr(k_gamma, "k_gamma"),
+        eps, _dev_ptr(slot_mapping, "slot_mapping"), _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"),
+        k_cache.shape[0], _dev_ptr(err_count, "err_count"), _dev_ptr(context_lens, "context_lens"),
+        _dev_ptr(seq_base, "seq_base"), B, max_context, scale, _dev_ptr(out, "out"), _dev_ptr(workspace, "workspace"),
+        ws_bytes, dtype_code(qkv.dtype), QW_DECODE_HISTORY_READY if history_ready else 0, _stream(stream)))
 
 
 def attention_decode_static(q, k_cache, v_cache, context_lens, seq_base, max_context, n_heads, n_kv_heads,

@@ -433,12 +433,32 @@ __device__ __forceinline__ unsigned int atom_add_acq_rel_gpu(unsigned int* p, un
   return old;
 }
 
+// The QK-RMSNorm + RoPE + KV store of the decode step ([SK] §3, §7.1, §8),
+// folded into the decode kernel: the q heads come from the merged QKV output,
+// and the CTA holding a pair's last tile stores that kv head's new k (normed,
+// roped) and v before it loads the tile.  qkv == nullptr: q is read as given.
+struct DecodeRope {
+  const bf16* qkv;            // [B, tp * (nh/tp + 2 nkv/tp) * 128], shard r = [q_r; k_r; v_r]
+  const int64_t* positions;   // [B]
+  const int64_t* slots;       // [B]: cache row of this step's k/v; -1 = not stored
+  const float* cos_sin;       // [max_pos, 128]: cos | sin
+  int64_t max_pos;
+  const bf16* q_gamma;        // [128]
+  const bf16* k_gamma;        // [128]
+  float eps;
+  int tp;
+  int32_t* err;               // counts bad positions and slots (may be null)
+  bf16* k_cache;
+  bf16* v_cache;
+  int64_t num_slots;
+};
+
 template <int G>
 __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const bf16* __restrict__ q,
     const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ seq_base, int nh, int nkv, int n_pairs,
     int T, int per, float scale_log2, int history_ready, float* __restrict__ ws_o, float* __restrict__ ws_ml,
-    unsigned int* __restrict__ counters, bf16* __restrict__ out) {
+    unsigned int* __restrict__ counters, bf16* __restrict__ out, const DecodeRope rp) {
   // history_ready: context lengths, bases and every cached row but each
   // sequence's last were complete before the previous kernel started, which
   // writes only q and those last rows.  Then the lengths are read and the
@@ -522,6 +542,67 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
     pdl_wait();      // q and the sequences' last rows are complete and visible
     pdl_trigger();   // only now may the next kernel start its prologue
   }
+  // ---- folded QK-norm + RoPE: head (sequence b, head slot h_off in a shard row) of
+  // the QKV output normed by gamma, roped at positions[b] and rounded to bf16.
+  // Thread d owns element d; RoPE pairs (d, d ^ 64) meet through shared memory.
+  float* nrm = sO;                                           // [G][128] normed values
+  bf16* qs = reinterpret_cast<bf16*>(sO + G * DC_HD);        // [G][128] roped q
+  float* red = sML;                                          // [G][4] sums of squares
+  const int d = tid;
+  const int nh_l = nh / rp.tp, nkv_l = nkv / rp.tp;
+  const int64_t width_r = int64_t(nh_l + 2 * nkv_l) * DC_HD;
+  auto norm_rope = [&](int b, const int64_t* h_off, const bf16* gamma, int nheads, float* y) {
+    const int64_t pos = rp.positions[b];
+    const bool pos_ok = pos >= 0 && pos < rp.max_pos;
+    const bf16* row = rp.qkv + int64_t(b) * width_r * rp.tp;
+    float x[G];
+    for (int j = 0; j < nheads; ++j) {
+      x[j] = __bfloat162float(row[h_off[j] + d]);
+      const float ss = warp_sum(x[j] * x[j]);
+      if (lane == 0) red[j * 4 + warp] = ss;
+    }
+    __syncthreads();
+    const float gm = __bfloat162float(gamma[d]);
+    for (int j = 0; j < nheads; ++j) {
+      const float ss = red[j * 4] + red[j * 4 + 1] + red[j * 4 + 2] + red[j * 4 + 3];
+      const float inv = rsqrtf(ss / float(DC_HD) + rp.eps);
+      nrm[j * DC_HD + d] = round_t<bf16>((x[j] * inv) * gm);   // q_norm / k_norm output
+    }
+    __syncthreads();
+    const float* cs = rp.cos_sin + (pos_ok ? pos : 0) * DC_HD;
+    const int i = d & 63;
+    const float c = cs[i], sn = cs[64 + i];
+    for (int j = 0; j < nheads; ++j) {
+      const float n = nrm[j * DC_HD + d], np = nrm[j * DC_HD + (d ^ 64)];
+      y[j] = pos_ok ? (d < 64 ? n * c - np * sn : n * c + np * sn) : 0.0f;
+    }
+    __syncthreads();   // nrm and red are free again
+    return pos_ok;
+  };
+  if (rp.qkv != nullptr) {
+    // this CTA holds the last tile of pair p: store that kv head's new k and v
+    for (int p = p_first; p <= p_last; ++p) {
+      int ta, tb, Tb;
+      seg_range(p, ta, tb, Tb);
+      if (Tb == 0 || tb != Tb) continue;   // (uniform over the CTA)
+      const int b = p / nkv, g = p % nkv;
+      const int64_t k_off = int64_t(g / nkv_l) * width_r + int64_t(nh_l + g % nkv_l) * DC_HD;
+      float y[G];
+      const bool pos_ok = norm_rope(b, &k_off, rp.k_gamma, 1, y);
+      const int64_t slot = rp.slots[b];
+      if (slot != -1) {
+        const bool slot_ok = slot >= 0 && slot < rp.num_slots;
+        if (slot_ok && pos_ok) {
+          rp.k_cache[(slot * nkv + g) * DC_HD + d] = __float2bfloat16_rn(y[0]);
+          rp.v_cache[(slot * nkv + g) * DC_HD + d] = rp.qkv[int64_t(b) * width_r * rp.tp + k_off + int64_t(nkv_l) * DC_HD + d];
+        }
+        if (g == 0 && d == 0 && rp.err != nullptr && (!slot_ok || !pos_ok)) atomicAdd(rp.err, 1);
+      }
+    }
+    // the stores above before the tensor copies that read them back
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncthreads();
+  }
   if (tid == 0)
     for (int j = issued; j < DT_STAGES && j < n_tiles; ++j)
       if (prod_next()) issue(j);
@@ -540,7 +621,23 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
     // q of this thread's row (head g * G + gq; rows >= G are zero)
     uint32_t qa[8][2];
     {
-      const bf16* qr = q + (int64_t(b) * nh + g * G + (gq < G ? gq : 0)) * DC_HD;
+      const bf16* qr;
+      if (rp.qkv == nullptr) {
+        qr = q + (int64_t(b) * nh + g * G + (gq < G ? gq : 0)) * DC_HD;
+      } else {   // QK-norm + RoPE of the group's q heads, into shared memory
+        int64_t q_off[G];
+#pragma unroll
+        for (int jh = 0; jh < G; ++jh) {
+          const int h = g * G + jh;
+          q_off[jh] = int64_t(h / nh_l) * width_r + int64_t(h % nh_l) * DC_HD;
+        }
+        float y[G];
+        norm_rope(b, q_off, rp.q_gamma, G, y);
+#pragma unroll
+        for (int jh = 0; jh < G; ++jh) qs[jh * DC_HD + d] = __float2bfloat16_rn(y[jh]);
+        __syncthreads();
+        qr = qs + (gq < G ? gq : 0) * DC_HD;
+      }
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         qa[kk][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tq) : 0u;
@@ -640,7 +737,6 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
     __syncthreads();
     const int c_first = int(int64_t(p) * T / per), c_last = int((int64_t(p) * T + T - 1) / per);
     const bool split = c_first != c_last;
-    const int d = tid;
 #pragma unroll
     for (int jh = 0; jh < G; ++jh) {
       float M = -INFINITY;
@@ -837,7 +933,8 @@ static int decode_tc_ctas_per_sm(int* out) {
 template <int G>
 static int launch_decode_tc(const void* q, const void* kc, const void* vc, const int32_t* cl, const int32_t* sb,
                             int B, int nh, int nkv, int64_t num_slots, int max_context, float sl2, void* ws,
-                            size_t ws_bytes, int history_ready, void* out, cudaStream_t st) {
+                            size_t ws_bytes, int history_ready, void* out, cudaStream_t st,
+                            const DecodeRope& rp = DecodeRope{}) {
   int per_sm = 0;
   int rc = decode_tc_ctas_per_sm<G>(&per_sm);
   if (rc) return rc;
@@ -882,7 +979,7 @@ static int launch_decode_tc(const void* q, const void* kc, const void* vc, const
   if (rc) return rc;
   launch_pdl(attn_decode_tc_kernel<G>, dim3(unsigned(W)), DT_THREADS, dt_smem<G>(), st, mk, mv,
              static_cast<const bf16*>(q), cl, sb, nh, nkv, int(n_pairs), T, int(per), sl2, history_ready, wo, wml,
-             cnt, static_cast<bf16*>(out));
+             cnt, static_cast<bf16*>(out), rp);
   return check_launch("attn_decode_tc_kernel");
 }
 
@@ -974,6 +1071,64 @@ extern "C" int qw_attention_decode(const void* q, const void* k_cache, const voi
   }
   QW_DEC(float)
 #undef QW_DEC
+}
+
+extern "C" int qw_attention_decode_rope(const void* qkv, int n_heads, int n_kv_heads, int head_dim, int tp,
+                                        const int64_t* positions, const float* cos_sin, int64_t max_position,
+                                        const void* q_gamma, const void* k_gamma, float eps,
+                                        const int64_t* slot_mapping, void* k_cache, void* v_cache, int64_t num_slots,
+                                        int32_t* err_count, const int32_t* context_lens, const int32_t* seq_base,
+                                        int B, int max_context, float scale, void* out, void* workspace,
+                                        size_t workspace_bytes, int dtype, int flags, void* stream) {
+  if (dtype != QW_BF16) return set_error(QW_ERR_DTYPE, "qw_attention_decode_rope: bf16 only");
+  if (flags & ~QW_DECODE_HISTORY_READY)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode_rope: flags %d", flags);
+  if (B < 0 || max_context < 0 || n_heads <= 0 || n_kv_heads <= 0 || tp <= 0 || num_slots < 0 || max_position <= 0)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode_rope: bad sizes");
+  const int G = n_kv_heads > 0 ? n_heads / n_kv_heads : 0;
+  if (head_dim != 128 || n_heads % n_kv_heads || n_heads % tp || n_kv_heads % tp ||
+      (G != 1 && G != 2 && G != 4 && G != 8))
+    return set_error(QW_ERR_SHAPE,
+                     "qw_attention_decode_rope: needs head_dim 128, nh %% nkv == 0 with group 1/2/4/8, tp | nh, nkv");
+  if (B == 0) return QW_OK;
+  if (!qkv || !positions || !cos_sin || !q_gamma || !k_gamma || !slot_mapping || !k_cache || !v_cache ||
+      !context_lens || !seq_base || !out)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode_rope: null pointer");
+  if (reinterpret_cast<uintptr_t>(k_cache) % 16 || reinterpret_cast<uintptr_t>(v_cache) % 16)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode_rope: caches must be 16-byte aligned");
+  if (size_t(B) * n_kv_heads * sizeof(unsigned int) > kCounterBytes)
+    return set_error(QW_ERR_SHAPE, "qw_attention_decode_rope: %d sequences x %d kv heads exceed the counter area",
+                     B, n_kv_heads);
+  const size_t bound = decode_tc_workspace_bound(B, n_heads);
+  if (!workspace || workspace_bytes < bound)
+    return set_error(QW_ERR_WORKSPACE, "qw_attention_decode_rope: workspace of %zu bytes needed", bound);
+  DecodeRope rp;
+  rp.qkv = static_cast<const bf16*>(qkv);
+  rp.positions = positions;
+  rp.slots = slot_mapping;
+  rp.cos_sin = cos_sin;
+  rp.max_pos = max_position;
+  rp.q_gamma = static_cast<const bf16*>(q_gamma);
+  rp.k_gamma = static_cast<const bf16*>(k_gamma);
+  rp.eps = eps;
+  rp.tp = tp;
+  rp.err = err_count;
+  rp.k_cache = static_cast<bf16*>(k_cache);
+  rp.v_cache = static_cast<bf16*>(v_cache);
+  rp.num_slots = num_slots;
+  const float sl2 = scale * kLog2e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int hr = flags & QW_DECODE_HISTORY_READY;
+  switch (G) {
+    case 1: return launch_decode_tc<1>(nullptr, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads,
+                                       num_slots, max_context, sl2, workspace, workspace_bytes, hr, out, st, rp);
+    case 2: return launch_decode_tc<2>(nullptr, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads,
+                                       num_slots, max_context, sl2, workspace, workspace_bytes, hr, out, st, rp);
+    case 4: return launch_decode_tc<4>(nullptr, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads,
+                                       num_slots, max_context, sl2, workspace, workspace_bytes, hr, out, st, rp);
+    default: return launch_decode_tc<8>(nullptr, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads,
+                                        num_slots, max_context, sl2, workspace, workspace_bytes, hr, out, st, rp);
+  }
 }
 
 // ===========================================================================

@@ -188,7 +188,8 @@ class Qwen3Forward:
         # dependent launch (2.4 vs 1.4 ms per 28-layer step of 8 tokens)
         self.fused_decode = False
         # decode attention may stream cached history before the previous kernel ends
-        # (valid while slot_mapping[b] == seq_base[b] + context_lens[b] - 1)
+        # (valid while slot_mapping[b] == seq_base[b] + context_lens[b] - 1, which the
+        # folded KV store requires anyway)
         self._history_ready = True
         self._fused = None     # (layer table, workspace), built on first use
 
@@ -231,23 +232,32 @@ class Qwen3Forward:
             with self._around(f"{ph}.gemm_qkv", l):
                 L.gemm(y, p.qkv, qkv, self.qkv_width, tp, L.QW_GEMM_COLUMN, L.QW_EPI_NONE, self.workspace, stream)
         q = self.q[:T]
-        with self._around(f"{ph}.qkv_norm_rope_store_kv", l):
-            L.qkv_norm_rope_store_kv(qkv, m.n_heads, m.n_kv_heads, m.head_dim, tp, ctx.positions, self.cos_sin,
-                                     p.q_norm, p.k_norm, m.eps, ctx.slot_mapping, self.k_cache[l], self.v_cache[l],
-                                     q, self.err, stream)
         attn = self.attn[:T]
-        with self._around(f"{ph}.attention", l):
-            if decode:
-                # sequence b's cache is contiguous from seq_base[b], so the kernel just
-                # before (QK-norm + RoPE + KV store) writes only q and each sequence's
-                # last row: the history can stream in before that kernel finishes
-                L.attention_decode(q, self.k_cache[l], self.v_cache[l], ctx.context_lens, ctx.seq_base,
-                                   ctx.max_context, m.n_heads, m.n_kv_heads, m.head_dim, self.scale, attn,
-                                   self.workspace, stream, history_ready=self._history_ready)
-            else:
-                L.attention_prefill(q, self.k_cache[l], self.v_cache[l], ctx.cu_seqlens, ctx.cu_seqlens,
-                                    ctx.seq_base, ctx.max_seqlen, m.n_heads, m.n_kv_heads, m.head_dim, self.scale,
-                                    attn, stream)
+        if decode and self.dtype == torch.bfloat16 and m.head_dim == 128:
+            # QK-norm + RoPE + KV store folded into decode attention.  Sequence b's
+            # cache is contiguous from seq_base[b] and this step's k/v go to its last
+            # row, so the kernel before (the QKV GEMV) writes none of the cached
+            # history: the history can stream in before that kernel finishes.
+            with self._around(f"{ph}.attention", l):
+                L.attention_decode_rope(qkv, m.n_heads, m.n_kv_heads, m.head_dim, tp, ctx.positions, self.cos_sin,
+                                        p.q_norm, p.k_norm, m.eps, ctx.slot_mapping, self.k_cache[l],
+                                        self.v_cache[l], self.err, ctx.context_lens, ctx.seq_base, ctx.max_context,
+                                        self.scale, attn, self.workspace, stream,
+                                        history_ready=self._history_ready)
+        else:
+            with self._around(f"{ph}.qkv_norm_rope_store_kv", l):
+                L.qkv_norm_rope_store_kv(qkv, m.n_heads, m.n_kv_heads, m.head_dim, tp, ctx.positions, self.cos_sin,
+                                         p.q_norm, p.k_norm, m.eps, ctx.slot_mapping, self.k_cache[l],
+                                         self.v_cache[l], q, self.err, stream)
+            with self._around(f"{ph}.attention", l):
+                if decode:
+                    L.attention_decode(q, self.k_cache[l], self.v_cache[l], ctx.context_lens, ctx.seq_base,
+                                       ctx.max_context, m.n_heads, m.n_kv_heads, m.head_dim, self.scale, attn,
+                                       self.workspace, stream)
+                else:
+                    L.attention_prefill(q, self.k_cache[l], self.v_cache[l], ctx.cu_seqlens, ctx.cu_seqlens,
+                                        ctx.seq_base, ctx.max_seqlen, m.n_heads, m.n_kv_heads, m.head_dim,
+                                        self.scale, attn, stream)
         with self._around(f"{ph}.gemm_o", l):
             L.gemm(attn, p.o, h, m.hidden, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, self.workspace, stream)
         act = self.act[:T]

@@ -83,6 +83,16 @@ def test_argument_errors_are_reported_before_launch(lib):
     # unknown flags
     assert lib.qw_attention_decode(fake, fake, fake, 100, fake, fake, 8, 4096, 16, 8, 128, 0.1, fake, None, 0,
                                    L.QW_BF16, 2, None) == L.QW_ERR_INVALID_ARG
+    # decode attention with the QK-norm + RoPE + KV store folded in: bf16, head_dim 128, tp | heads
+    rope = lambda hd, nh, nkv, tp, dt, flags, ws, wsb: (fake, nh, nkv, hd, tp, fake, fake, 4096, fake, fake, 1e-6,  # noqa: E731
+                                                        fake, fake, fake, 100, None, fake, fake, 8, 2048, 0.1, fake,
+                                                        ws, wsb, dt, flags, None)
+    assert lib.qw_attention_decode_rope(*rope(128, 16, 8, 2, L.QW_F32, 0, None, 0)) == L.QW_ERR_DTYPE
+    assert lib.qw_attention_decode_rope(*rope(64, 16, 8, 2, L.QW_BF16, 0, None, 0)) == L.QW_ERR_SHAPE
+    assert lib.qw_attention_decode_rope(*rope(128, 16, 8, 3, L.QW_BF16, 0, None, 0)) == L.QW_ERR_SHAPE
+    assert lib.qw_attention_decode_rope(*rope(128, 12, 4, 2, L.QW_BF16, 0, None, 0)) == L.QW_ERR_SHAPE
+    assert lib.qw_attention_decode_rope(*rope(128, 16, 8, 2, L.QW_BF16, 4, None, 0)) == L.QW_ERR_INVALID_ARG
+    assert lib.qw_attention_decode_rope(*rope(128, 16, 8, 2, L.QW_BF16, 0, None, 0)) == L.QW_ERR_WORKSPACE
     # one-kernel decode step: at most 16 tokens, head_dim 128, group size 1/2/4/8
     args = lambda B, hd, nh, nkv: (fake, 28, fake, fake, fake, fake, fake, B, 100, 1024, nh, nkv, hd, 3072, 2, fake,  # noqa: E731
                                    4096, 100, 1e-6, 0.1, fake, fake, None, fake, 1 << 30, None)

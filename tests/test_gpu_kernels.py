@@ -497,6 +497,86 @@ def test_attention_decode_partition_edges(L, case):
     assert float(np.mean(err)) < 2e-3
 
 
+ROPE_DECODE_CASES = {
+    # name: (context lengths, q heads, kv heads, tp)
+    "mixed_tp2": ([1, 63, 64, 65, 700], 16, 8, 2),
+    "bench_shape": ([2049] * 8, 16, 8, 2),
+    "group1_tp1": ([130, 2049, 1], 8, 8, 1),
+    "group4": ([700, 2049], 32, 8, 2),
+    "not_stored": ([0, 5, 300], 16, 8, 2),    # sequence 0: slot -1, no keys
+}
+
+
+@pytest.mark.parametrize("case", sorted(ROPE_DECODE_CASES))
+@pytest.mark.parametrize("history_ready", [False, True])
+def test_attention_decode_rope(L, case, history_ready):
+    """QK-norm + RoPE + KV store folded into decode attention, against the
+    oracle: the stored k (two roundings) and the bit-copied v, and the
+    attention output over the cache with this step's rows in place."""
+    ctx, nh, nkv, tp = ROPE_DECODE_CASES[case]
+    hd, B = 128, len(ctx)
+    m = si.ModelShape(vocab=64, hidden=64, n_heads=nh, n_kv_heads=nkv, head_dim=hd, intermediate=64, n_layers=1,
+                      tp=tp, dtype="bf16", max_position=4096)
+    cap = [c + 3 for c in ctx]
+    base = np.concatenate([[0], np.cumsum(cap)[:-1]]).astype(np.int32)
+    S = int(sum(cap))
+    width = tp * (nh // tp + 2 * (nkv // tp)) * hd
+    qkv = si.normal(0, f"dr.{case}.qkv", (B, width), 1.0, "bf16")
+    qg = (si.normal(0, f"dr.{case}.qg", (hd,), 0.2, "f32") + 1.0).to(torch.bfloat16)
+    kg = (si.normal(0, f"dr.{case}.kg", (hd,), 0.2, "f32") + 1.0).to(torch.bfloat16)
+    kc = si.normal(0, f"dr.{case}.k", (S, nkv, hd), 1.0, "bf16")
+    vc = si.normal(0, f"dr.{case}.v", (S, nkv, hd), 1.0, "bf16")
+    pos = torch.tensor([max(c - 1, 0) for c in ctx], dtype=torch.int64)
+    slots = torch.tensor([int(base[b]) + ctx[b] - 1 if ctx[b] > 0 else -1 for b in range(B)], dtype=torch.int64)
+    cs = L.rope_cos_sin_table(m.max_position, hd, m.rope_theta)
+    kc_d, vc_d = dev(kc.clone()), dev(vc.clone())
+    out = torch.full((B, nh * hd), 7.0, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mc = max(ctx)
+    ws = torch.zeros(L.attention_decode_workspace_size(B, max(mc, 1), nh, hd), dtype=torch.uint8, device="cuda")
+    L.attention_decode_rope(dev(qkv), nh, nkv, hd, tp, dev(pos), dev(cs), dev(qg), dev(kg), m.eps, dev(slots),
+                            kc_d, vc_d, err, dev(torch.tensor(ctx, dtype=torch.int32)), dev(torch.tensor(base)),
+                            max(mc, 1), hd ** -0.5, out, ws, history_ready=history_ready)
+    sync_ok(L)
+    assert int(err.item()) == 0
+    assert int(ws[:64 * 1024].view(torch.int32).abs().sum()) == 0
+    # oracle: split the merged rows per shard, norm, rope, store, attend
+    cos_t, sin_t = O.rope_cos_sin(m.max_position, hd, m.rope_theta)
+    nh_l, nkv_l = nh // tp, nkv // tp
+    x = qkv.double().numpy()
+    wr = (nh_l + 2 * nkv_l) * hd
+    qs, ks, vs = [], [], []
+    for r in range(tp):
+        blk = x[:, r * wr:(r + 1) * wr]
+        qs.append(blk[:, : nh_l * hd].reshape(B, nh_l, hd))
+        ks.append(blk[:, nh_l * hd:(nh_l + nkv_l) * hd].reshape(B, nkv_l, hd))
+        vs.append(blk[:, (nh_l + nkv_l) * hd:].reshape(B, nkv_l, hd))
+    q = O.apply_rope(O.rms_norm(np.concatenate(qs, 1), qg.double().numpy(), m.eps, "bf16"), pos.numpy(), cos_t,
+                     sin_t, "bf16")
+    k = O.apply_rope(O.rms_norm(np.concatenate(ks, 1), kg.double().numpy(), m.eps, "bf16"), pos.numpy(), cos_t,
+                     sin_t, "bf16")
+    v = np.concatenate(vs, 1)
+    kc_n, vc_n = to_np(kc_d), to_np(vc_d)
+    kd, vd = kc.double().numpy(), vc.double().numpy()
+    live = [b for b in range(B) if ctx[b] > 0]
+    rows = [int(slots[b]) for b in live]
+    assert np.array_equal(vc_n[rows], v[live])                          # v: bit copy into the last row
+    assert_within_ulps(kc_n[rows], k[live], 2.0, 0.97, "stored k")       # k: two roundings, as qkv_norm_rope
+    others = np.ones(S, bool)
+    others[rows] = False
+    assert np.array_equal(kc_n[others], kd[others]) and np.array_equal(vc_n[others], vd[others])
+    got = to_np(out).reshape(B, nh, hd)
+    for b in range(B):
+        if ctx[b] == 0:
+            assert np.all(got[b] == 0.0)
+    kref = [kc_n[base[b]:base[b] + ctx[b]].astype(np.float64) for b in live]   # the cache as stored
+    vref = [vc_n[base[b]:base[b] + ctx[b]].astype(np.float64) for b in live]
+    ref = O.attention_decode(q[live], kref, vref, hd ** -0.5, "bf16")
+    err_o = np.abs(got[live] - ref)
+    assert np.all(err_o <= _attn_tol(ref, vd)), float(err_o.max())
+    assert float(np.mean(err_o)) < 2e-3
+
+
 # ----------------------------------------------------------------------------
 # lm_head and argmax
 # ----------------------------------------------------------------------------
