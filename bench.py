@@ -287,6 +287,7 @@ class Workload:
             "prefill.qkv_norm_rope_store_kv": ("hbm", 2.0 * T * (qkvw + nh * hd + 2 * nkv * hd) + 16.0 * T),
             "decode.gemm_qkv": ("hbm", gemm_b(B, qkvw, H)),
             "decode.add_rmsnorm_gemm_qkv": ("hbm", gemm_b(B, qkvw, H) + 2.0 * 3 * B * H),
+            "decode.add_rmsnorm_gemm_gate_up": ("hbm", 2.0 * (2 * I * H + B * H + B * I) + 2.0 * 3 * B * H),
             "decode.gemm_o": ("hbm", gemm_b(B, H, nh * hd)),
             "decode.gemm_gate_up_silu": ("hbm", 2.0 * (2 * I * H + B * H + B * I)),
             "decode.gemm_down": ("hbm", gemm_b(B, H, I)),
@@ -307,7 +308,7 @@ class Workload:
     def launches_per_step(self, kind):
         nl = self.m.n_layers
         fused_norm = self.fwd.norm_fusion_ok(self.B)
-        per_layer = {"add_rmsnorm": 1 if fused_norm and kind.startswith("decode.") else 2}
+        per_layer = {"add_rmsnorm": 0 if fused_norm and kind.startswith("decode.") else 2}
         base = kind.split(".", 1)[-1]
         if kind in ("lm_head", "embed_vocab"):
             return 1 + self.S
@@ -523,9 +524,9 @@ def count_launches(wl):
     from qwen3_transformer_forward_gb300 import _lib as L
     m = wl.m
     per_layer = 2 + 1 + 1 + 1 + 1 + 1 + 1   # 2 norms, qkv gemm, rope/kv, attention, o, gate_up, down
-    # decode with few tokens: the input norm runs inside the QKV GEMM; in bf16 the
+    # decode with few tokens: both norms run inside the GEMVs they feed; in bf16 the
     # QK-norm + RoPE + KV store runs inside decode attention
-    dec_layer = per_layer - 1 if wl.fwd.norm_fusion_ok(wl.B) else per_layer
+    dec_layer = per_layer - 2 if wl.fwd.norm_fusion_ok(wl.B) else per_layer
     if wl.fwd.dtype == torch.bfloat16 and m.head_dim == 128:
         dec_layer -= 1
     # split-K sums and the split-KV merge happen inside the GEMM and attention kernels

@@ -527,29 +527,35 @@ struct NormArgs {
 };
 constexpr int GV_YPAD = 8;   // y row padding (elements): 16-byte rows at distinct bank groups
 
-template <int NT, int EPI, bool WROW, int RPC, int MAXC, bool NORM = false>
+// TL: m16 row tiles per CTA (2 only with SiluAndMul: 16 outputs per CTA, half
+// the CTAs, so a norm prologue runs in one wave).
+template <int NT, int EPI, bool WROW, int RPC, int MAXC, bool NORM = false, int TL = 1>
 __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
     gemv_mma_kernel(const bf16* __restrict__ A, const bf16* __restrict__ W, bf16* __restrict__ C, int M, int N, int K,
                     int K_l, int64_t ldc, int64_t i_l, NormArgs na) {
+  static_assert(TL == 1 || EPI == tc::EPI_SILU, "two row tiles per CTA only with SiluAndMul");
   constexpr int GV_MAXC = MAXC;
-  __shared__ float red[GV_WARPS][16][NT * 8];
+  __shared__ float red[GV_WARPS][16 * TL][NT * 8];
   extern __shared__ __align__(16) uint8_t gv_dyn[];
   bf16* ys = reinterpret_cast<bf16*>(gv_dyn);   // NORM: [M][K + GV_YPAD]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  // the two weight rows of this thread (m16 tile rows g and g + 8)
-  int64_t rowA, rowB;
-  bool okA, okB;
-  if (EPI == tc::EPI_SILU) {
-    const int64_t o0 = int64_t(blockIdx.x) * 8;        // first output column
-    const int64_t r = o0 / i_l, j = o0 % i_l + g;
-    rowA = r * 2 * i_l + j;                            // gate row
-    rowB = rowA + i_l;                                 // matching up row
-    okA = okB = (o0 + g) < int64_t(N / 2) && j < i_l;
-  } else {
-    rowA = int64_t(blockIdx.x) * RPC + g;
-    rowB = rowA + 8;
-    okA = rowA < N;
-    okB = RPC == 16 && rowB < N;
+  // the two weight rows of this thread in each row tile (m16 tile rows g and g + 8)
+  int64_t rowA[TL], rowB[TL];
+  bool okA[TL], okB[TL];
+#pragma unroll
+  for (int tl = 0; tl < TL; ++tl) {
+    if (EPI == tc::EPI_SILU) {
+      const int64_t o0 = (int64_t(blockIdx.x) * TL + tl) * 8;   // first output column of the tile
+      const int64_t r = o0 / i_l, j = o0 % i_l + g;
+      rowA[tl] = r * 2 * i_l + j;                                // gate row
+      rowB[tl] = rowA[tl] + i_l;                                 // matching up row
+      okA[tl] = okB[tl] = (o0 + g) < int64_t(N / 2) && j < i_l;
+    } else {
+      rowA[tl] = int64_t(blockIdx.x) * RPC + g;
+      rowB[tl] = rowA[tl] + 8;
+      okA[tl] = rowA[tl] < N;
+      okB[tl] = RPC == 16 && rowB[tl] < N;
+    }
   }
   const int kw = ((K + GV_WARPS * 32 - 1) / (GV_WARPS * 32)) * 32;   // k values per warp, whole chunks
   const int k0 = warp * kw;
@@ -561,18 +567,22 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
     }
     return W + row * int64_t(K) + k;
   };
-  float acc[NT][4];
+  float acc[TL][NT][4];
 #pragma unroll
-  for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
-  uint4 wa[GV_MAXC], wb[GV_MAXC];
+  for (int tl = 0; tl < TL; ++tl)
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[tl][n][0] = acc[tl][n][1] = acc[tl][n][2] = acc[tl][n][3] = 0.0f;
+  uint4 wa[TL][GV_MAXC], wb[TL][GV_MAXC];
   auto load_w = [&](int kb) {
 #pragma unroll
-    for (int c = 0; c < GV_MAXC; ++c) {
-      const int k = kb + 32 * c + 8 * t;
-      const bool in = kb + 32 * c < k1;
-      wa[c] = (in && okA) ? ldg_stream(wptr(rowA, k)) : make_uint4(0, 0, 0, 0);
-      wb[c] = (RPC == 16 && in && okB) ? ldg_stream(wptr(rowB, k)) : make_uint4(0, 0, 0, 0);
-    }
+    for (int tl = 0; tl < TL; ++tl)
+#pragma unroll
+      for (int c = 0; c < GV_MAXC; ++c) {
+        const int k = kb + 32 * c + 8 * t;
+        const bool in = kb + 32 * c < k1;
+        wa[tl][c] = (in && okA[tl]) ? ldg_stream(wptr(rowA[tl], k)) : make_uint4(0, 0, 0, 0);
+        wb[tl][c] = (RPC == 16 && in && okB[tl]) ? ldg_stream(wptr(rowB[tl], k)) : make_uint4(0, 0, 0, 0);
+      }
   };
   // the first weights are constants: load them before the dependency wait
   if (k0 < k1) load_w(k0);
@@ -639,30 +649,35 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
         if (tok < M)
           x = NORM ? *reinterpret_cast<const uint4*>(ys + tok * ys_stride + k)
                    : __ldg(reinterpret_cast<const uint4*>(A + int64_t(tok) * K + k));
-        mma_16816(acc[n], wa[c].x, wb[c].x, wa[c].y, wb[c].y, x.x, x.y);
-        mma_16816(acc[n], wa[c].z, wb[c].z, wa[c].w, wb[c].w, x.z, x.w);
+#pragma unroll
+        for (int tl = 0; tl < TL; ++tl) {
+          mma_16816(acc[tl][n], wa[tl][c].x, wb[tl][c].x, wa[tl][c].y, wb[tl][c].y, x.x, x.y);
+          mma_16816(acc[tl][n], wa[tl][c].z, wb[tl][c].z, wa[tl][c].w, wb[tl][c].w, x.z, x.w);
+        }
       }
     }
   }
-  // partial tiles to shared memory: rows g, g+8; tokens 2t, 2t+1 of each n-tile
+  // partial tiles to shared memory: rows 16 tl + g, 16 tl + g + 8; tokens 2t, 2t+1 of each n-tile
 #pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    red[warp][g][n * 8 + 2 * t] = acc[n][0];
-    red[warp][g][n * 8 + 2 * t + 1] = acc[n][1];
-    red[warp][g + 8][n * 8 + 2 * t] = acc[n][2];
-    red[warp][g + 8][n * 8 + 2 * t + 1] = acc[n][3];
-  }
+  for (int tl = 0; tl < TL; ++tl)
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      red[warp][16 * tl + g][n * 8 + 2 * t] = acc[tl][n][0];
+      red[warp][16 * tl + g][n * 8 + 2 * t + 1] = acc[tl][n][1];
+      red[warp][16 * tl + g + 8][n * 8 + 2 * t] = acc[tl][n][2];
+      red[warp][16 * tl + g + 8][n * 8 + 2 * t + 1] = acc[tl][n][3];
+    }
   __syncthreads();
   if (EPI == tc::EPI_SILU) {
-    for (int e = threadIdx.x; e < 8 * M; e += GV_WARPS * 32) {
-      const int r = e & 7, tok = e >> 3;
+    for (int e = threadIdx.x; e < 8 * TL * M; e += GV_WARPS * 32) {
+      const int r = e & 7, tl = (e >> 3) % TL, tok = (e >> 3) / TL;
       float gs = 0.0f, us = 0.0f;
 #pragma unroll
       for (int w = 0; w < GV_WARPS; ++w) {
-        gs += red[w][r][tok];
-        us += red[w][r + 8][tok];
+        gs += red[w][16 * tl + r][tok];
+        us += red[w][16 * tl + r + 8][tok];
       }
-      const int64_t o = int64_t(blockIdx.x) * 8 + r;
+      const int64_t o = (int64_t(blockIdx.x) * TL + tl) * 8 + r;
       if (o < N / 2) C[int64_t(tok) * ldc + o] = __float2bfloat16_rn(tc::silu_mul_bf16(gs, us));
     }
   } else {
@@ -670,7 +685,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
       const int r = e % RPC, tok = e / RPC;
       float sum = 0.0f;
 #pragma unroll
-      for (int w = 0; w < GV_WARPS; ++w) sum += red[w][r][tok];
+      for (int w = 0; w < GV_WARPS; ++w) sum += red[w][r][tok];   // (TL == 1 here)
       const int64_t row = int64_t(blockIdx.x) * RPC + r;
       if (row < N) C[int64_t(tok) * ldc + row] = __float2bfloat16_rn(sum);
     }
@@ -972,20 +987,49 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
 
 // y = RMSNorm(x + res_in) * gamma (in every CTA's shared memory), C = y W^T,
 // for at most 16 tokens: the weight-streaming GEMV with a norm prologue.
+// SMs of the current device (152 when it cannot be queried)
+static int gv_device_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 152;
+  }
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 152;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 int norm_gemm_bf16(const bf16* x, const NormArgs& na, const bf16* W, bf16* C, int M, int N, int K, int tp, int epi,
                    cudaStream_t st) {
   const int nt = M <= 8 ? 1 : 2;
   const bool small_k = K <= GV_WARPS * 32 * 4;
   const bool half = epi != QW_EPI_SILU_MUL && N <= 2048;
-  const unsigned blocks = unsigned(epi == QW_EPI_SILU_MUL ? (N / 2 + 7) / 8 : half ? (N + 7) / 8 : (N + 15) / 16);
+  unsigned blocks = unsigned(epi == QW_EPI_SILU_MUL ? (N / 2 + 7) / 8 : half ? (N + 7) / 8 : (N + 15) / 16);
+  // SiluAndMul with more 8-output CTAs than fit at once (two per SM): 16 outputs
+  // per CTA, so the norm prologue is not repeated by a second wave
+  const bool two_tiles = epi == QW_EPI_SILU_MUL && small_k && blocks > unsigned(2 * gv_device_sms());
+  if (two_tiles) blocks = (blocks + 1) / 2;
   const int64_t ldc = epi == QW_EPI_SILU_MUL ? N / 2 : N;
   const int64_t i_l = epi == QW_EPI_SILU_MUL ? N / 2 / tp : 0;
   const size_t smem = size_t(M) * (K + GV_YPAD) * 2;
   cudaError_t e = cudaSuccess;
-#define QW_NG_ONE(NTV, EPIV, RPCV, MC)                                                                            \
+#define QW_NG_ONE(NTV, EPIV, RPCV, MC, TLV)                                                                      \
   {                                                                                                              \
-    auto kern = gemv_mma_kernel<NTV, EPIV, false, RPCV, MC, true>;                                               \
-    static size_t allowed = 48 * 1024;                                                                           \
+    auto kern = gemv_mma_kernel<NTV, EPIV, false, RPCV, MC, true, TLV>;                                          \
+    static size_t allowed = 0;   /* dynamic bytes this kernel may take; static ones count against 48 KB too */  \
+    if (allowed == 0) {                                                                                          \
+      cudaFuncAttributes fa;                                                                                     \
+      e = cudaFuncGetAttributes(&fa, kern);                                                                      \
+      if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));   \
+      allowed = 48 * 1024 - fa.sharedSizeBytes;                                                                  \
+    }                                                                                                            \
     if (smem > allowed) {                                                                                        \
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));                    \
       if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));    \
@@ -995,13 +1039,15 @@ int norm_gemm_bf16(const bf16* x, const NormArgs& na, const bf16* W, bf16* C, in
   }
 #define QW_NG(NTV)                                                                                               \
   if (epi == QW_EPI_SILU_MUL) {                                                                                  \
-    if (small_k) QW_NG_ONE(NTV, tc::EPI_SILU, 16, 4) else QW_NG_ONE(NTV, tc::EPI_SILU, 16, 12)                    \
+    if (two_tiles) QW_NG_ONE(NTV, tc::EPI_SILU, 16, 4, 2)                                                        \
+    else if (small_k) QW_NG_ONE(NTV, tc::EPI_SILU, 16, 4, 1)                                                     \
+    else QW_NG_ONE(NTV, tc::EPI_SILU, 16, 12, 1)                                                                 \
   } else if (half) {                                                                                             \
-    QW_NG_ONE(NTV, tc::EPI_NONE, 8, 12)                                                                          \
+    QW_NG_ONE(NTV, tc::EPI_NONE, 8, 12, 1)                                                                       \
   } else if (small_k) {                                                                                          \
-    QW_NG_ONE(NTV, tc::EPI_NONE, 16, 4)                                                                          \
+    QW_NG_ONE(NTV, tc::EPI_NONE, 16, 4, 1)                                                                       \
   } else {                                                                                                       \
-    QW_NG_ONE(NTV, tc::EPI_NONE, 16, 12)                                                                         \
+    QW_NG_ONE(NTV, tc::EPI_NONE, 16, 12, 1)                                                                      \
   }
   if (nt == 1) { QW_NG(1) } else { QW_NG(2) }
 #undef QW_NG
@@ -1133,7 +1179,10 @@ extern "C" int qw_add_rmsnorm_gemm(const void* x, const void* residual_in, void*
     return set_error(QW_ERR_INVALID_ARG, "qw_add_rmsnorm_gemm: epilogue %d", epilogue);
   if (K % 32 || N % 16 || N % tp || (epilogue == QW_EPI_SILU_MUL && ((N % (2 * tp)) || (N / 2 / tp) % 8)))
     return set_error(QW_ERR_SHAPE, "qw_add_rmsnorm_gemm: K %% 32, N %% 16 and the gate_up split rules");
-  if (K > 16384) return set_error(QW_ERR_SHAPE, "qw_add_rmsnorm_gemm: K too large");
+  // the normed rows of all tokens sit in shared memory beside the <= 16 KB reduction tile
+  if (size_t(M) * (K + GV_YPAD) * 2 > size_t(211) * 1024)
+    return set_error(QW_ERR_SHAPE, "qw_add_rmsnorm_gemm: %lld tokens x K %lld exceed shared memory",
+                     (long long)M, (long long)K);
   if (M == 0) return QW_OK;
   if (!x || !gamma || !W || !C) return set_error(QW_ERR_INVALID_ARG, "qw_add_rmsnorm_gemm: null pointer");
   if (!al16(x) || !al16(W) || !al16(C) || !al16(gamma) || (residual_in && !al16(residual_in)) ||

@@ -261,16 +261,17 @@ class Qwen3Forward:
         with self._around(f"{ph}.gemm_o", l):
             L.gemm(attn, p.o, h, m.hidden, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, self.workspace, stream)
         act = self.act[:T]
-        # (gate_up keeps its own norm kernel: fused, its 3 * I / 8 CTAs need a
-        # second wave that repeats the norm prologue, which costs more than it saves)
-        with self._around(f"{ph}.add_rmsnorm", l):
-            if fused:
-                L.add_rmsnorm(h, self._res(2 * l, T), self._res(2 * l + 1, T), p.post_ln, m.eps, y, stream)
-            else:
+        if fused:
+            # residual update 2l + 1 as the prologue of gate_up + SiluAndMul
+            with self._around(f"{ph}.add_rmsnorm_gemm_gate_up", l):
+                L.add_rmsnorm_gemm(h, self._res(2 * l, T), self._res(2 * l + 1, T), p.post_ln, m.eps, p.gate_up, act,
+                                   2 * m.intermediate, tp, L.QW_EPI_SILU_MUL, stream)
+        else:
+            with self._around(f"{ph}.add_rmsnorm", l):
                 L.add_rmsnorm(h, res, res, p.post_ln, m.eps, y, stream)
-        with self._around(f"{ph}.gemm_gate_up_silu", l):
-            L.gemm(y, p.gate_up, act, 2 * m.intermediate, tp, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL,
-                   self.workspace, stream)
+            with self._around(f"{ph}.gemm_gate_up_silu", l):
+                L.gemm(y, p.gate_up, act, 2 * m.intermediate, tp, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL,
+                       self.workspace, stream)
         with self._around(f"{ph}.gemm_down", l):
             L.gemm(act, p.down, h, m.hidden, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, self.workspace, stream)
 

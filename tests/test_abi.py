@@ -105,6 +105,9 @@ def test_argument_errors_are_reported_before_launch(lib):
                                    None) == L.QW_ERR_SHAPE
     assert lib.qw_add_rmsnorm_gemm(fake, fake, fake, fake, 1e-6, fake, fake, 4, 64, 64, 1, 0, L.QW_BF16,
                                    None) == L.QW_ERR_INVALID_ARG
+    # 16 tokens of K = 8192 normed rows do not fit in shared memory
+    assert lib.qw_add_rmsnorm_gemm(fake, None, None, fake, 1e-6, fake, fake, 16, 64, 8192, 1, 0, L.QW_BF16,
+                                   None) == L.QW_ERR_SHAPE
     # lm_head: V not divisible by tp
     assert lib.qw_lm_head(fake, 4, None, 4, fake, 10, 64, 4, fake, None, None, 0, L.QW_BF16,
                           None) == L.QW_ERR_SHAPE

@@ -253,7 +253,9 @@ def test_gemm_bf16(L, M, N, K, tp, mode, epi):
 
 @pytest.mark.parametrize("M,N,K,tp,epi,with_res", [(8, 4096, 1024, 2, 0, True), (8, 6144, 1024, 2, 1, True),
                                                     (1, 4096, 1024, 1, 0, False), (16, 6144, 1024, 2, 1, True),
-                                                    (13, 1024, 2048, 2, 0, True), (5, 512, 96, 2, 1, False)])
+                                                    (13, 1024, 2048, 2, 0, True), (5, 512, 96, 2, 1, False),
+                                                    # 311 groups of 8 outputs: two per CTA, the last CTA half empty
+                                                    (3, 4976, 256, 1, 1, True)])
 def test_add_rmsnorm_gemm(L, M, N, K, tp, epi, with_res):
     """Fused add + RMSNorm + column Linear (decode QKV / gate_up) against the
     oracle's add_rms_norm followed by the oracle Linear."""
