@@ -529,7 +529,10 @@ constexpr int GV_YPAD = 8;   // y row padding (elements): 16-byte rows at distin
 
 // TL: m16 row tiles per CTA (2 only with SiluAndMul: 16 outputs per CTA, half
 // the CTAs, so a norm prologue runs in one wave).
-template <int NT, int EPI, bool WROW, int RPC, int MAXC, bool NORM = false, int TL = 1>
+// STAGE: A [M][K] is copied into shared memory first by asynchronous 16-byte
+// copies, all in flight at once (otherwise each k chunk's activations are one
+// more L2 round trip before its MMAs).
+template <int NT, int EPI, bool WROW, int RPC, int MAXC, bool NORM = false, int TL = 1, bool STAGE = false>
 __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
     gemv_mma_kernel(const bf16* __restrict__ A, const bf16* __restrict__ W, bf16* __restrict__ C, int M, int N, int K,
                     int K_l, int64_t ldc, int64_t i_l, NormArgs na) {
@@ -537,7 +540,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
   constexpr int GV_MAXC = MAXC;
   __shared__ float red[GV_WARPS][16 * TL][NT * 8];
   extern __shared__ __align__(16) uint8_t gv_dyn[];
-  bf16* ys = reinterpret_cast<bf16*>(gv_dyn);   // NORM: [M][K + GV_YPAD]
+  bf16* ys = reinterpret_cast<bf16*>(gv_dyn);   // NORM, STAGE: [M][K + GV_YPAD]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   // the two weight rows of this thread in each row tile (m16 tile rows g and g + 8)
   int64_t rowA[TL], rowB[TL];
@@ -636,6 +639,16 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
     }
     __syncthreads();
   }
+  if (STAGE) {
+    const int nvec = K / 8;
+    const int total = M * nvec;
+    for (int v = threadIdx.x; v < total; v += GV_WARPS * 32)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(ys + (v / nvec) * ys_stride + (v % nvec) * 8)),
+                   "l"(A + int64_t(v / nvec) * K + (v % nvec) * 8)
+                   : "memory");
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+  }
   for (int kb = k0; kb < k1; kb += GV_MAXC * 32) {
     if (kb != k0) load_w(kb);
 #pragma unroll
@@ -647,8 +660,8 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
         const int tok = n * 8 + g;
         uint4 x = make_uint4(0, 0, 0, 0);
         if (tok < M)
-          x = NORM ? *reinterpret_cast<const uint4*>(ys + tok * ys_stride + k)
-                   : __ldg(reinterpret_cast<const uint4*>(A + int64_t(tok) * K + k));
+          x = (NORM || STAGE) ? *reinterpret_cast<const uint4*>(ys + tok * ys_stride + k)
+                              : __ldg(reinterpret_cast<const uint4*>(A + int64_t(tok) * K + k));
 #pragma unroll
         for (int tl = 0; tl < TL; ++tl) {
           mma_16816(acc[tl][n], wa[tl][c].x, wb[tl][c].x, wa[tl][c].y, wb[tl][c].y, x.x, x.y);
@@ -893,6 +906,24 @@ int launch_tc(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArgs& ar
   return check_launch("gemm_tc_kernel");
 }
 
+// Lets kernel `kern` take `smem` bytes of dynamic shared memory: the default
+// allows 48 KB minus its static shared memory; beyond that it opts in (once
+// per size growth).  `allowed` is the caller's per-kernel record.
+static int gv_allow_smem(const void* kern, size_t smem, size_t& allowed) {
+  if (allowed == 0) {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
+    allowed = 48 * 1024 - fa.sharedSizeBytes;
+  }
+  if (smem > allowed) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    allowed = smem;
+  }
+  return QW_OK;
+}
+
 int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64_t K, int tp, int mode, int epi,
               cudaStream_t st) {
   const Plan p = plan_bf16(M, N, K, tp, mode, epi);
@@ -939,9 +970,22 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
     const unsigned blocks =
         unsigned(epi == QW_EPI_SILU_MUL ? (N / 2 + 7) / 8 : half ? (N + 7) / 8 : (N + 15) / 16);
     cudaError_t e;
+    // up to 8 tokens: activations staged in shared memory (measured on the
+    // 28-layer decode step: 139.3 -> 136.3 ms for 128 steps)
+    const size_t stage_smem = size_t(M) * (K + GV_YPAD) * 2;
+    const bool stage = M <= 8 && stage_smem <= size_t(200) * 1024;
 #define QW_GV_ONE(NTV, EPIV, WR, RPCV, MC)                                                                     \
-  e = launch_pdl(gemv_mma_kernel<NTV, EPIV, WR, RPCV, MC>, dim3(blocks), dim3(GV_WARPS * 32), 0, st, A, W, C,   \
-                 int(M), int(N), int(K), int(Kl), a.ldc, a.i_l, NormArgs{nullptr, nullptr, nullptr, 0.0f});
+  if (NTV == 1 && stage) {                                                                                     \
+    auto kern = gemv_mma_kernel<1, EPIV, WR, RPCV, MC, false, 1, true>;                                        \
+    static size_t allowed = 0;                                                                                 \
+    const int rc_ = gv_allow_smem(reinterpret_cast<const void*>(kern), stage_smem, allowed);                  \
+    if (rc_) return rc_;                                                                                       \
+    e = launch_pdl(kern, dim3(blocks), dim3(GV_WARPS * 32), stage_smem, st, A, W, C, int(M), int(N), int(K),   \
+                   int(Kl), a.ldc, a.i_l, NormArgs{nullptr, nullptr, nullptr, 0.0f});                          \
+  } else {                                                                                                     \
+    e = launch_pdl(gemv_mma_kernel<NTV, EPIV, WR, RPCV, MC>, dim3(blocks), dim3(GV_WARPS * 32), 0, st, A, W, C, \
+                   int(M), int(N), int(K), int(Kl), a.ldc, a.i_l, NormArgs{nullptr, nullptr, nullptr, 0.0f}); \
+  }
 #define QW_GV(NTV)                                                                                             \
   if (epi == QW_EPI_SILU_MUL) {                                                                                \
     if (small_k) { QW_GV_ONE(NTV, tc::EPI_SILU, false, 16, 4) } else { QW_GV_ONE(NTV, tc::EPI_SILU, false, 16, 12) } \
@@ -1023,18 +1067,9 @@ int norm_gemm_bf16(const bf16* x, const NormArgs& na, const bf16* W, bf16* C, in
 #define QW_NG_ONE(NTV, EPIV, RPCV, MC, TLV)                                                                      \
   {                                                                                                              \
     auto kern = gemv_mma_kernel<NTV, EPIV, false, RPCV, MC, true, TLV>;                                          \
-    static size_t allowed = 0;   /* dynamic bytes this kernel may take; static ones count against 48 KB too */  \
-    if (allowed == 0) {                                                                                          \
-      cudaFuncAttributes fa;                                                                                     \
-      e = cudaFuncGetAttributes(&fa, kern);                                                                      \
-      if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));   \
-      allowed = 48 * 1024 - fa.sharedSizeBytes;                                                                  \
-    }                                                                                                            \
-    if (smem > allowed) {                                                                                        \
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));                    \
-      if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));    \
-      allowed = smem;                                                                                            \
-    }                                                                                                            \
+    static size_t allowed = 0;                                                                                   \
+    const int rc_ = gv_allow_smem(reinterpret_cast<const void*>(kern), smem, allowed);                          \
+    if (rc_) return rc_;                                                                                         \
     e = launch_pdl(kern, dim3(blocks), dim3(GV_WARPS * 32), smem, st, x, W, C, M, N, K, K, ldc, i_l, na);        \
   }
 #define QW_NG(NTV)                                                                                               \
