@@ -58,7 +58,7 @@ def parse_args(argv=None):
     ap.add_argument("--profile-window", action="store_true",
                     help="after the timed region, run one more step between cudaProfilerStart/Stop "
                          "(for ncu --profile-from-start off)")
-    ap.add_argument("--profile-kernel", choices=["decode.attention"], default=None,
+    ap.add_argument("--profile-kernel", choices=["decode.attention", "prefill.gemm_gate_up_silu"], default=None,
                     help="launch only this kernel, --profile-reps times, on inputs of the workload's shape "
                          "(random values, mean decode context) and exit: a small case for ncu section captures")
     ap.add_argument("--profile-reps", type=int, default=3)
@@ -688,6 +688,15 @@ def profile_kernel(args):
         for _ in range(args.profile_reps):
             L.attention_decode_rope(qkv, nh, nkv, hd, m.tp, pos, cs, gamma, gamma, m.eps, slots, kc, vc, None, ctx,
                                     base, cap, hd ** -0.5, out, ws)
+    if args.profile_kernel == "prefill.gemm_gate_up_silu":   # merged gate_up + SiluAndMul over the prompt tokens
+        T, H, I = sum(seqs), m.hidden, m.intermediate
+        x = rnd(T, H)
+        w = (rnd(2 * I, H) * 0.02).to(torch.bfloat16)
+        act = torch.empty(T, I, dtype=torch.bfloat16, device="cuda")
+        ws = torch.zeros(max(L.gemm_workspace_size(T, 2 * I, H, m.tp, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL,
+                                                   torch.bfloat16), 16), dtype=torch.uint8, device="cuda")
+        for _ in range(args.profile_reps):
+            L.gemm(x, w, act, 2 * I, m.tp, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL, ws)
     torch.cuda.synchronize()
     L.device_error()
 

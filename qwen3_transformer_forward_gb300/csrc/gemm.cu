@@ -157,10 +157,14 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
 }
 
 __device__ __forceinline__ float silu_mul_bf16(float g, float u) {
-  // gate_up is a model-dtype tensor before SiluAndMul: round both halves first
+  // gate_up is a model-dtype tensor before SiluAndMul: round both halves first.
+  // The fast exp and divide intrinsics (a few fp32 ulp) sit far below the bf16
+  // rounding of the result; the accurate ones kept the prefill gate_up
+  // epilogue on the transcendental pipe.  (For g -> -inf: 1 + e -> inf and
+  // the quotient -> 0, as SiLU.)
   g = round_t<bf16>(g);
   u = round_t<bf16>(u);
-  return g / (1.0f + expf(-g)) * u;
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 template <int BN>
