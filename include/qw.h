@@ -202,6 +202,36 @@ int qw_attention_decode(const void* q, const void* k_cache, const void* v_cache,
 size_t qw_attention_decode_workspace_size(int B, int max_context, int n_heads, int head_dim);
 
 /*
+ * Paged KV cache ([SK] §7.2; nano-vllm's block_table with block_size 256):
+ * key position p of sequence s is cache row
+ *   block_table[s * max_blocks + p / block_size] * block_size + p % block_size.
+ * The caller owns block_table (int32 [n_seqs, max_blocks], device) and keeps
+ * every entry a sequence uses a valid block: rows outside [0, num_slots) read
+ * as zeros.  Both entry points are bf16 with head_dim 128.
+ *
+ * qw_attention_decode_paged: qw_attention_decode with the block table in place
+ *   of seq_base.  block_size a multiple of 64; max_context <= max_blocks *
+ *   block_size.  flags: 0 or QW_DECODE_HISTORY_READY (the block table then
+ *   counts among the inputs complete before the previous kernel started).
+ * qw_attention_prefill_paged: causal prefill attention with every key read
+ *   from the cache through the block table, the prefix-cache prefill: query i
+ *   of sequence s (Lq_s = cu_seqlens_q[s+1] - cu_seqlens_q[s] new tokens) sits
+ *   at key position Lk_s - Lq_s + i, Lk_s = cu_seqlens_k[s+1] - cu_seqlens_k[s]
+ *   keys cached (new tokens' k/v stored first).  block_size a multiple of 128.
+ * Errors: QW_ERR_DTYPE, QW_ERR_SHAPE (head_dim, group, block_size,
+ * max_context), QW_ERR_INVALID_ARG (null or misaligned pointers, flags),
+ * QW_ERR_WORKSPACE (decode).
+ */
+int qw_attention_decode_paged(const void* q, const void* k_cache, const void* v_cache, int64_t num_slots,
+                              const int32_t* context_lens, const int32_t* block_table, int max_blocks, int block_size,
+                              int B, int max_context, int n_heads, int n_kv_heads, int head_dim, float scale,
+                              void* out, void* workspace, size_t workspace_bytes, int dtype, int flags, void* stream);
+int qw_attention_prefill_paged(const void* q, const void* k_cache, const void* v_cache, int64_t num_slots,
+                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* block_table,
+                               int max_blocks, int block_size, int n_seqs, int max_seqlen_q, int n_heads,
+                               int n_kv_heads, int head_dim, float scale, void* out, int dtype, void* stream);
+
+/*
  * Decode step's QK-RMSNorm + RoPE + KV-cache store ([SK] §3, §7.1, §8) and
  * decode attention ([SK] §7.2) in one launch: qw_qkv_norm_rope_store_kv on
  * one token per sequence followed by qw_attention_decode, without the q_out

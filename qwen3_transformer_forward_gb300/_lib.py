@@ -38,6 +38,10 @@ SIGNATURES = {
     "qw_attention_decode": (C.c_int, [_p, _p, _p, _i64, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _p, _sz,
                                       _i32, _i32, _p]),
     "qw_attention_decode_workspace_size": (C.c_size_t, [_i32, _i32, _i32, _i32]),
+    "qw_attention_decode_paged": (C.c_int, [_p, _p, _p, _i64, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32,
+                                            _p, _p, _sz, _i32, _i32, _p]),
+    "qw_attention_prefill_paged": (C.c_int, [_p, _p, _p, _i64, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                             _f32, _p, _i32, _p]),
     "qw_attention_decode_rope": (C.c_int, [_p, _i32, _i32, _i32, _i32, _p, _p, _i64, _p, _p, _f32, _p, _p, _p, _i64,
                                            _p, _p, _p, _i32, _i32, _f32, _p, _p, _sz, _i32, _i32, _p]),
     "qw_attention_decode_static": (C.c_int, [_p, _p, _p, _i64, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _i32,
@@ -211,6 +215,30 @@ def attention_decode_rope(qkv, n_heads, n_kv_heads, head_dim, tp, positions, cos
         k_cache.shape[0], _dev_ptr(err_count, "err_count"), _dev_ptr(context_lens, "context_lens"),
         _dev_ptr(seq_base, "seq_base"), B, max_context, scale, _dev_ptr(out, "out"), _dev_ptr(workspace, "workspace"),
         ws_bytes, dtype_code(qkv.dtype), QW_DECODE_HISTORY_READY if history_ready else 0, _stream(stream)))
+
+
+def attention_decode_paged(q, k_cache, v_cache, context_lens, block_table, block_size, max_context, n_heads,
+                           n_kv_heads, head_dim, scale, out, workspace, stream=None, history_ready=False):
+    """Decode attention over a paged cache: block_table int32 [B, max_blocks]."""
+    B = q.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().qw_attention_decode_paged(
+        _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), k_cache.shape[0],
+        _dev_ptr(context_lens, "context_lens"), _dev_ptr(block_table, "block_table"), block_table.shape[1],
+        block_size, B, max_context, n_heads, n_kv_heads, head_dim, scale, _dev_ptr(out, "out"),
+        _dev_ptr(workspace, "workspace"), ws_bytes, dtype_code(q.dtype), QW_DECODE_HISTORY_READY if history_ready else 0,
+        _stream(stream)))
+
+
+def attention_prefill_paged(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, block_size, max_seqlen_q,
+                            n_heads, n_kv_heads, head_dim, scale, out, stream=None):
+    """Causal prefill attention with every key read from a paged cache (prefix-cache prefill)."""
+    n_seqs = cu_seqlens_q.shape[0] - 1
+    _check(load().qw_attention_prefill_paged(
+        _dev_ptr(q, "q"), _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), k_cache.shape[0],
+        _dev_ptr(cu_seqlens_q, "cu_seqlens_q"), _dev_ptr(cu_seqlens_k, "cu_seqlens_k"),
+        _dev_ptr(block_table, "block_table"), block_table.shape[1], block_size, n_seqs, max_seqlen_q, n_heads,
+        n_kv_heads, head_dim, scale, _dev_ptr(out, "out"), dtype_code(q.dtype), _stream(stream)))
 
 
 def attention_decode_static(q, k_cache, v_cache, context_lens, seq_base, max_context, n_heads, n_kv_heads,

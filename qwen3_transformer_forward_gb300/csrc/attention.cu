@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const bf16* __restrict__ q,
     const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ seq_base, int nh, int nkv, int n_pairs,
     int T, int per, float scale_log2, int history_ready, float* __restrict__ ws_o, float* __restrict__ ws_ml,
-    unsigned int* __restrict__ counters, bf16* __restrict__ out, const DecodeRope rp) {
+    unsigned int* __restrict__ counters, bf16* __restrict__ out, const DecodeRope rp, const KvPages pages) {
   // history_ready: context lengths, bases and every cached row but each
   // sequence's last were complete before the previous kernel started, which
   // writes only q and those last rows.  Then the lengths are read and the
@@ -484,7 +484,8 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_last + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int p_first = int(lo / T), p_last = int((hi - 1) / T);
-  const int L_first = ctx_lens[p_first / nkv], base_first = seq_base[p_first / nkv];   // loaded together
+  const int L_first = ctx_lens[p_first / nkv];   // loaded together with the base below
+  const int base_first = pages.table == nullptr ? seq_base[p_first / nkv] : 0;
   // this CTA's tiles of pair p: the static range clipped to the sequence's own length (Tb tiles)
   auto seg_range = [&](int p, int& ta, int& tb, int& Tb) {
     const int ts = p == p_first ? int(lo - int64_t(p) * T) : 0;
@@ -517,7 +518,10 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
     const int s = j % DT_STAGES;
     const uint32_t dst = smem_u32(sm + s * DT_STAGE);
     const int b = pp / nkv, g = pp % nkv;
-    const int z = (b == p_first / nkv ? base_first : seq_base[b]) + pt * DT_KT;
+    const int z = pages.table != nullptr   // cache row of key pt * 64, through the block table when paged
+                      ? pages.table[int64_t(b) * pages.max_blocks + pt * DT_KT / pages.block_size] * pages.block_size +
+                            (pt * DT_KT) % pages.block_size
+                      : (b == p_first / nkv ? base_first : seq_base[b]) + pt * DT_KT;
     tcx::mbar_expect_tx(full(s), DT_STAGE);
     tcx::tma_load_3d(dst, &tmK, full(s), 0, g, z);
     tcx::tma_load_3d(dst + DT_BOX, &tmK, full(s), 64, g, z);
@@ -839,7 +843,7 @@ using namespace qw::attn;
 namespace qw {
 int launch_attention_prefill_tc(const void* q, const void* k, const void* v, int64_t kv_rows, const int32_t* cu_q,
                                 const int32_t* cu_k, const int32_t* seq_base, int n_seqs, int max_seqlen_q, int nh,
-                                int nkv, float scale, void* out, cudaStream_t st);
+                                int nkv, float scale, void* out, cudaStream_t st, const KvPages& pages);
 }  // namespace qw
 
 extern "C" int qw_attention_prefill(const void* q, const void* k, const void* v, int64_t kv_rows,
@@ -860,7 +864,7 @@ extern "C" int qw_attention_prefill(const void* q, const void* k, const void* v,
     if (kv_rows <= 0 || (reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16)
       return set_error(QW_ERR_INVALID_ARG, "qw_attention_prefill: kv_rows must be > 0 and k, v 16-byte aligned");
     return launch_attention_prefill_tc(q, k, v, kv_rows, cu_seqlens_q, cu_seqlens_k, seq_base, n_seqs, max_seqlen_q,
-                                       n_heads, n_kv_heads, scale, out, st);
+                                       n_heads, n_kv_heads, scale, out, st, KvPages{nullptr, 0, 0});
   }
   if (dtype == QW_BF16)
     return launch_attn_small<bf16>(q, k, v, cu_seqlens_q, cu_seqlens_k, seq_base, nullptr, n_seqs, max_seqlen_q,
@@ -934,7 +938,7 @@ template <int G>
 static int launch_decode_tc(const void* q, const void* kc, const void* vc, const int32_t* cl, const int32_t* sb,
                             int B, int nh, int nkv, int64_t num_slots, int max_context, float sl2, void* ws,
                             size_t ws_bytes, int history_ready, void* out, cudaStream_t st,
-                            const DecodeRope& rp = DecodeRope{}) {
+                            const DecodeRope& rp = DecodeRope{}, const KvPages& pages = KvPages{nullptr, 0, 0}) {
   int per_sm = 0;
   int rc = decode_tc_ctas_per_sm<G>(&per_sm);
   if (rc) return rc;
@@ -979,7 +983,7 @@ static int launch_decode_tc(const void* q, const void* kc, const void* vc, const
   if (rc) return rc;
   launch_pdl(attn_decode_tc_kernel<G>, dim3(unsigned(W)), DT_THREADS, dt_smem<G>(), st, mk, mv,
              static_cast<const bf16*>(q), cl, sb, nh, nkv, int(n_pairs), T, int(per), sl2, history_ready, wo, wml,
-             cnt, static_cast<bf16*>(out), rp);
+             cnt, static_cast<bf16*>(out), rp, pages);
   return check_launch("attn_decode_tc_kernel");
 }
 
@@ -1129,6 +1133,82 @@ extern "C" int qw_attention_decode_rope(const void* qkv, int n_heads, int n_kv_h
     default: return launch_decode_tc<8>(nullptr, k_cache, v_cache, context_lens, seq_base, B, n_heads, n_kv_heads,
                                         num_slots, max_context, sl2, workspace, workspace_bytes, hr, out, st, rp);
   }
+}
+
+// Paged KV cache ([SK] §7.2 with a block table): the bf16 head_dim-128 kernels,
+// rows found through the block table instead of a contiguous base.
+static int check_pages(const char* who, const int32_t* table, int max_blocks, int block_size, int tile) {
+  if (!table) return set_error(QW_ERR_INVALID_ARG, "%s: null block table", who);
+  if (max_blocks <= 0 || block_size <= 0 || block_size % tile)
+    return set_error(QW_ERR_SHAPE, "%s: block_size %d must be a positive multiple of %d", who, block_size, tile);
+  return QW_OK;
+}
+
+extern "C" int qw_attention_decode_paged(const void* q, const void* k_cache, const void* v_cache, int64_t num_slots,
+                                         const int32_t* context_lens, const int32_t* block_table, int max_blocks,
+                                         int block_size, int B, int max_context, int n_heads, int n_kv_heads,
+                                         int head_dim, float scale, void* out, void* workspace,
+                                         size_t workspace_bytes, int dtype, int flags, void* stream) {
+  if (dtype != QW_BF16) return set_error(QW_ERR_DTYPE, "qw_attention_decode_paged: bf16 only");
+  if (flags & ~QW_DECODE_HISTORY_READY)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode_paged: flags %d", flags);
+  if (B < 0 || max_context < 0 || n_heads <= 0 || n_kv_heads <= 0 || num_slots < 0)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode_paged: bad sizes");
+  const int G = n_heads / n_kv_heads;
+  if (head_dim != 128 || n_heads % n_kv_heads || (G != 1 && G != 2 && G != 4 && G != 8))
+    return set_error(QW_ERR_SHAPE, "qw_attention_decode_paged: needs head_dim 128 and group 1/2/4/8");
+  int rc = check_pages("qw_attention_decode_paged", block_table, max_blocks, block_size, DT_KT);
+  if (rc) return rc;
+  if (int64_t(max_context) > int64_t(max_blocks) * block_size)
+    return set_error(QW_ERR_SHAPE, "qw_attention_decode_paged: max_context %d > max_blocks x block_size", max_context);
+  if (B == 0) return QW_OK;
+  if (!q || !k_cache || !v_cache || !context_lens || !out)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode_paged: null pointer");
+  if (reinterpret_cast<uintptr_t>(k_cache) % 16 || reinterpret_cast<uintptr_t>(v_cache) % 16)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_decode_paged: caches must be 16-byte aligned");
+  if (size_t(B) * n_kv_heads * sizeof(unsigned int) > kCounterBytes)
+    return set_error(QW_ERR_SHAPE, "qw_attention_decode_paged: %d sequences x %d kv heads exceed the counter area", B,
+                     n_kv_heads);
+  const size_t bound = decode_tc_workspace_bound(B, n_heads);
+  if (!workspace || workspace_bytes < bound)
+    return set_error(QW_ERR_WORKSPACE, "qw_attention_decode_paged: workspace of %zu bytes needed", bound);
+  const KvPages pages{block_table, max_blocks, block_size};
+  const float sl2 = scale * kLog2e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int hr = flags & QW_DECODE_HISTORY_READY;
+  switch (G) {
+    case 1: return launch_decode_tc<1>(q, k_cache, v_cache, context_lens, nullptr, B, n_heads, n_kv_heads, num_slots,
+                                       max_context, sl2, workspace, workspace_bytes, hr, out, st, DecodeRope{}, pages);
+    case 2: return launch_decode_tc<2>(q, k_cache, v_cache, context_lens, nullptr, B, n_heads, n_kv_heads, num_slots,
+                                       max_context, sl2, workspace, workspace_bytes, hr, out, st, DecodeRope{}, pages);
+    case 4: return launch_decode_tc<4>(q, k_cache, v_cache, context_lens, nullptr, B, n_heads, n_kv_heads, num_slots,
+                                       max_context, sl2, workspace, workspace_bytes, hr, out, st, DecodeRope{}, pages);
+    default: return launch_decode_tc<8>(q, k_cache, v_cache, context_lens, nullptr, B, n_heads, n_kv_heads,
+                                        num_slots, max_context, sl2, workspace, workspace_bytes, hr, out, st,
+                                        DecodeRope{}, pages);
+  }
+}
+
+extern "C" int qw_attention_prefill_paged(const void* q, const void* k_cache, const void* v_cache, int64_t num_slots,
+                                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                          const int32_t* block_table, int max_blocks, int block_size, int n_seqs,
+                                          int max_seqlen_q, int n_heads, int n_kv_heads, int head_dim, float scale,
+                                          void* out, int dtype, void* stream) {
+  if (dtype != QW_BF16) return set_error(QW_ERR_DTYPE, "qw_attention_prefill_paged: bf16 only");
+  if (n_seqs < 0 || max_seqlen_q < 0 || n_heads <= 0 || n_kv_heads <= 0 || num_slots <= 0)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_prefill_paged: bad sizes");
+  if (head_dim != 128 || n_heads % n_kv_heads)
+    return set_error(QW_ERR_SHAPE, "qw_attention_prefill_paged: needs head_dim 128 and nh %% nkv == 0");
+  int rc = check_pages("qw_attention_prefill_paged", block_table, max_blocks, block_size, 128);
+  if (rc) return rc;
+  if (n_seqs == 0 || max_seqlen_q == 0) return QW_OK;
+  if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !out)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_prefill_paged: null pointer");
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) % 16)
+    return set_error(QW_ERR_INVALID_ARG, "qw_attention_prefill_paged: caches must be 16-byte aligned");
+  return launch_attention_prefill_tc(q, k_cache, v_cache, num_slots, cu_seqlens_q, cu_seqlens_k, nullptr, n_seqs,
+                                     max_seqlen_q, n_heads, n_kv_heads, scale, out, static_cast<cudaStream_t>(stream),
+                                     KvPages{block_table, max_blocks, block_size});
 }
 
 // ===========================================================================

@@ -89,7 +89,7 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
 __global__ void __launch_bounds__(THREADS, 1) attn_prefill_tc_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const bf16* __restrict__ q,
     const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, const int32_t* __restrict__ seq_base,
-    int nh, int nkv, int pair_heads, float scale_log2, bf16* __restrict__ out) {
+    int nh, int nkv, int pair_heads, float scale_log2, bf16* __restrict__ out, const KvPages pages) {
   pdl_wait();      // inputs of this kernel are complete and visible
   pdl_trigger();   // only now may the next kernel start its prologue
   extern __shared__ uint8_t smem_dyn[];
@@ -161,8 +161,13 @@ __global__ void __launch_bounds__(THREADS, 1) attn_prefill_tc_kernel(
     auto load = [&](uint32_t dst, const CUtensorMap* map, uint32_t b, int j) {
       if (lane == 0) {
         tcx::mbar_expect_tx(b, TILE);
-        tcx::tma_load_3d(dst, map, b, 0, g, int(kbase) + j * BN);
-        tcx::tma_load_3d(dst + BOX, map, b, 64, g, int(kbase) + j * BN);
+        // cache row of key j * BN: contiguous from kbase, or through the block table
+        const int row = pages.table == nullptr ? int(kbase) + j * BN
+                                               : pages.table[int64_t(s) * pages.max_blocks + j * BN / pages.block_size] *
+                                                         pages.block_size +
+                                                     (j * BN) % pages.block_size;
+        tcx::tma_load_3d(dst, map, b, 0, g, row);
+        tcx::tma_load_3d(dst + BOX, map, b, 64, g, row);
       }
     };
     auto load_k = [&](int j) {
@@ -391,7 +396,7 @@ unsigned int take_prefill_timeouts() {
 // checks are done by the caller (qw_attention_prefill).
 int launch_attention_prefill_tc(const void* q, const void* k, const void* v, int64_t kv_rows, const int32_t* cu_q,
                                 const int32_t* cu_k, const int32_t* seq_base, int n_seqs, int max_seqlen_q, int nh,
-                                int nkv, float scale, void* out, cudaStream_t st) {
+                                int nkv, float scale, void* out, cudaStream_t st, const KvPages& pages) {
   using namespace pfa;
   static bool configured = false;
   if (!configured) {
@@ -415,7 +420,7 @@ int launch_attention_prefill_tc(const void* q, const void* k, const void* v, int
             unsigned(n_seqs));
   constexpr float kLog2e = 1.4426950408889634f;
   launch_pdl(attn_prefill_tc_kernel, grid, THREADS, SMEM, st, mk, mv, static_cast<const bf16*>(q), cu_q, cu_k,
-             seq_base, nh, nkv, pair, scale * kLog2e, static_cast<bf16*>(out));
+             seq_base, nh, nkv, pair, scale * kLog2e, static_cast<bf16*>(out), pages);
   return check_launch("attn_prefill_tc_kernel");
 }
 

@@ -108,6 +108,15 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // host-side error reporting shared by every entry point (defined in qw_api.cu)
 // ---------------------------------------------------------------------------
 namespace qw {
+// Paged KV cache: key position p of sequence s sits at row
+// table[s * max_blocks + p / block_size] * block_size + p % block_size.
+// table == nullptr: rows are contiguous from the sequence's base row.
+struct KvPages {
+  const int32_t* table;
+  int max_blocks;
+  int block_size;
+};
+
 int set_error(int code, const char* fmt, ...);
 int check_launch(const char* what);
 bool pdl_enabled();   // programmatic dependent launch on (default) unless QW_NO_PDL=1

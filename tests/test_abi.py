@@ -83,6 +83,19 @@ def test_argument_errors_are_reported_before_launch(lib):
     # unknown flags
     assert lib.qw_attention_decode(fake, fake, fake, 100, fake, fake, 8, 4096, 16, 8, 128, 0.1, fake, None, 0,
                                    L.QW_BF16, 2, None) == L.QW_ERR_INVALID_ARG
+    # paged decode / prefill: bf16, head_dim 128, block size a multiple of the key tile, context within the table
+    pd = lambda bs, maxb, mc, table, dt: (fake, fake, fake, 100, fake, table, maxb, bs, 8, mc, 16, 8, 128, 0.1, fake,  # noqa: E731
+                                          None, 0, dt, 0, None)
+    assert lib.qw_attention_decode_paged(*pd(256, 4, 1024, fake, L.QW_F32)) == L.QW_ERR_DTYPE
+    assert lib.qw_attention_decode_paged(*pd(100, 4, 400, fake, L.QW_BF16)) == L.QW_ERR_SHAPE
+    assert lib.qw_attention_decode_paged(*pd(256, 4, 1025, fake, L.QW_BF16)) == L.QW_ERR_SHAPE
+    assert lib.qw_attention_decode_paged(*pd(256, 4, 1024, None, L.QW_BF16)) == L.QW_ERR_INVALID_ARG
+    assert lib.qw_attention_decode_paged(*pd(256, 4, 1024, fake, L.QW_BF16)) == L.QW_ERR_WORKSPACE
+    pp = lambda bs, table, hd: (fake, fake, fake, 100, fake, fake, table, 4, bs, 2, 64, 16, 8, hd, 0.1, fake,  # noqa: E731
+                                L.QW_BF16, None)
+    assert lib.qw_attention_prefill_paged(*pp(64, fake, 128)) == L.QW_ERR_SHAPE      # block size below the 128-key tile
+    assert lib.qw_attention_prefill_paged(*pp(256, fake, 64)) == L.QW_ERR_SHAPE
+    assert lib.qw_attention_prefill_paged(*pp(256, None, 128)) == L.QW_ERR_INVALID_ARG
     # decode attention with the QK-norm + RoPE + KV store folded in: bf16, head_dim 128, tp | heads
     rope = lambda hd, nh, nkv, tp, dt, flags, ws, wsb: (fake, nh, nkv, hd, tp, fake, fake, 4096, fake, fake, 1e-6,  # noqa: E731
                                                         fake, fake, fake, 100, None, fake, fake, 8, 2048, 0.1, fake,

@@ -579,6 +579,83 @@ def test_attention_decode_rope(L, case, history_ready):
     assert float(np.mean(err_o)) < 2e-3
 
 
+def _paged_cache(name, lens, nkv, hd, block_size, spare_blocks=3, poison=False):
+    """A cache of shuffled blocks: sequence s's position p at row
+    table[s, p // block_size] * block_size + p % block_size.  Returns the
+    cache, the table and each sequence's keys/values in position order."""
+    blocks = [(L + block_size - 1) // block_size for L in lens]
+    n_blocks = sum(blocks) + spare_blocks
+    perm = torch.randperm(n_blocks, generator=torch.Generator().manual_seed(7)).to(torch.int32)
+    max_blocks = max(max(blocks), 1)
+    table = torch.full((len(lens), max_blocks), -1, dtype=torch.int32)
+    nxt = 0
+    for s_, nb in enumerate(blocks):
+        table[s_, :nb] = perm[nxt:nxt + nb]
+        nxt += nb
+    fill = float("nan") if poison else 0.0
+    kc = torch.full((n_blocks * block_size, nkv, hd), fill, dtype=torch.bfloat16)
+    vc = torch.full((n_blocks * block_size, nkv, hd), fill, dtype=torch.bfloat16)
+    ks, vs = [], []
+    for s_, L_ in enumerate(lens):
+        k = si.normal(0, f"{name}.k{s_}", (L_, nkv, hd), 1.0, "bf16")
+        v = si.normal(0, f"{name}.v{s_}", (L_, nkv, hd), 1.0, "bf16")
+        pos = torch.arange(L_)
+        rows = table[s_, pos // block_size].long() * block_size + pos % block_size
+        kc[rows] = k
+        vc[rows] = v
+        ks.append(k.double().numpy())
+        vs.append(v.double().numpy())
+    return kc, vc, table, ks, vs
+
+
+@pytest.mark.parametrize("lens,nh,nkv,block_size,history_ready",
+                         [([1, 300, 2049, 256, 257], 16, 8, 256, False), ([700, 64, 1000], 32, 8, 64, True),
+                          ([2049] * 8, 16, 8, 256, True)])
+def test_attention_decode_paged(L, lens, nh, nkv, block_size, history_ready):
+    """Decode attention through a block table over shuffled cache blocks."""
+    hd, B = 128, len(lens)
+    kc, vc, table, ks, vs = _paged_cache(f"pd{len(lens)}", lens, nkv, hd, block_size, poison=True)
+    q = si.normal(0, f"pd{len(lens)}.q", (B, nh, hd), 1.0, "bf16")
+    out = torch.full((B, nh * hd), 7.0, dtype=torch.bfloat16, device="cuda")
+    mc = table.shape[1] * block_size
+    ws = torch.zeros(L.attention_decode_workspace_size(B, mc, nh, hd), dtype=torch.uint8, device="cuda")
+    L.attention_decode_paged(dev(q), dev(kc), dev(vc), dev(torch.tensor(lens, dtype=torch.int32)), dev(table),
+                             block_size, mc, nh, nkv, hd, hd ** -0.5, out, ws, history_ready=history_ready)
+    sync_ok(L)
+    ref = O.attention_decode(q.double().numpy(), ks, vs, hd ** -0.5, "bf16")
+    got = to_np(out).reshape(B, nh, hd)
+    err = np.abs(got - ref)
+    assert np.all(err <= _attn_tol(ref, np.concatenate(vs))), float(np.nanmax(err))
+    assert float(np.mean(err)) < 2e-3
+
+
+@pytest.mark.parametrize("Lk,Lq,nh,nkv", [([600, 130, 256], [90, 130, 1], 16, 8), ([1024, 300], [1024, 44], 16, 4)])
+def test_attention_prefill_paged_prefix(L, Lk, Lq, nh, nkv):
+    """Prefix-cache prefill: Lq new queries per sequence over Lk keys (the
+    cached prefix plus the new tokens), all read through a block table."""
+    hd, bs = 128, 256
+    kc, vc, table, ks, vs = _paged_cache(f"pp{len(Lk)}", Lk, nkv, hd, bs, poison=True)
+    q = si.normal(0, f"pp{len(Lk)}.q", (sum(Lq), nh, hd), 1.0, "bf16")
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(Lq)]), dtype=torch.int32)
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(Lk)]), dtype=torch.int32)
+    out = torch.empty(sum(Lq), nh * hd, dtype=torch.bfloat16, device="cuda")
+    L.attention_prefill_paged(dev(q), dev(kc), dev(vc), dev(cu_q), dev(cu_k), dev(table), bs, max(Lq), nh, nkv, hd,
+                              hd ** -0.5, out)
+    sync_ok(L)
+    qd = q.double().numpy()
+    refs = []
+    for s_ in range(len(Lk)):
+        a, b_ = int(cu_q[s_]), int(cu_q[s_ + 1])
+        qfull = np.zeros((Lk[s_], nh, hd))
+        qfull[Lk[s_] - Lq[s_]:] = qd[a:b_]
+        o = O.attention_prefill(qfull, ks[s_], vs[s_], [0, Lk[s_]], hd ** -0.5, "bf16")
+        refs.append(o[Lk[s_] - Lq[s_]:])
+    ref = np.concatenate(refs)
+    got = to_np(out).reshape(-1, nh, hd)
+    err = np.abs(got - ref)
+    assert np.all(err <= _attn_tol(ref, np.concatenate(vs))), float(np.nanmax(err))
+
+
 # ----------------------------------------------------------------------------
 # lm_head and argmax
 # ----------------------------------------------------------------------------
