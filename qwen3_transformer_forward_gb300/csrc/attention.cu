@@ -2,13 +2,21 @@
 // path for small head_dim (prefill and decode) and decode over the KV cache.
 // (Prefill with head_dim 128 runs on tcgen05 tensor cores: attention_prefill.cu.)
 //
-// Decode (head_dim 128): split-KV.  One CTA of 128 threads owns one
-// (sequence, kv head, key chunk) and all q heads of that GQA group, so each
-// cached K/V byte is read once.  K/V tiles stream through shared memory (a
-// TMA ring for bf16, cp.async double buffer for f32); partial (m, l, o) per
-// chunk go to the caller's workspace and the last chunk of a (sequence, kv
-// head) to finish (an atomic completion counter) merges them and writes the
-// output.
+// Decode (head_dim 128): split-KV, each cached K/V byte read once, all q heads
+// of a GQA group served together.
+//   bf16: one persistent wave (attn_decode_tc_kernel).  CTAs take contiguous
+//   ranges of the (sequence, kv head, 64-key tile) sequence, stream the tiles
+//   through a TMA ring and run QK^T / PV on mma.sync.  Options: the QK-norm +
+//   RoPE + KV store folded in (qw_attention_decode_rope), a paged cache
+//   (qw_attention_decode_paged), history copies started before the
+//   programmatic wait (QW_DECODE_HISTORY_READY).
+//   f32: one CTA per (key chunk, kv head, sequence) over a cp.async double
+//   buffer.
+// In both, a (sequence, kv head) split over several CTAs leaves partial
+// (m, l, o) in the caller's workspace.  The last to finish, by an atomic
+// completion counter, merges them and writes the output.
+// The paged prefill entry (qw_attention_prefill_paged) is also here; its kernel
+// is in attention_prefill.cu.
 #include <math.h>
 
 #include <mutex>
