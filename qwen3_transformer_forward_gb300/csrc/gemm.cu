@@ -482,6 +482,282 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Persistent prefill GEMM (many tokens: MMA-A = activations, MMA-B = weights,
+// 128 x 256 tiles, no K split).  One CTA per SM walks the tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ...  The TMA ring runs on across tile boundaries,
+// and TMEM holds two 128 x 256 fp32 accumulators (all 512 columns): the
+// epilogue warps drain tile j from one buffer while the MMA thread
+// accumulates tile j + 1 into the other, so neither the pipeline fill nor
+// the epilogue of a tile leaves the tensor cores idle.
+//
+// Barriers: full[s] / empty[s] per ring stage (TMA bytes landed / MMAs done
+// reading); acc_full[b] (MMA commit: the tile in buffer b is complete) and
+// acc_empty[b] (one arrival per epilogue warp: buffer b has been read out);
+// drain (the MMA thread's last commit, so that no MMA is in flight at exit).
+// Ring iteration `it` counts (tile, k-block) pairs of this CTA: stage it % S,
+// phase parity (it / S) & 1.  The u-th use of accumulator b (tile j = 2u + b)
+// waits for acc_empty completion u - 1 (parity (u & 1) ^ 1, which a fresh
+// barrier satisfies for u = 0) and the epilogue waits for acc_full
+// completion u (parity u & 1).
+// ---------------------------------------------------------------------------
+constexpr int PBN = 256, PSTAGES = 4;
+constexpr uint32_t P_TMEM_COLS = 512;
+
+template <int EPI, bool WROW>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_persist_kernel(const __grid_constant__ CUtensorMap tmAct, const __grid_constant__ CUtensorMap tmW,
+                           TcArgs a) {
+  constexpr int BN = PBN, STAGES = PSTAGES;
+  constexpr uint32_t A_BYTES = TileCfg<BN>::A_BYTES, B_BYTES = TileCfg<BN>::B_BYTES;
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = sm;
+  uint8_t* sB = sm + STAGES * A_BYTES;
+  // full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* consumed = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  auto bar_full = [&](int s) { return smem_u32(bars + s); };
+  auto bar_empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto bar_acc_full = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
+  auto bar_acc_empty = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
+  const uint32_t bar_drain = smem_u32(bars + 2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = a.p_tiles * a.q_tiles;   // the host keeps this and `total` inside int
+  const int bx = int(blockIdx.x), gx = int(gridDim.x);
+  const int my_tiles = bx < n_tiles ? (n_tiles - bx + gx - 1) / gx : 0;
+  const int nk = a.kblocks_total;
+  const int total = my_tiles * nk;   // ring iterations of this CTA
+  auto tile_of = [&](int j, int& tile_p, int& tile_q) {
+    const int t = bx + j * gx;
+    tile_p = a.p_fastest ? t % a.p_tiles : t / a.q_tiles;
+    tile_q = a.p_fastest ? t / a.p_tiles : t % a.q_tiles;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_acc_full(b), 1);
+      mbar_init(bar_acc_empty(b), 4);   // one arrival per epilogue warp
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    *consumed = 0;
+    fence_mbar_init();
+    prefetch_map(&tmAct);
+    prefetch_map(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), P_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_trigger();   // the next kernel may start its prologue
+  int issued = 0;
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    // ring iteration it: the weight slab (w) and/or activation slab (act) of
+    // its k-block into stage s
+    auto load = [&](int it, int s, bool w, bool act) {
+      const int j = it / nk, kb = it - j * nk;
+      int tile_p, tile_q;
+      tile_of(j, tile_p, tile_q);
+      if (w) {
+        int xw, rw = 0;
+        if (WROW) {
+          rw = kb / a.kpb;
+          xw = (kb % a.kpb) * BK;
+        } else {
+          xw = kb * BK;
+        }
+        const uint32_t dW = smem_u32(sB + s * B_BYTES);
+        if (EPI == EPI_SILU) {
+          // 128 gate rows then the matching 128 up rows of shard r_s
+          const int r_s = tile_q / a.silu_tps;
+          const int64_t g0 = int64_t(r_s) * 2 * a.i_l + int64_t(tile_q % a.silu_tps) * (BN / 2);
+          tma_load_2d(dW, &tmW, bar_full(s), xw, int(g0));
+          tma_load_2d(dW + B_BYTES / 2, &tmW, bar_full(s), xw, int(g0 + a.i_l));
+        } else if (WROW) {
+          tma_load_3d(dW, &tmW, bar_full(s), xw, tile_q * BN, rw);
+        } else {
+          tma_load_2d(dW, &tmW, bar_full(s), xw, tile_q * BN);
+        }
+      }
+      if (act) {
+        const int xa = WROW ? int((kb / a.kpb) * a.k_shard) + (kb % a.kpb) * BK : kb * BK;
+        tma_load_2d(smem_u32(sA + s * A_BYTES), &tmAct, bar_full(s), xa, tile_p * BM);
+      }
+    };
+    // the first ring's weights (constants) stream in while the previous kernel finishes
+    const int npre = total < STAGES ? total : STAGES;
+    for (int i = 0; i < npre; ++i) {
+      mbar_expect_tx(bar_full(i), A_BYTES + B_BYTES);
+      load(i, i, true, false);
+    }
+    pdl_wait();
+    for (int i = 0; i < npre; ++i) load(i, i, false, true);
+    issued = npre;
+    for (int it = npre; it < total; ++it) {
+      const int s = it % STAGES;
+      const uint32_t ph = uint32_t(it / STAGES) & 1u;
+      if (!mbar_wait(bar_empty(s), ph ^ 1u, 1u)) {
+        *abort_flag = 1;
+        break;
+      }
+      if (*abort_flag) break;
+      mbar_expect_tx(bar_full(s), A_BYTES + B_BYTES);
+      load(it, s, true, true);
+      issued = it + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idesc = idesc_bf16(BM, BN);
+    int it = 0;
+    for (int j = 0; j < my_tiles; ++j) {
+      const int b = j & 1;
+      const uint32_t use = uint32_t(j >> 1) & 1u;
+      if (*abort_flag) break;
+      if (!mbar_wait(bar_acc_empty(b), use ^ 1u, 2u)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + uint32_t(b * BN);
+      bool stop = false;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = uint32_t(it / STAGES) & 1u;
+        if (!mbar_wait(bar_full(s), ph, 2u)) {
+          *abort_flag = 1;
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t da = sw128_desc(smem_u32(sA + s * A_BYTES));
+        const uint64_t db = sw128_desc(smem_u32(sB + s * B_BYTES));
+#pragma unroll
+        for (int k = 0; k < BK / UMMA_K; ++k)
+          umma_bf16(d, da + uint64_t(2 * k), db + uint64_t(2 * k), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        umma_commit(bar_empty(s));
+        *consumed = it + 1;
+      }
+      if (stop) break;
+      umma_commit(bar_acc_full(b));
+    }
+    // past this wait no MMA of this CTA is in flight (nor reads shared memory)
+    umma_commit(bar_drain);
+    mbar_wait(bar_drain, 0, 8u);
+  } else if (warp >= 2) {
+    // ---------------- epilogue ----------------
+    // waits and the abort check are warp-uniform: tcgen05.ld is .sync.aligned
+    const int quarter = warp & 3;
+    for (int j = 0; j < my_tiles; ++j) {
+      const int b = j & 1;
+      const uint32_t use = uint32_t(j >> 1) & 1u;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_acc_full(b), use, 4u));
+      if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      int tile_p, tile_q;
+      tile_of(j, tile_p, tile_q);
+      const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(b * BN);
+      const int64_t m = int64_t(tile_p) * BM + quarter * 32 + lane;
+      if (EPI == EPI_NONE) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(trow + c, r);
+          tmem_ld_wait();
+          const int64_t n0 = int64_t(tile_q) * BN + c;
+          if (m < a.M) {
+            bf16* dst = a.C + m * a.ldc + n0;
+            if (n0 + 32 <= a.N) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint4 u;
+                u.x = pack_bf16(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                u.y = pack_bf16(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                u.z = pack_bf16(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                u.w = pack_bf16(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                d4[v] = u;
+              }
+            } else {
+              for (int e = 0; e < 32; ++e)
+                if (n0 + e < a.N) dst[e] = __float2bfloat16_rn(__uint_as_float(r[e]));
+            }
+          }
+        }
+      } else {  // EPI_SILU: columns [0, 128) gate, [128, 256) up
+        const int r_s = tile_q / a.silu_tps;
+        const int64_t jl0 = int64_t(tile_q % a.silu_tps) * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32(trow + c, g);
+          tmem_ld32(trow + BN / 2 + c, u);
+          tmem_ld_wait();
+          if (m < a.M) {
+            const int64_t j0 = jl0 + c;
+            bf16* dst = a.C + m * a.ldc + int64_t(r_s) * a.i_l + j0;
+            if (j0 + 32 <= a.i_l) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                float o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  o[e] = silu_mul_bf16(__uint_as_float(g[8 * v + e]), __uint_as_float(u[8 * v + e]));
+                uint4 w;
+                w.x = pack_bf16(o[0], o[1]);
+                w.y = pack_bf16(o[2], o[3]);
+                w.z = pack_bf16(o[4], o[5]);
+                w.w = pack_bf16(o[6], o[7]);
+                d4[v] = w;
+              }
+            } else {
+              for (int e = 0; e < 32; ++e)
+                if (j0 + e < a.i_l)
+                  dst[e] = __float2bfloat16_rn(silu_mul_bf16(__uint_as_float(g[e]), __uint_as_float(u[e])));
+            }
+          }
+        }
+      }
+      // this warp's 32 accumulator lanes are read out: hand the buffer back
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tcx::mbar_arrive(bar_acc_empty(b));
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // drain copies that were issued but never consumed, so that no TMA write
+    // lands in shared memory after the CTA exits
+    for (int i = *consumed; i < issued; ++i) mbar_wait(bar_full(i % STAGES), uint32_t(i / STAGES) & 1u, 8u);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, P_TMEM_COLS);
+  }
+}
+
 }  // namespace tc
 
 // ===========================================================================
@@ -910,6 +1186,43 @@ int launch_tc(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArgs& ar
   return check_launch("gemm_tc_kernel");
 }
 
+static int gv_device_sms();
+
+// The persistent prefill GEMM (gemm_tc_persist_kernel) replaces the one-tile-
+// per-CTA kernel for many-token GEMMs while QW_TC_PERSISTENT=1 (read at each
+// call: one process can compare both).
+bool tc_persistent_enabled() {
+  const char* v = getenv("QW_TC_PERSISTENT");
+  return v && v[0] == '1';
+}
+
+template <int EPI, bool WROW>
+int launch_tc_persist(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArgs& args, cudaStream_t st) {
+  auto kern = tc::gemm_tc_persist_kernel<EPI, WROW>;
+  constexpr size_t smem = tc::smem_bytes<tc::PBN, tc::PSTAGES>();
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    configured = true;
+  }
+  // one CTA per SM (the ring takes the shared memory, the two accumulators all of TMEM)
+  const int64_t n_tiles = int64_t(args.p_tiles) * args.q_tiles;
+  const int64_t grid = n_tiles < gv_device_sms() ? n_tiles : gv_device_sms();
+  if (grid <= 0) return QW_OK;
+  if (n_tiles > INT32_MAX || ((n_tiles + grid - 1) / grid) * int64_t(args.kblocks_total) > INT32_MAX)
+    return set_error(QW_ERR_SHAPE, "gemm_tc_persist_kernel: too many tiles");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid), 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.numAttrs = 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, act, w, args);
+  if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "gemm_tc_persist_kernel launch: %s", cudaGetErrorString(e));
+  return check_launch("gemm_tc_persist_kernel");
+}
+
 // Lets kernel `kern` take `smem` bytes of dynamic shared memory: the default
 // allows 48 KB minus its static shared memory; beyond that it opts in (once
 // per size growth).  `allowed` is the caller's per-kernel record.
@@ -962,6 +1275,11 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
     }
     a.p_fastest = (M * K * 2) <= (int64_t(48) << 20) ? 1 : 0;
     a.kblocks = p.kblocks_total;
+    if (tc_persistent_enabled()) {
+      if (epi == QW_EPI_SILU_MUL) return launch_tc_persist<tc::EPI_SILU, false>(mA, mW, a, st);
+      if (wrow) return launch_tc_persist<tc::EPI_NONE, true>(mA, mW, a, st);
+      return launch_tc_persist<tc::EPI_NONE, false>(mA, mW, a, st);
+    }
     if (epi == QW_EPI_SILU_MUL) return launch_tc<256, 4, false, tc::EPI_SILU, false>(mA, mW, a, 1, st);
     if (wrow) return launch_tc<256, 4, false, tc::EPI_NONE, true>(mA, mW, a, 1, st);
     return launch_tc<256, 4, false, tc::EPI_NONE, false>(mA, mW, a, 1, st);

@@ -286,6 +286,32 @@ def test_add_rmsnorm_gemm(L, M, N, K, tp, epi, with_res):
                        atol=_gemm_abs_bound(y, W, 0, epi, tp) + y_step)
 
 
+@pytest.mark.parametrize("M,N,K,tp,mode,epi", [
+    (300, 528, 192, 1, 0, 0),       # ragged M and N, one tile per CTA
+    (200, 272, 256, 2, 1, 0),       # row split
+    (333, 800, 128, 2, 0, 1),       # SiluAndMul, I/tp = 200: a half-filled last tile per shard
+    (4096, 4096, 64, 1, 0, 0),      # one k-block per tile: the ring spans tile boundaries
+    (16384, 6144, 1024, 2, 0, 1),   # the 0.6B prefill gate_up: 20 tiles per CTA
+])
+def test_gemm_persistent_equals_one_tile_kernel(L, monkeypatch, M, N, K, tp, mode, epi):
+    """The persistent prefill GEMM (QW_TC_PERSISTENT=1) accumulates each tile
+    in the same k order as the one-tile-per-CTA kernel, which the oracle tests
+    above cover: the outputs must agree bit for bit."""
+    g = torch.Generator(device="cuda").manual_seed(7)
+    A = (torch.randn(M, K, device="cuda", generator=g) * 0.5).to(torch.bfloat16)
+    W = (torch.randn(*((tp, N, K // tp) if mode == 1 else (N, K)), device="cuda", generator=g) * 0.05).to(torch.bfloat16)
+    n_out = N // 2 if epi == 1 else N
+    out = {}
+    for flag in ("0", "1"):
+        monkeypatch.setenv("QW_TC_PERSISTENT", flag)
+        C = torch.full((M, n_out), float("nan"), dtype=torch.bfloat16, device="cuda")
+        L.gemm(A, W, C, N, tp, mode, epi)
+        sync_ok(L)
+        out[flag] = C
+    assert not torch.isnan(out["1"].float()).any()
+    assert torch.equal(out["0"], out["1"])
+
+
 @pytest.mark.parametrize("M,N,K,tp,mode,epi", [(32, 128, 64, 2, 0, 0), (32, 64, 64, 2, 1, 0),
                                                (32, 256, 64, 2, 0, 1), (5, 512, 64, 1, 0, 0)])
 def test_gemm_f32(L, M, N, K, tp, mode, epi):
