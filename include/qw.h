@@ -42,6 +42,14 @@
  *     every call leaves the counters at zero again, so one workspace serves
  *     successive calls on one stream.  Calls that may run concurrently need
  *     separate workspaces.
+ *   - One CUDA device per process: kernel attributes (shared-memory limits)
+ *     are set once, on the device current at the first call.  Replicas on
+ *     several GPUs run as one process each.
+ *   - Environment switches, read on the host: QW_NO_PDL=1 launches every
+ *     kernel without programmatic dependent launch (read once per process);
+ *     QW_TC_PERSISTENT=1 runs many-token GEMMs on the persistent tensor-core
+ *     kernel (two TMEM accumulators, one CTA per SM) instead of one CTA per
+ *     output tile (read at each call; the outputs are bit-identical).
  *   - Device-side data errors (token id outside [0, V), position outside the
  *     RoPE table, slot outside the cache) do not fail the call: the affected
  *     row is zero (embedding, q) or not written (cache), and, when the
