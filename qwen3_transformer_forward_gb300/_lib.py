@@ -53,6 +53,7 @@ SIGNATURES = {
     "qw_lm_head": (C.c_int, [_p, _i64, _p, _i64, _p, _i64, _i64, _i32, _p, _p, _p, _sz, _i32, _p]),
     "qw_lm_head_workspace_size": (C.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
     "qw_argmax": (C.c_int, [_p, _i64, _i64, _p, _i32, _p]),
+    "qw_prefetch_l2": (C.c_int, [_p, _p, _i32, _p]),
     "qw_add_rmsnorm_gemm": (C.c_int, [_p, _p, _p, _p, _f32, _p, _p, _i64, _i64, _i64, _i32, _i32, _i32, _p]),
     "qw_decode_layers": (C.c_int, [_p, _i32, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _p,
                                    _i64, _i64, _f32, _f32, _p, _p, _p, _p, _sz, _p]),
@@ -289,6 +290,14 @@ def argmax(logits, out, stream=None):
     M, V = logits.shape
     _check(load().qw_argmax(_dev_ptr(logits, "logits"), M, V, _dev_ptr(out, "out"), dtype_code(logits.dtype),
                             _stream(stream)))
+
+
+def prefetch_l2(tensors, stream=None):
+    """L2 prefetch hint for the bytes of up to 8 CUDA tensors (no output)."""
+    n = len(tensors)
+    ptrs = (C.c_void_p * max(n, 1))(*[_dev_ptr(t, "tensor") for t in tensors])
+    sizes = (C.c_size_t * max(n, 1))(*[t.numel() * t.element_size() for t in tensors])
+    _check(load().qw_prefetch_l2(C.cast(ptrs, C.c_void_p), C.cast(sizes, C.c_void_p), n, _stream(stream)))
 
 
 class DecodeLayer(C.Structure):
