@@ -90,12 +90,13 @@ def test_clock_sampler_flags_thermal_slowdown_and_empty_runs(tmp_path):
 
 def test_load_peaks_measured_and_fallback(tmp_path, monkeypatch):
     import bench
-    with open(bench.os.path.join(bench.ROOT, "MEASURED_PEAKS.json")) as f:
-        mp = json.load(f)
-    p = bench.load_peaks()
-    assert p["source"] == "measured" and p["hbm"] == mp["hbm_gbs"]
-    assert p["tensor"] == mp.get("bf16_tflops_sustained", mp["bf16_tflops"]) and p["tensor_burst"] == mp["bf16_tflops"]
+    mp = {"hbm_gbs": 6000.5, "bf16_tflops": 1900.25, "bf16_tflops_sustained": 1700.75}
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(mp))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    p = bench.load_peaks()
+    assert p["source"] == "measured" and p["hbm"] == 6000.5
+    assert p["tensor"] == 1700.75 and p["tensor_burst"] == 1900.25   # sustained for kernels inside the step
+    (tmp_path / "MEASURED_PEAKS.json").unlink()
     assert bench.load_peaks()["source"] == "fallback"
 
 
