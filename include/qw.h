@@ -322,6 +322,17 @@ size_t qw_attention_decode_static_scratch_bytes(void);
 int qw_prefetch_l2(const void* const* ptrs, const size_t* sizes, int n, void* stream);
 
 /*
+ * Self-test of the failure path: launches one thread that waits on an
+ * mbarrier that nothing completes.  The wait is bounded like every wait of
+ * the tensor-core kernels (2 s of %globaltimer); when it gives up it records
+ * code 0x100 in the tensor-core error word and the kernel returns.  The next
+ * qw_device_error on the stream then returns QW_ERR_TIMEOUT and clears the
+ * word.  No fault, no trap; the context stays usable.  It has no counterpart in
+ * the cited sources.  Errors: QW_ERR_CUDA if the launch fails.
+ */
+int qw_selftest_wait_timeout(void* stream);
+
+/*
  * Linear layer C = A W^T with the tensor-parallel layouts of [TP] §3 / [SK] §5.
  *   A dtype [M, K]
  *   QW_GEMM_COLUMN:     W dtype [N, K] (tp shards stacked along N; shard r = rows

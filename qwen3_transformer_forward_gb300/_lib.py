@@ -54,6 +54,7 @@ SIGNATURES = {
     "qw_lm_head_workspace_size": (C.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
     "qw_argmax": (C.c_int, [_p, _i64, _i64, _p, _i32, _p]),
     "qw_prefetch_l2": (C.c_int, [_p, _p, _i32, _p]),
+    "qw_selftest_wait_timeout": (C.c_int, [_p]),
     "qw_add_rmsnorm_gemm": (C.c_int, [_p, _p, _p, _p, _f32, _p, _p, _i64, _i64, _i64, _i32, _i32, _i32, _p]),
     "qw_decode_layers": (C.c_int, [_p, _i32, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _p,
                                    _i64, _i64, _f32, _f32, _p, _p, _p, _p, _sz, _p]),
@@ -298,6 +299,11 @@ def prefetch_l2(tensors, stream=None):
     ptrs = (C.c_void_p * max(n, 1))(*[_dev_ptr(t, "tensor") for t in tensors])
     sizes = (C.c_size_t * max(n, 1))(*[t.numel() * t.element_size() for t in tensors])
     _check(load().qw_prefetch_l2(C.cast(ptrs, C.c_void_p), C.cast(sizes, C.c_void_p), n, _stream(stream)))
+
+
+def selftest_wait_timeout(stream=None):
+    """Launches a bounded wait that runs out; the next device_error() raises QW_ERR_TIMEOUT."""
+    _check(load().qw_selftest_wait_timeout(_stream(stream)))
 
 
 class DecodeLayer(C.Structure):

@@ -758,6 +758,21 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// The bounded-wait path of the tensor-core kernels, run on purpose: one
+// thread waits on a fresh mbarrier for a phase that nothing completes.  After
+// the time limit the wait records kSelftestCode in the error word and the
+// kernel returns, leaving the context usable; qw_device_error reports it.
+constexpr uint32_t kSelftestCode = 0x100u;
+
+__global__ void __launch_bounds__(32) selftest_wait_kernel() {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);   // one arrival completes phase 0, and none is made
+  fence_mbar_init();
+  mbar_wait(b, 0, kSelftestCode);
+}
+
 }  // namespace tc
 
 // ===========================================================================
@@ -1551,4 +1566,9 @@ extern "C" int qw_add_rmsnorm_gemm(const void* x, const void* residual_in, void*
                     static_cast<const bf16*>(gamma), eps};
   return norm_gemm_bf16(static_cast<const bf16*>(x), na, static_cast<const bf16*>(W), static_cast<bf16*>(C), int(M),
                         int(N), int(K), tp, epilogue, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int qw_selftest_wait_timeout(void* stream) {
+  tc::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+  return check_launch("qw_selftest_wait_timeout");
 }
