@@ -84,16 +84,29 @@ def bf16_round(x) -> np.ndarray:
     bf16 keeps 8 significant bits; for |x| in [2^(e-1), 2^e) one unit in the
     last place is 2^(e-8).  Below the smallest normal (2^-126) the spacing is
     fixed at 2^-133.  Results at or beyond the overflow threshold become +-inf.
+
+    For |x| >= 2^-126 the float64 encoding already holds x exactly, so the
+    rounding is done on its bits: keep the sign, the exponent and the top 7
+    of the 52 stored fraction bits, and round the 45 dropped bits to nearest,
+    ties to the even kept bit (adding 2^44 - 1 plus the kept LSB, then
+    clearing the dropped bits; a carry out of the fraction correctly bumps
+    the exponent).  Below 2^-126 the fixed spacing is applied by scaling.
     """
     x = np.asarray(x, dtype=np.float64)
     out = np.array(x, copy=True)
-    finite = np.isfinite(x) & (x != 0)
-    xf = x[finite]
-    _, e = np.frexp(xf)                       # xf = f * 2**e, 0.5 <= |f| < 1
-    ulp = np.ldexp(1.0, np.maximum(e, -125) - 8)
-    r = np.rint(xf / ulp) * ulp                # np.rint rounds half to even
-    r = np.where(np.abs(r) > _BF16_MAX, np.copysign(np.inf, r), r)
-    out[finite] = r
+    bits = out.reshape(-1).view(np.uint64)
+    expo = (bits >> np.uint64(52)) & np.uint64(0x7FF)
+    normal = (expo >= np.uint64(1023 - 126)) & (expo < np.uint64(0x7FF))
+    kept = bits[normal]
+    lsb = (kept >> np.uint64(45)) & np.uint64(1)
+    bits[normal] = (kept + np.uint64((1 << 44) - 1) + lsb) & ~np.uint64((1 << 45) - 1)
+    flat = x.reshape(-1)
+    small = (expo < np.uint64(1023 - 126)) & (flat != 0)
+    if small.any():
+        spacing = 2.0 ** -133
+        bits[small] = (np.rint(flat[small] / spacing) * spacing).view(np.uint64)
+    big = (np.abs(out) > _BF16_MAX) & np.isfinite(x)
+    out[big] = np.copysign(np.inf, out[big])
     return out
 
 

@@ -35,6 +35,35 @@ def test_bf16_round_matches_torch_cast_on_fp32_values():
     assert np.array_equal(ours, ref)
 
 
+def test_bf16_round_brute_force_on_float64_inputs():
+    # float64 inputs carry more bits than fp32, so the torch-cast pin above does
+    # not reach them: compare with the two bf16 neighbours found by brute force
+    # (8 significant bits via math.frexp, or the 2^-133 grid below 2^-126) and
+    # pick the nearer, the even one on a tie
+    rng = np.random.default_rng(99)
+    e = rng.integers(-138, 128, size=3000)
+    x = np.ldexp(rng.uniform(1.0, 2.0, size=e.size), e) * rng.choice([-1.0, 1.0], size=e.size)
+    ties = np.ldexp(1.0 + (2 * rng.integers(0, 128, size=300) + 1) * 2.0 ** -8, rng.integers(-100, 100, size=300))
+    x = np.concatenate([x, ties, -ties])
+    got = O.bf16_round(x)
+    for xi, gi in zip(x, got):
+        a = abs(float(xi))
+        if a >= 2.0 ** -126:
+            _, ex = math.frexp(a)
+            step = 2.0 ** (ex - 8)
+        else:
+            step = 2.0 ** -133
+        lo = math.floor(a / step) * step
+        hi = lo + step
+        if a - lo < hi - a or (a - lo == hi - a and (lo / step) % 2 == 0):
+            want = lo
+        else:
+            want = hi
+        if want > (2.0 - 2.0 ** -7) * 2.0 ** 127:
+            want = math.inf
+        assert gi == math.copysign(want, xi), (xi, gi, want)
+
+
 def test_bf16_round_ties_and_limits():
     u = 2.0 ** -7          # bf16 spacing in [1, 2)
     assert O.bf16_round(1.0 + u / 2)[()] == 1.0                 # tie -> even mantissa
