@@ -95,10 +95,14 @@ int qw_abi_version(void);
 const char* qw_last_error_string(void);
 
 /*
- * Synchronises `stream`, then reports and clears the device-side error word
- * that bounded waits inside the tensor-core kernels set when they give up
- * (a wait that should never time out; it exists so that a broken pipeline
- * returns instead of hanging the GPU).  Returns QW_OK or QW_ERR_TIMEOUT.
+ * Synchronises `stream`, then reports and clears the device-side error words.
+ * Bounded waits inside the tensor-core and decode kernels set them when they
+ * give up (a wait that should never time out; it exists so that a broken
+ * pipeline returns instead of hanging the GPU): QW_ERR_TIMEOUT.  Decode
+ * attention also records a context_lens entry larger than the max_context of
+ * its call (the keys past max_context were not read, so that output is
+ * wrong): QW_ERR_INVALID_ARG.  Returns QW_OK, QW_ERR_TIMEOUT or
+ * QW_ERR_INVALID_ARG (QW_ERR_CUDA if the synchronisation fails).
  */
 int qw_device_error(void* stream);
 
@@ -183,13 +187,18 @@ int qw_attention_prefill(const void* q, const void* k, const void* v, int64_t kv
  * one new query token per sequence, sees cache rows
  * seq_base[b] .. seq_base[b] + context_lens[b] - 1 (the token just stored included).
  *   q   dtype [B, nh, hd];  k_cache, v_cache dtype [num_slots, nkv, hd] (16-byte aligned)
- *   context_lens, seq_base int32 [B];  max_context >= every context_lens[b];
+ *   context_lens, seq_base int32 [B];  max_context >= every context_lens[b]
+ *   (it sizes the split of the keys over CTAs; max_context 0 means every
+ *   sequence is empty and gets a zero output; an entry above max_context is
+ *   not an argument error the host can see, so the kernel records it for
+ *   qw_device_error, which returns QW_ERR_INVALID_ARG);
  *   every cache row read, seq_base[b] .. seq_base[b] + context_lens[b] - 1, < num_slots
  *   out dtype [B, nh, hd]
  *   workspace: device scratch of qw_attention_decode_workspace_size(...) bytes
  *   (split-KV partial results); may be NULL only when that size is 0.  The
  *   first 64 KiB are completion counters: zero before the first call, and
- *   every call leaves them zero.
+ *   every call leaves them zero, including a call whose bounded wait gave up
+ *   (every CTA still runs to its end and counts itself in).
  *   flags: 0, or QW_DECODE_HISTORY_READY (bf16, hd 128).  With that flag the
  *   caller states that context_lens, seq_base and every cache row the call
  *   reads except each sequence's last (position context_lens[b] - 1) were
@@ -293,9 +302,13 @@ int qw_attention_decode_rope(const void* qkv, int n_heads, int n_kv_heads, int h
  * call starts: the array is zero when the library is loaded and every call
  * leaves its counters at zero; the rest of the array needs no clearing,
  * because every value a call reads there was written earlier in the same
- * call.  Calls that can run at the same time on the GPU (on two streams, or
- * from two host threads) race on the array and give wrong results: keep
- * them on one stream.  Each process has its own copy of the array.
+ * call.  A call whose bounded wait gave up (qw_device_error returns
+ * QW_ERR_TIMEOUT) still runs every CTA to its end, so it too leaves the
+ * counters at zero; only its output is invalid.  Calls that can run at the
+ * same time on the GPU (on two streams, or from two host threads) race on
+ * the array and give wrong results: keep them on one stream.  Each process
+ * has its own copy of the array.  Its results are bit-identical to
+ * qw_attention_decode's with a workspace (same kernels, same partition).
  */
 int qw_attention_decode_static(const void* q, const void* k_cache, const void* v_cache, int64_t num_slots,
                                const int32_t* context_lens, const int32_t* seq_base, int B, int max_context,

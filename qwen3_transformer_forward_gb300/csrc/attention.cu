@@ -29,6 +29,10 @@ namespace attn {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Error word of the decode kernels: bits 0x1/0x2 record a bounded wait that gave up.
+__device__ unsigned int g_attn_timeout = 0;
+// Bit kErrContextOverflow (common.cuh) records a context length beyond max_context.
+
 // ---------------------------------------------------------------------------
 // tensor-core helpers (legacy warp-level MMA)
 // ---------------------------------------------------------------------------
@@ -251,6 +255,7 @@ __global__ void __launch_bounds__(DC_THREADS) attn_decode_kernel(
   const int b = blockIdx.z, g = blockIdx.y, split = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int L = ctx_lens[b];
+  if (tid == 0 && split == n_splits - 1 && L > n_splits * chunk) atomicOr(&g_attn_timeout, kErrContextOverflow);
   const int start = split * chunk;
   const int end = min(L, start + chunk);
   const int h0 = g * G;
@@ -415,7 +420,6 @@ __global__ void __launch_bounds__(DC_THREADS) attn_decode_kernel(
 // starts at or after the pair where an earlier one stopped), and the last to
 // finish, by the pair's completion counter, merges them in CTA order.
 // ---------------------------------------------------------------------------
-__device__ unsigned int g_attn_timeout = 0;
 
 constexpr int DT_KT = 64, DT_STAGES = 3, DT_THREADS = 128;
 constexpr uint32_t DT_BOX = 64 * 64 * 2;          // 64 keys x 64 dims of bf16
@@ -629,6 +633,7 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
     const int b = p / nkv, g = p % nkv;
     int ta, tb, Tb;
     seg_range(p, ta, tb, Tb);
+    if (tid == 0 && Tb > T) atomicOr(&g_attn_timeout, kErrContextOverflow);   // keys past max_context
     const int L = b == p_first / nkv ? L_first : ctx_lens[b];
     // q of this thread's row (head g * G + gq; rows >= G are zero)
     uint32_t qa[8][2];
@@ -710,15 +715,21 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
       for (int i = 0; i < 16; ++i) {
         o[i][0] *= alpha;
         o[i][1] *= alpha;
+        o[i][2] *= alpha;
+        o[i][3] *= alpha;
       }
-      const uint32_t a0 = pack_bf16(pr[0], pr[1]);
-      const uint32_t a2 = pack_bf16(pr[2], pr[3]);
+      // P as two bf16 parts in the two row halves of the A fragment: rows 0-7
+      // (the group's heads) hold hi = bf16(p), rows 8-15 (unused by the
+      // heads) hold lo = bf16(p - hi), so accumulator rows 8-15 collect lo*V
+      // at no extra MMA and hi + lo carries p to about 2^-17 relative.
+      uint32_t a0, a1, a2, a3;
+      split_p(pr, a0, a1, a2, a3);
 #pragma unroll
       for (int dp = 0; dp < 8; ++dp) {
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(st + 2 * DT_BOX + kv_off(key0 + ri + 8 * (mi & 1), 2 * dp + (mi >> 1)), b0, b1, b2, b3);
-        mma_bf16(o[2 * dp], a0, 0u, a2, 0u, b0, b1);
-        mma_bf16(o[2 * dp + 1], a0, 0u, a2, 0u, b2, b3);
+        mma_bf16(o[2 * dp], a0, a1, a2, a3, b0, b1);
+        mma_bf16(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
       }
       __syncwarp();
       if (lane == 0) tcx::mbar_arrive(empty(s));
@@ -737,9 +748,9 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     if (gq < G) {
 #pragma unroll
-      for (int dn = 0; dn < 16; ++dn) {
-        sO[(warp * G + gq) * DC_HD + 8 * dn + 2 * tq] = o[dn][0];
-        sO[(warp * G + gq) * DC_HD + 8 * dn + 2 * tq + 1] = o[dn][1];
+      for (int dn = 0; dn < 16; ++dn) {   // the hi and lo parts of P * V
+        sO[(warp * G + gq) * DC_HD + 8 * dn + 2 * tq] = o[dn][0] + o[dn][2];
+        sO[(warp * G + gq) * DC_HD + 8 * dn + 2 * tq + 1] = o[dn][1] + o[dn][3];
       }
       if (tq == 0) {
         sML[(warp * G + gq) * 2] = m_run;
@@ -912,7 +923,7 @@ static size_t decode_tc_workspace_bound(int B, int n_heads) {
 }
 
 extern "C" size_t qw_attention_decode_workspace_size(int B, int max_context, int n_heads, int head_dim) {
-  if (B <= 0 || max_context <= 0 || n_heads <= 0 || head_dim != 128) return 0;
+  if (B <= 0 || max_context < 0 || n_heads <= 0 || head_dim != 128) return 0;
   size_t need = decode_tc_workspace_bound(B, n_heads);   // bf16
   const DecodePlan p = decode_plan(B, max_context, 0);   // f32 split plan
   if (p.splits > 1) {
@@ -954,7 +965,7 @@ static int launch_decode_tc(const void* q, const void* kc, const void* vc, const
   // equal key chunks (T padded to S * per), so the CTAs of one sequence's kv
   // heads stream the same key rows side by side; otherwise the pairs' tiles
   // are dealt out evenly.  Either way a CTA gets at least two tiles.
-  int T = (max_context + DT_KT - 1) / DT_KT;
+  int T = max_context > 0 ? (max_context + DT_KT - 1) / DT_KT : 1;   // max_context 0: empty sequences only
   const int64_t n_pairs = int64_t(B) * nkv;
   int64_t slots_sm = int64_t(device_sms()) * per_sm;
   if (slots_sm > 8 * device_sms() / G) slots_sm = 8 * device_sms() / G;   // keeps the workspace bound

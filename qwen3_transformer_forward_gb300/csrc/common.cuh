@@ -15,6 +15,11 @@ using bf16 = __nv_bfloat16;
 // must be zero before the first call and each call leaves them zero.
 constexpr size_t kCounterBytes = 64 * 1024;
 
+// Bit of the decode-attention error word set when a context_lens entry exceeds
+// the max_context a call was planned for: keys past it are not read, so the
+// output misses them.  qw_device_error reports it as QW_ERR_INVALID_ARG.
+constexpr unsigned int kErrContextOverflow = 0x100u;
+
 // ---------------------------------------------------------------------------
 // element conversions
 // ---------------------------------------------------------------------------
@@ -36,6 +41,18 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);   // .x = a (low half), .y = b
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Softmax weights p[0..3] of one m16n8k16 A-fragment row (keys 2t, 2t+1,
+// 2t+8, 2t+9) as a bf16 pair hi = bf16(p), lo = bf16(p - hi): hi + lo
+// represents p to about 2^-17 relative (p - hi is exact in fp32).  a0/a2
+// carry hi, a1/a3 carry lo: the fragment's rows r and r + 8.
+__device__ __forceinline__ void split_p(const float (&p)[4], uint32_t& a0, uint32_t& a1, uint32_t& a2,
+                                        uint32_t& a3) {
+  a0 = pack_bf16(p[0], p[1]);
+  a2 = pack_bf16(p[2], p[3]);
+  a1 = pack_bf16(p[0] - bf16_lo(a0), p[1] - bf16_hi(a0));
+  a3 = pack_bf16(p[2] - bf16_lo(a2), p[3] - bf16_hi(a2));
 }
 
 // 16-byte vector load into floats

@@ -775,16 +775,20 @@ __device__ void att_consume(const Params& p, uint8_t* aring, AttShared& as, int6
       for (int i = 0; i < 16; ++i) {
         o[i][0] *= alpha;
         o[i][1] *= alpha;
+        o[i][2] *= alpha;
+        o[i][3] *= alpha;
       }
-      const uint32_t a0 = pack_bf16(pr[0], pr[1]);
-      const uint32_t a2 = pack_bf16(pr[2], pr[3]);
+      // P split into bf16 hi (A rows 0-7, the heads) and lo = bf16(p - hi)
+      // (A rows 8-15, otherwise unused): accumulator rows 8-15 collect lo*V
+      uint32_t a0, a1, a2, a3;
+      split_p(pr, a0, a1, a2, a3);
       if (ok) {
 #pragma unroll
         for (int dp = 0; dp < 8; ++dp) {
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(smem_u32(tv + kv_off(key0 + ri + 8 * (mi & 1), 2 * dp + (mi >> 1))), b0, b1, b2, b3);
-          mma16816(o[2 * dp], a0, 0u, a2, 0u, b0, b1);
-          mma16816(o[2 * dp + 1], a0, 0u, a2, 0u, b2, b3);
+          mma16816(o[2 * dp], a0, a1, a2, a3, b0, b1);
+          mma16816(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
         }
       }
       __syncwarp();
@@ -796,9 +800,9 @@ __device__ void att_consume(const Params& p, uint8_t* aring, AttShared& as, int6
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     if (gq < G) {
 #pragma unroll
-      for (int dn = 0; dn < 16; ++dn) {
-        sO[(wg * G + gq) * HD + 8 * dn + 2 * tq] = o[dn][0];
-        sO[(wg * G + gq) * HD + 8 * dn + 2 * tq + 1] = o[dn][1];
+      for (int dn = 0; dn < 16; ++dn) {   // the hi and lo parts of P * V
+        sO[(wg * G + gq) * HD + 8 * dn + 2 * tq] = o[dn][0] + o[dn][2];
+        sO[(wg * G + gq) * HD + 8 * dn + 2 * tq + 1] = o[dn][1] + o[dn][3];
       }
       if (tq == 0) {
         sML[(wg * G + gq) * 2] = m_run;

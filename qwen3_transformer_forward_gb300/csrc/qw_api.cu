@@ -50,12 +50,17 @@ extern "C" const char* qw_last_error_string(void) { return qw::g_last_error.c_st
 extern "C" int qw_device_error(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return qw::set_error(QW_ERR_CUDA, "qw_device_error: %s", cudaGetErrorString(e));
-  const unsigned int gemm = qw::take_tc_timeouts(), dec = qw::take_attn_timeouts(),
+  const unsigned int gemm = qw::take_tc_timeouts(), dec_word = qw::take_attn_timeouts(),
                      pre = qw::take_prefill_timeouts(), step = qw::take_dstep_errors();
+  const unsigned int dec = dec_word & ~qw::kErrContextOverflow;
   if (gemm | dec | pre | step)
     return qw::set_error(QW_ERR_TIMEOUT,
                          "a bounded device-side wait timed out (gemm 0x%x, decode attention 0x%x, prefill attention "
                          "0x%x, decode step 0x%x)",
                          gemm, dec, pre, step);
+  if (dec_word & qw::kErrContextOverflow)
+    return qw::set_error(QW_ERR_INVALID_ARG,
+                         "decode attention: a context_lens entry exceeded the call's max_context; the keys past it "
+                         "were not read");
   return QW_OK;
 }

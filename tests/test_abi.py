@@ -140,6 +140,9 @@ def test_workspace_sizes(lib):
     assert L.gemm_workspace_size(8, 1024, 3072, 2, L.QW_GEMM_ROW_REDUCE, 0, torch.bfloat16) == 0
     assert L.lm_head_workspace_size(8, 151936, 1024, 2, torch.bfloat16) >= 64 * 1024 + 8 * 1024 * 2
     assert L.attention_decode_workspace_size(64, 2048, 16, 128) > 0
+    # max_context 0 (every sequence empty) still plans one key tile per pair
+    assert L.attention_decode_workspace_size(8, 0, 16, 128) > 0
+    assert L.attention_decode_workspace_size(8, -1, 16, 128) == 0
 
 
 def test_prefetch_l2_checks_its_ranges_on_the_host(lib):
