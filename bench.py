@@ -62,6 +62,8 @@ def parse_args(argv=None):
                     help="launch only this kernel, --profile-reps times, on inputs of the workload's shape "
                          "(random values, mean decode context) and exit: a small case for ncu section captures")
     ap.add_argument("--profile-reps", type=int, default=3)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload lines (embedding + lm_head, one layer, 64-sequence decode)")
     return ap.parse_args(argv)
 
 
@@ -302,7 +304,9 @@ class Workload:
                                                    + 2.0 * 2 * nkv * hd * B * mean_ctx + 2.0 * 2 * nkv * hd * B
                                                    + 2.0 * B * (4 * H + qkvw + nh * hd + I))),
             "lm_head": ("hbm", 2.0 * V * H + 2.0 * B * V),
-            "embed_vocab": ("hbm", 2.0 * 2 * T * H + 8.0 * T),
+            # each launch: its ids, the table rows they select, the output rows
+            "prefill.embed_vocab": ("hbm", 2.0 * 2 * T * H + 8.0 * T),
+            "decode.embed_vocab": ("hbm", 2.0 * 2 * B * H + 8.0 * B),
         }
 
     def launches_per_step(self, kind):
@@ -310,8 +314,12 @@ class Workload:
         fused_norm = self.fwd.norm_fusion_ok(self.B)
         per_layer = {"add_rmsnorm": 0 if fused_norm and kind.startswith("decode.") else 2}
         base = kind.split(".", 1)[-1]
-        if kind in ("lm_head", "embed_vocab"):
+        if kind == "lm_head":
             return 1 + self.S
+        if kind == "prefill.embed_vocab":
+            return 1
+        if kind == "decode.embed_vocab":
+            return self.S
         if kind == "decode.layers":
             return self.S
         n = per_layer.get(base, 1) * nl
@@ -329,24 +337,24 @@ def load_peaks():
         return {"hbm": 6800.0, "tensor": 1700.0, "tensor_burst": 1900.0, "source": "fallback"}
 
 
-def attention_traffic_from_profile():
-    """dram bytes per launch of the decode attention kernel from its committed ncu
-    summary, or None when attention.cu changed since that capture."""
+def profile_traffic(name: str):
+    """DRAM bytes per launch of a kernel from its committed ncu capture
+    (profiles/<name>.json), or None when a source file it records has changed
+    since the capture."""
     import hashlib
-    import re
-    prof = os.path.join(ROOT, "profiles", "decode_attention_bench_shape.md")
-    src = os.path.join(ROOT, "qwen3_transformer_forward_gb300", "csrc", "attention.cu")
-    if not os.path.exists(prof):
+    path = os.path.join(ROOT, "profiles", name + ".json")
+    if not os.path.exists(path):
         return None
-    with open(prof) as f:
-        text = f.read()
-    with open(src, "rb") as f:
-        src_sha1 = hashlib.sha1(f.read()).hexdigest()
-    m_b = re.search(r"dram_bytes_per_launch = (\d+)", text)
-    m_h = re.search(r"attention\.cu sha1 = ([0-9a-f]{40})", text)
-    if not m_b or not m_h or src_sha1 != m_h.group(1):
-        return None
-    return int(m_b.group(1))
+    with open(path) as f:
+        prof = json.load(f)
+    for rel, sha in prof.get("sources_sha1", {}).items():
+        try:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                if hashlib.sha1(f.read()).hexdigest() != sha:
+                    return None
+        except OSError:
+            return None
+    return prof.get("dram_bytes_per_launch")
 
 
 def attention_roofline(wl, peaks, reps=5):
@@ -391,7 +399,7 @@ def attention_roofline(wl, peaks, reps=5):
     qkvw = (nh + 2 * nkv) * hd
     algo = 2.0 * 2 * nkv * hd * sum(ctx) + 2.0 * B * nh * hd + 2.0 * B * qkvw + 2.0 * 2 * B * nkv * hd + 16.0 * B
     achieved = algo / (us * 1e-6) / 1e9
-    traffic = attention_traffic_from_profile()
+    traffic = profile_traffic("decode_attention_bench_shape")
     if traffic is not None:   # the capture ran at the mean context: scale to this one
         traffic = round(traffic * sum(ctx) / (B * (statistics.mean(wl.seq_lens) + wl.S // 2)))
     return {"kernel": "decode.attention", "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm"],
@@ -400,6 +408,158 @@ def attention_roofline(wl, peaks, reps=5):
             "peak_source": f"{peaks['source']} (HBM copy)",
             "timing": f"{m.n_layers} back-to-back launches over the {m.n_layers} layers' KV caches (larger than L2), "
                       f"decode step {s}, one CUDA graph replayed {reps} times, events on the replay stream"}
+
+
+# ----------------------------------------------------------------------------
+# the other workloads: one line each, with its own roofline
+# ----------------------------------------------------------------------------
+
+def _time_launches(fn, reps, flush=None):
+    """Mean ms of fn() over reps launches, each timed alone with CUDA events on the
+    current stream; flush() (an L2-sized write) runs before each, outside the events."""
+    total = 0.0
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    return total / reps
+
+
+def _graph(fn):
+    fn()
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def _roof(bound, amount, ms, peaks, peak_key, what):
+    if bound == "hbm":
+        achieved, peak, unit = amount / (ms / 1e3) / 1e9, peaks["hbm"], "GB/s"
+    else:
+        achieved, peak, unit = amount / (ms / 1e3) / 1e12, peaks[peak_key], "TFLOP/s"
+    return {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 3), "algorithmic": round(amount), "what": what,
+            "peak_source": f"{peaks['source']} ({'HBM copy' if bound == 'hbm' else peak_key.replace('_', ' ')})"}
+
+
+def config_embed_lm_head(peaks, reps=10):
+    """Vocab-sharded embedding of 8192 ids (5 % on shard boundaries) and the lm_head
+    producing the full [8192, 151936] logits, bf16, vocab 151936 x 1024."""
+    import seeded_inputs as si
+    from qwen3_transformer_forward_gb300 import _lib as L
+    w = si.workload("embed_lm_head")
+    m = w.model
+    T, H, V = w.n_tokens, m.hidden, m.vocab
+    table = si.checkpoint_tensor(m, "embed_tokens", device="cuda")
+    ids = si.embed_ids(m, T, w.boundary_fraction).cuda()
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")   # 256 MB > L2
+    flush = flush_buf.zero_
+    out = {}
+    emb = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    for tp in w.tps:
+        ms = _time_launches(lambda: L.embed_vocab(ids, table, tp, emb), reps, flush)
+        out[f"embed_tp{tp}"] = {"us_per_launch": round(ms * 1e3, 2),
+                                "roofline": _roof("hbm", 2.0 * 2 * T * H + 8.0 * T, ms, peaks, "hbm",
+                                                  "ids + selected table rows + output rows")}
+    hidden = si.normal(0, "embed_lm_head.hidden", (T, H), 1.0, "bf16").cuda()
+    logits = torch.empty(T, V, dtype=torch.bfloat16, device="cuda")
+    for tp in w.tps:
+        ws = torch.zeros(L.lm_head_workspace_size(T, V, H, tp, torch.bfloat16), dtype=torch.uint8, device="cuda")
+        ms = _time_launches(lambda: L.lm_head(hidden, None, T, table, tp, logits, None, ws), max(3, reps // 2), flush)
+        out[f"lm_head_tp{tp}"] = {"us_per_launch": round(ms * 1e3, 2),
+                                  "roofline": _roof("tensor", 2.0 * T * H * V, ms, peaks, "tensor_burst",
+                                                    "2 x 8192 x 1024 x 151936 FLOP (2.49 GB of logits written)")}
+    L.device_error()
+    del table, logits, flush_buf
+    torch.cuda.empty_cache()
+    return {"workload": "vocab 151936 x 1024 bf16, 8192 ids (5 % at shard boundaries), tp 1/2/4; "
+                        "lm_head over 8192 N(0,1) hidden rows -> full [8192, 151936] logits",
+            "timing": f"each launch alone after a 256 MB L2 flush, CUDA events, mean of {reps} (lm_head "
+                      f"{max(3, reps // 2)})", **out}
+
+
+def config_layer_prefill(peaks, reps=20):
+    """One Qwen3-0.6B decoder layer, two shards, prefill of 4 x 512 tokens."""
+    import seeded_inputs as si
+    from qwen3_transformer_forward_gb300 import _lib as L
+    from qwen3_transformer_forward_gb300 import model as M
+    w = si.workload("layer_prefill")
+    m = w.model
+    b = si.prefill_batch(m, w.seq_lens)
+    T = b.ids.shape[0]
+    x = si.normal(0, "layer_prefill.hidden", (T, m.hidden), 1.0, "bf16").cuda()
+    params = M.load_params(m, device="cuda")
+    fwd = M.Qwen3Forward(m, params, max_tokens=T, num_slots=b.num_slots, max_seqs=len(w.seq_lens),
+                         max_context=max(w.seq_lens))
+    ctx = M.to_device_prefill(b)
+    g = _graph(lambda: fwd.run_layers(ctx, decode=False, hidden_in=x, final_norm=False))
+    ms = _time_launches(g.replay, reps)
+    L.device_error()
+    H, I, hd, nh, nkv = m.hidden, m.intermediate, m.head_dim, m.n_heads, m.n_kv_heads
+    flops = 2.0 * T * ((nh + 2 * nkv) * hd * H + H * nh * hd + 2 * I * H + H * I) + \
+        4.0 * hd * nh * sum(L_ * (L_ + 1) // 2 for L_ in w.seq_lens)
+    return {"workload": "one Qwen3-0.6B layer (bf16, tp=2 layout), prefill 4 x 512, N(0,1) hidden inputs",
+            "metric": "prefill tokens/s", "value": round(T / (ms / 1e3), 1), "unit": "tokens/s",
+            "us_per_layer": round(ms * 1e3, 2),
+            "roofline": _roof("tensor", flops, ms, peaks, "tensor_burst",
+                              "GEMM + causal attention FLOP of the layer (68.7 GFLOP); the norms, RoPE and KV "
+                              "store are HBM-bound extras inside the same time"),
+            "timing": f"one CUDA graph of the layer's kernels (plus a 4 MB copy of the input rows), "
+                      f"mean of {reps} replays; weights and activations fit in L2"}
+
+
+def config_model_decode(peaks, reps=10):
+    """The 28-layer model (tp 1), one decode step of 64 sequences with contexts
+    uniform in [256, 2048] over a synthetic cache history."""
+    import seeded_inputs as si
+    from qwen3_transformer_forward_gb300 import _lib as L
+    from qwen3_transformer_forward_gb300 import model as M
+    w = si.workload("model_decode")
+    m = w.model
+    ctx_lens = si.decode_context_lens(0, w.batch, w.ctx_low, w.ctx_high)
+    batch = si.decode_batch(m, ctx_lens)
+    params = M.load_params(m, device="cuda")
+    kc = [torch.zeros(batch.num_slots, m.n_kv_heads, m.head_dim, dtype=torch.bfloat16, device="cuda")
+          for _ in range(m.n_layers)]
+    vc = [torch.zeros_like(kc[0]) for _ in range(m.n_layers)]
+    hist = torch.cat([torch.arange(int(batch.seq_base[b]), int(batch.seq_base[b]) + ctx_lens[b] - 1)
+                      for b in range(w.batch)]).cuda()
+    for l in range(m.n_layers):
+        kc[l][hist] = si.kv_history(m, l, "k", hist)
+        vc[l][hist] = si.kv_history(m, l, "v", hist)
+    fwd = M.Qwen3Forward(m, params, max_tokens=w.batch, num_slots=batch.num_slots, max_seqs=w.batch,
+                         max_context=max(ctx_lens), kv_caches=(kc, vc))
+    ctx = M.to_device_decode(batch)
+    g = _graph(lambda: fwd.decode(ctx))
+    for _ in range(3):
+        g.replay()
+    ms = _time_launches(g.replay, reps)
+    L.device_error()
+    H, I, hd, nh, nkv, V = m.hidden, m.intermediate, m.head_dim, m.n_heads, m.n_kv_heads, m.vocab
+    weights = m.n_layers * 2.0 * ((nh + 2 * nkv) * hd * H + H * nh * hd + 2 * I * H + H * I) + 2.0 * V * H
+    kv = m.n_layers * 2.0 * 2 * nkv * hd * sum(ctx_lens)
+    out = {"workload": "28-layer Qwen3-0.6B shape (bf16, tp=1), one decode step for 64 sequences, contexts "
+                       "U[256, 2048] (sum %d) over a seeded N(0,1) cache history, greedy argmax" % sum(ctx_lens),
+           "metric": "decode tokens/s", "value": round(w.batch / (ms / 1e3), 1), "unit": "tokens/s",
+           "ms_per_step": round(ms, 3),
+           "roofline": _roof("hbm", weights + kv, ms, peaks, "hbm",
+                             f"every weight byte once ({weights / 1e9:.3f} GB incl. the tied table) + the cached "
+                             f"K/V each sequence attends to ({kv / 1e9:.2f} GB)"),
+           "timing": f"one CUDA graph of the step (embedding, 28 layers, final norm, lm_head, argmax), "
+                     f"mean of {reps} replays after 3; {(weights + kv) / 1e9:.1f} GB streamed, larger than L2"}
+    del fwd, kc, vc, params
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args, rank, world, local):
@@ -496,10 +656,34 @@ def run_ours(args, rank, world, local):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(wl, args, world)
+    launches = count_launches(wl)
+
+    # the decode phase as a whole against HBM: every weight byte and the cached
+    # K/V rows once per step, over the measured decode time (launch gaps,
+    # phase boundaries and all)
+    m = wl.m
+    H, I, hd, nh, nkv, V = m.hidden, m.intermediate, m.head_dim, m.n_heads, m.n_kv_heads, m.vocab
+    layer_w = 2.0 * ((nh + 2 * nkv) * hd * H + H * nh * hd + 2 * I * H + H * I)
+    mean_ctx = statistics.mean(L0 + s + 1 for s in range(wl.S) for L0 in wl.seq_lens)
+    layer_kv = 2.0 * 2 * nkv * hd * wl.B * mean_ctx
+    step_bytes = m.n_layers * (layer_w + layer_kv) + 2.0 * V * H
+    step_ms = decode_ms / wl.S
+    decode_chain = {"bound": "hbm", "bytes_per_step": round(step_bytes), "ms_per_step": round(step_ms, 4),
+                    "achieved": round(step_bytes / (step_ms / 1e3) / 1e9, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                    "frac": round(step_bytes / (step_ms / 1e3) / 1e9 / peaks["hbm"], 3),
+                    "bytes_per_layer": round(layer_w + layer_kv),
+                    "what": "28 layers' weights + the K/V each sequence attends to (mean context) + the tied "
+                            "table for the lm_head, over the measured decode time per step"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args)
+
+    configs = None
+    if not args.no_configs and world == 1:
+        configs = {"embed_lm_head": config_embed_lm_head(peaks), "layer_prefill": config_layer_prefill(peaks),
+                   "model_decode": config_model_decode(peaks)}
+
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -513,8 +697,8 @@ def run_ours(args, rank, world, local):
         "prefill_tok_s": round(sum(wl.seq_lens) / (prefill_ms / 1e3), 1),
         "decode_tok_s": round(wl.S * wl.B / (decode_ms / 1e3), 1),
         "prefill_ms": round(prefill_ms, 3), "decode_ms": round(decode_ms, 3),
-        "roofline": roofline, "kernels": kernels, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
-        "gpu_launches": count_launches(wl),
+        "roofline": roofline, "decode_chain": decode_chain, "kernels": kernels, "clocks": clocks, "e2e": e2e,
+        "cpu_baseline": cpu, "gpu_launches": launches, "configs": configs,
     }
     return out
 
@@ -597,15 +781,21 @@ def cpu_sample_setup(n_layers_sample: int):
     return m, weights, cos_sin
 
 
-def cpu_sample_run(m, weights, cos_sin, n_tokens: int):
-    """Prefill of one sequence of n_tokens through the sampled layers, final norm,
-    lm_head of the last token; returns (seconds for the 28-layer model, detail)."""
+def cpu_sample_run(m, weights, cos_sin, n_tokens: int, decode_seqs: int = 8):
+    """One bounded sample of the workload through the oracle:
+      prefill: one sequence of n_tokens through the sampled layers, final norm and
+               the lm_head of its last token;
+      decode:  one decode step of decode_seqs sequences at context n_tokens + 1
+               through the same layers (each sequence's cache holds the prefill's
+               rows), final norm, lm_head and argmax of every sequence.
+    Returns measured seconds and the full-model projection (layer time x
+    n_layers / sampled layers)."""
     import numpy as np
     import oracle as O
     import seeded_inputs as si
     nl = len(weights.layers)
     b = si.prefill_batch(m, [n_tokens])
-    cache = O.KVCache(nl, b.num_slots, m.n_kv_heads, m.head_dim, m.tp)
+    cache = O.KVCache(nl, n_tokens, m.n_kv_heads, m.head_dim, m.tp)
     ctx = O.AttnContext(True, b.slot_mapping.numpy(), cu_seqlens=b.cu_seqlens.numpy())
     t0 = time.perf_counter()
     h = O.vocab_parallel_embedding(b.ids.numpy(), weights.embed, m.tp)
@@ -618,46 +808,89 @@ def cpu_sample_run(m, weights, cos_sin, n_tokens: int):
     lg = O.compute_logits(m, weights.embed, h, m.tp, b.cu_seqlens.numpy())
     O.greedy(lg)
     t3 = time.perf_counter()
-    model_s = (t1 - t0) + (t2 - t1) * m.n_layers / nl + (t3 - t2)
-    return model_s, t3 - t0
+    prefill_model = (t1 - t0) + (t2 - t1) * m.n_layers / nl + (t3 - t2)
+    # decode: every sequence's cache = the prefill's rows, then this step's row
+    L = n_tokens + 1
+    dcache = O.KVCache(nl, decode_seqs * L, m.n_kv_heads, m.head_dim, m.tp)
+    for r in range(m.tp):
+        for l in range(nl):
+            for q in range(decode_seqs):
+                dcache.k[r][l][q * L:q * L + n_tokens] = cache.k[r][l]
+                dcache.v[r][l][q * L:q * L + n_tokens] = cache.v[r][l]
+    base = np.arange(decode_seqs) * L
+    pos = np.full(decode_seqs, n_tokens)
+    dctx = O.AttnContext(False, base + n_tokens, seq_base=base, context_lens=pos + 1)
+    ids = si.uniform_int(0, "decode.forced_ids", (decode_seqs,), 0, m.vocab).numpy()
+    t4 = time.perf_counter()
+    h = O.vocab_parallel_embedding(ids, weights.embed, m.tp)
+    t5 = time.perf_counter()
+    res = None
+    for l in range(nl):
+        h, res = O.decoder_layer(m, weights.layers[l], l, pos, h, res, dctx, dcache, *cos_sin)
+    t6 = time.perf_counter()
+    h, _ = O.add_rms_norm(h, res, weights.final_norm, m.eps, m.dtype)
+    O.greedy(O.compute_logits(m, weights.embed, h, m.tp))
+    t7 = time.perf_counter()
+    decode_model = (t5 - t4) + (t6 - t5) * m.n_layers / nl + (t7 - t6)
+    return {"prefill_s": prefill_model, "decode_s": decode_model, "wall_s": (t3 - t0) + (t7 - t4)}
+
+
+def cpu_projection(m, r, w):
+    """Full-workload tokens/s from one sample: the step's prefill sequences each cost
+    one sampled prefill, its decode steps each one sampled decode step."""
+    n_seq, S, B = len(w.seq_lens), w.decode_steps, len(w.seq_lens)
+    step_s = n_seq * r["prefill_s"] + S * r["decode_s"]
+    tokens = sum(w.seq_lens) + S * B
+    return tokens / step_s, step_s
+
+
+def _cpu_sample_text(args, m, w):
+    return (f"prefill of 1 sequence x {args.cpu_sample_tokens} tokens and one decode step of {len(w.seq_lens)} "
+            f"sequences at context {args.cpu_sample_tokens + 1}, each through {args.cpu_sample_layers} of the "
+            f"{m.n_layers} layers plus embedding, final norm and lm_head; layer time scaled x "
+            f"{m.n_layers}/{args.cpu_sample_layers}; the workload step = {len(w.seq_lens)} such prefills + "
+            f"{w.decode_steps} such decode steps (numpy float64, threads = all host cores)")
 
 
 def cpu_baseline(args):
+    import seeded_inputs as si
     m, weights, cos_sin = cpu_sample_setup(args.cpu_sample_layers)
-    model_s, wall = cpu_sample_run(m, weights, cos_sin, args.cpu_sample_tokens)
-    n = args.cpu_sample_tokens
-    return {"value": round(n / model_s, 2), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"prefill of 1 sequence x {n} tokens through {args.cpu_sample_layers} of the 28 layers, "
-                      f"embedding, final norm, lm_head of the last token; layer time scaled x "
-                      f"{m.n_layers}/{args.cpu_sample_layers} to the full model ({wall:.1f} s of CPU work, "
-                      f"numpy float64, threads = all host cores)"}
+    w = si.workload(WORKLOAD)
+    r = cpu_sample_run(m, weights, cos_sin, args.cpu_sample_tokens)
+    value, step_s = cpu_projection(m, r, w)
+    return {"value": round(value, 2), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "prefill_tok_s": round(args.cpu_sample_tokens / r["prefill_s"], 2),
+            "decode_tok_s": round(len(w.seq_lens) / r["decode_s"], 3),
+            "projected_step_s": round(step_s, 1), "sample_wall_s": round(r["wall_s"], 2),
+            "sample": _cpu_sample_text(args, m, w)}
 
 
 def run_reference(args, rank, world):
+    import seeded_inputs as si
     if rank != 0:
         return None
     m, weights, cos_sin = cpu_sample_setup(args.cpu_sample_layers)
+    w = si.workload(WORKLOAD)
     n = args.cpu_sample_tokens
     for _ in range(args.warmup):
         cpu_sample_run(m, weights, cos_sin, n)
-    times = []
-    walls = []
-    for _ in range(args.steps):
-        s, w = cpu_sample_run(m, weights, cos_sin, n)
-        times.append(s)
-        walls.append(w)
-    ms_step = statistics.mean(times) * 1e3
-    value = n / (ms_step / 1e3)
-    sample = (f"each step: prefill of 1 sequence x {n} tokens through {args.cpu_sample_layers} of the 28 layers, "
-              f"embedding, final norm, lm_head of the last token; layer time scaled x "
-              f"{m.n_layers}/{args.cpu_sample_layers}")
+    runs = [cpu_sample_run(m, weights, cos_sin, n) for _ in range(args.steps)]
+    wall_ms = statistics.mean(r["wall_s"] for r in runs) * 1e3
+    proj = [cpu_projection(m, r, w) for r in runs]
+    value = statistics.mean(p[0] for p in proj)
     return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 1), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded), random-init weights",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall_ms, 1),
+            "projected_ms_per_full_step": round(statistics.mean(p[1] for p in proj) * 1e3, 1),
+            "prefill_tok_s": round(statistics.mean(n / r["prefill_s"] for r in runs), 2),
+            "decode_tok_s": round(statistics.mean(len(w.seq_lens) / r["decode_s"] for r in runs), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded), random-init weights",
             "config": {"workload": "qwen3-0.6b-shape 28 layers, tp=2 layout, prefill 8x2048 + 128 greedy decode "
                                    "steps x 8 (bounded CPU sample, see cpu_baseline.sample)"},
             "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": "each step: " + _cpu_sample_text(args, m, w) +
+                                       "; ms_per_step is the measured wall time of the sample, value the "
+                                       "full-step projection"},
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -321,7 +321,7 @@ class Qwen3Forward:
         m = self.m
         B = ctx.n_tokens
         table, ws = self._fused_state()
-        with self._around("embed_vocab", -1):
+        with self._around("decode.embed_vocab", -1):
             L.embed_vocab(ctx.ids, self.p.embed, m.tp, self.h[:B], self.err, stream)
         with self._around("decode.layers", -1):
             L.decode_layers(table, len(self.p.layers), self.h[:B], ctx.positions, ctx.slot_mapping, ctx.context_lens,
@@ -338,7 +338,7 @@ class Qwen3Forward:
         if decode and hidden_in is None and final_norm and self.fused_decode_ok(T):
             return self._decode_fused(ctx, stream)
         if hidden_in is None:
-            with self._around("embed_vocab", -1):
+            with self._around(f"{'decode' if decode else 'prefill'}.embed_vocab", -1):
                 L.embed_vocab(ctx.ids, self.p.embed, m.tp, self.h[:T], self.err, stream)
         else:
             self.h[:T].copy_(hidden_in)

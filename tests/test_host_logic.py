@@ -100,19 +100,21 @@ def test_load_peaks_measured_and_fallback(tmp_path, monkeypatch):
     assert bench.load_peaks()["source"] == "fallback"
 
 
-def test_attention_traffic_only_for_the_captured_source(tmp_path, monkeypatch):
+def test_profile_traffic_only_for_the_captured_source(tmp_path, monkeypatch):
     import bench
     src = tmp_path / "qwen3_transformer_forward_gb300" / "csrc"
     src.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
     code = b"// kernel source as captured\n"
     (src / "attention.cu").write_bytes(code)
-    (tmp_path / "profiles" / "decode_attention_bench_shape.md").write_text(
-        f"- dram_bytes_per_launch = 69676000\n- attention.cu sha1 = {hashlib.sha1(code).hexdigest()}\n")
+    (tmp_path / "profiles" / "k.json").write_text(json.dumps(
+        {"dram_bytes_per_launch": 69676000,
+         "sources_sha1": {"qwen3_transformer_forward_gb300/csrc/attention.cu": hashlib.sha1(code).hexdigest()}}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.attention_traffic_from_profile() == 69676000
+    assert bench.profile_traffic("k") == 69676000
+    assert bench.profile_traffic("missing") is None
     (src / "attention.cu").write_bytes(code + b"// changed since\n")
-    assert bench.attention_traffic_from_profile() is None
+    assert bench.profile_traffic("k") is None
 
 
 def test_max_over_ranks_is_identity_on_one_rank():
