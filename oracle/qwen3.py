@@ -67,7 +67,7 @@ __all__ = [
     "KVCache", "LayerWeights", "ModelWeights", "load_weights", "load_layer", "AttnContext",
     "attention_block", "mlp_block",
     "decoder_layer", "model_forward", "compute_logits", "greedy",
-    "parallel_lm_head_rank", "lm_head_unsharded",
+    "parallel_lm_head_rank", "lm_head_unsharded", "sample",
 ]
 
 
@@ -553,3 +553,48 @@ def compute_logits(m, table, hidden, tp: int, cu_seqlens=None) -> np.ndarray:
 def greedy(logits) -> np.ndarray:
     """Greedy sampling: argmax over the vocab, lowest index on ties (np.argmax's first occurrence)."""
     return np.argmax(np.asarray(logits), axis=-1).astype(np.int64)
+
+
+# ----------------------------------------------------------------------------
+# sampling  ([SK] §3 note: the Sampler is one of the small compiled operators)
+# ----------------------------------------------------------------------------
+
+def sample(logits, temperature, top_p, uniforms) -> np.ndarray:
+    """Temperature / top-p sampling of one token per row (a reading: the pages
+    name the Sampler among nano-vllm's compiled small operators but give no
+    semantics).
+
+    Row b with temperature T and nucleus mass P:
+      * T == 0: greedy, the argmax of the logits (lowest index on ties).
+      * otherwise the token is drawn from softmax(logits / T) restricted to the
+        nucleus: with c_1 > c_2 > ... the row's distinct logit values and
+        m_k the softmax mass of the tokens whose logit is c_k, K is the first k
+        with m_1 + ... + m_k >= P (mass relative to the whole row); the nucleus
+        is every token with logit >= c_K (tokens tied at the boundary value are
+        all kept).  P = 1 keeps the whole row.
+      * the draw uses the Gumbel-max identity: with u_v uniform in (0, 1) and
+        G_v = -log(-log u_v), argmax over the nucleus of logits_v / T + G_v is
+        distributed as the restricted softmax (E. J. Gumbel's extreme-value
+        distribution; argmax ties to the lowest index).
+    logits [B, V]; temperature, top_p [B]; uniforms [B, V] in (0, 1), the random
+    numbers of the draw (an input, so both sides use the same ones).
+    """
+    logits = np.asarray(logits, dtype=np.float64)
+    uniforms = np.asarray(uniforms, dtype=np.float64)
+    out = np.zeros(logits.shape[0], dtype=np.int64)
+    for b in range(logits.shape[0]):
+        lg = logits[b]
+        T = float(temperature[b])
+        if T == 0.0:
+            out[b] = int(np.argmax(lg))
+            continue
+        z = lg / T
+        e = np.exp(z - np.max(z))
+        values, which = np.unique(lg, return_inverse=True)          # ascending distinct values
+        mass = np.bincount(which, weights=e, minlength=len(values))
+        cum = np.cumsum(mass[::-1])                                    # from the largest value down
+        K = int(np.argmax(cum >= float(top_p[b]) * cum[-1]))
+        nucleus = lg >= values[::-1][K]
+        g = -np.log(-np.log(uniforms[b]))
+        out[b] = int(np.argmax(np.where(nucleus, z + g, -np.inf)))
+    return out

@@ -123,6 +123,20 @@ def uniform_int(seed: int, name: str, shape, low: int, high: int, device="cpu") 
     return (a % (high - low) + low).view(shape)
 
 
+def uniform01(seed: int, name: str, shape, device="cpu") -> torch.Tensor:
+    """float32 values in the open interval (0, 1): (2 k + 1) * 2^-24 for k the top 23
+    bits of a hash word, exact in fp32 (an integer below 2^24 and a power-of-two multiply)."""
+    shape = tuple(int(s) for s in shape)
+    n = math.prod(shape)
+    out = torch.empty(n, dtype=torch.float32, device=device)
+    for s0 in range(0, n, _CHUNK):
+        s1 = min(n, s0 + _CHUNK)
+        idx = torch.arange(s0, s1, dtype=torch.int64, device=device)
+        a, _ = hash_words(seed, name, idx)
+        out[s0:s1] = ((a >> 9) * 2 + 1).to(torch.float32) * (2.0 ** -24)
+    return out.view(shape)
+
+
 def uniform_word(seed: int, name: str, shape, device="cpu") -> torch.Tensor:
     """Raw 32-bit words (int64 tensor in [0, 2**32))."""
     shape = tuple(int(s) for s in shape)

@@ -499,3 +499,50 @@ def test_attention_block_uses_default_softmax_scale():
             torch.from_numpy(q).transpose(0, 1), torch.from_numpy(k).transpose(0, 1).repeat_interleave(group, 0),
             torch.from_numpy(v).transpose(0, 1).repeat_interleave(group, 0), is_causal=True).transpose(0, 1)
         assert np.allclose(tr["o"][r], ref.numpy(), atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# sampler (temperature / top-p, Gumbel-max draw)
+# ----------------------------------------------------------------------------
+
+def test_sample_zero_temperature_is_greedy_and_shift_invariant():
+    lg = np.array([[0.5, 2.0, 2.0, -1.0], [1.0, 1.0, 1.0, 1.0]])
+    u = si.uniform01(0, "pin.sample.u", lg.shape).double().numpy()
+    assert list(O.sample(lg, [0.0, 0.0], [0.9, 0.1], u)) == [1, 0]      # lowest index on ties
+    t = O.sample(lg, [0.8, 1.3], [1.0, 0.6], u)
+    assert np.array_equal(O.sample(lg + 7.25, [0.8, 1.3], [1.0, 0.6], u), t)
+
+
+def test_sample_nucleus_of_a_worked_row():
+    # logits [3, 1, 1, 0] at T = 1: p = [e^3, e, e, 1] / (e^3 + 2e + 1) = [0.7573, 0.1025, 0.1025, 0.0377];
+    # P = 0.8 needs the first two distinct values, so the nucleus is {0, 1, 2} (the tie at 1 kept whole);
+    # P = 0.97 needs all four.  u_3 near 1 gives token 3 a Gumbel value of about 13.8.
+    lg = np.array([[3.0, 1.0, 1.0, 0.0]])
+    u = np.array([[0.5, 0.5, 0.5, 1.0 - 1e-6]])
+    assert O.sample(lg, [1.0], [0.8], u)[0] == 0
+    assert O.sample(lg, [1.0], [0.97], u)[0] == 3
+    u2 = np.array([[0.5, 0.5, 1.0 - 1e-6, 0.5]])
+    assert O.sample(lg, [1.0], [0.8], u2)[0] == 2        # inside the nucleus, the large draw wins
+    assert O.sample(lg, [1.0], [0.7], u2)[0] == 0        # P below m_1 = 0.757: only token 0
+    assert O.sample(lg, [1.0], [1e-9], u2)[0] == 0
+
+
+@pytest.mark.parametrize("T,P", [(0.7, 1.0), (1.5, 0.8)])
+def test_sample_frequencies_follow_the_restricted_softmax(T, P):
+    # many rows of the same logits, each with its own uniforms: the token
+    # frequencies converge to softmax(l / T) over the nucleus, renormalised
+    lg = np.array([1.2, -0.3, 0.4, 2.0, 0.0, -1.1])
+    N = 120000
+    u = si.uniform01(0, f"pin.sample.freq.{T}", (N, lg.size)).double().numpy()
+    tok = O.sample(np.tile(lg, (N, 1)), np.full(N, T), np.full(N, P), u)
+    p = np.exp(lg / T)
+    p /= p.sum()
+    order = np.argsort(-lg)
+    keep = np.zeros(lg.size, bool)
+    cum = np.cumsum(p[order])
+    keep[order[:int(np.argmax(cum >= P * cum[-1])) + 1]] = True
+    q = np.where(keep, p, 0.0)
+    q /= q.sum()
+    freq = np.bincount(tok, minlength=lg.size) / N
+    assert np.all(freq[~keep] == 0)
+    assert np.max(np.abs(freq - q)) < 5 * np.sqrt(0.25 / N), (freq, q)
