@@ -88,7 +88,7 @@ typedef enum {
   QW_EPI_SILU_MUL = 1     /* fused SiluAndMul on a merged gate_up output ([SK] §4) */
 } qw_epilogue;
 
-/* Version of this ABI (increments on any signature change); this is version 5. */
+/* Version of this ABI (increments on any signature change); this is version 6. */
 int qw_abi_version(void);
 
 /* Description of the last failure on the calling thread ("" if none). */
@@ -414,6 +414,37 @@ size_t qw_lm_head_workspace_size(int64_t n_out, int64_t V, int64_t H, int tp, in
 
 /* Greedy argmax over rows of logits dtype [M, V] -> int64 [M], lowest index on ties. */
 int qw_argmax(const void* logits, int64_t M, int64_t V, int64_t* out, int dtype, void* stream);
+
+/*
+ * Temperature / top-p sampling of one token per row: the Sampler that
+ * nano-vllm compiles with RMSNorm, RoPE and SiluAndMul ([SK] §3).  The pages
+ * give no semantics; this is the reading implemented:
+ *   temperature[b] <= 0 (or NaN): greedy, argmax with the lowest index on ties
+ *   (top_p and uniforms of that row are not read);
+ *   otherwise the token is drawn from softmax(logits[b] / T) restricted to the
+ *   nucleus: the row's distinct logit values are taken from the largest down
+ *   until their softmax mass reaches top_p[b] of the row's mass, and every
+ *   token whose logit is at least the last value taken is kept (tokens tied
+ *   at the boundary are all kept; top_p outside (0, 1] keeps the whole row).
+ *   The draw is the Gumbel-max identity: argmax over the nucleus of
+ *   logits / T - log(-log u), lowest index on ties.
+ *   logits      bf16 [B, V], finite, 16-byte aligned
+ *   temperature float [B], top_p float [B] (device)
+ *   uniforms    float [B, V] (device, 16-byte aligned): the random numbers of
+ *               the draw, each in (0, 1) (clamped to [2^-24, 1 - 2^-24]);
+ *               supplied by the caller so that draws are reproducible
+ *   out         int64 [B]
+ *   workspace:  qw_sample_workspace_size(B, V) bytes, 16-byte aligned, zero
+ *               when first used; every call leaves it ready for the next
+ *               (calls that may run concurrently need separate workspaces).
+ * Three launches; results do not depend on timing (fixed reduction orders).
+ * Rules: bf16 (else QW_ERR_DTYPE); V a positive multiple of 8 below 2^30;
+ * B <= 16384.  Errors: QW_ERR_INVALID_ARG, QW_ERR_SHAPE, QW_ERR_WORKSPACE.
+ */
+int qw_sample(const void* logits, int64_t B, int64_t V, const float* temperature, const float* top_p,
+              const float* uniforms, int64_t* out, void* workspace, size_t workspace_bytes, int dtype,
+              void* stream);
+size_t qw_sample_workspace_size(int64_t B, int64_t V);
 
 /*
  * One decode step of every decoder layer in one persistent kernel: for each

@@ -53,6 +53,8 @@ SIGNATURES = {
     "qw_lm_head": (C.c_int, [_p, _i64, _p, _i64, _p, _i64, _i64, _i32, _p, _p, _p, _sz, _i32, _p]),
     "qw_lm_head_workspace_size": (C.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
     "qw_argmax": (C.c_int, [_p, _i64, _i64, _p, _i32, _p]),
+    "qw_sample": (C.c_int, [_p, _i64, _i64, _p, _p, _p, _p, _p, _sz, _i32, _p]),
+    "qw_sample_workspace_size": (C.c_size_t, [_i64, _i64]),
     "qw_prefetch_l2": (C.c_int, [_p, _p, _i32, _p]),
     "qw_selftest_wait_timeout": (C.c_int, [_p]),
     "qw_add_rmsnorm_gemm": (C.c_int, [_p, _p, _p, _p, _f32, _p, _p, _i64, _i64, _i64, _i32, _i32, _i32, _p]),
@@ -291,6 +293,19 @@ def argmax(logits, out, stream=None):
     M, V = logits.shape
     _check(load().qw_argmax(_dev_ptr(logits, "logits"), M, V, _dev_ptr(out, "out"), dtype_code(logits.dtype),
                             _stream(stream)))
+
+
+def sample_workspace_size(B, V) -> int:
+    return load().qw_sample_workspace_size(B, V)
+
+
+def sample(logits, temperature, top_p, uniforms, out, workspace, stream=None):
+    """Temperature / top-p sampling (qw_sample): one token per logits row into out."""
+    B, V = logits.shape
+    _check(load().qw_sample(_dev_ptr(logits, "logits"), B, V, _dev_ptr(temperature, "temperature"),
+                            _dev_ptr(top_p, "top_p"), _dev_ptr(uniforms, "uniforms"), _dev_ptr(out, "out"),
+                            _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                            dtype_code(logits.dtype), _stream(stream)))
 
 
 def prefetch_l2(tensors, stream=None):

@@ -19,7 +19,8 @@ INCLUDE = ROOT / "include"
 LIB = PKG / "libqw.so"
 BUILD_DIR = ROOT / "_build"
 
-SOURCES = ["qw_api.cu", "elementwise.cu", "gemm.cu", "attention.cu", "attention_prefill.cu", "decode_step.cu"]
+SOURCES = ["qw_api.cu", "elementwise.cu", "gemm.cu", "attention.cu", "attention_prefill.cu", "decode_step.cu",
+           "sampler.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-warn-spills"]

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.qw_abi_version() == 5
+    assert lib.qw_abi_version() == 6
 
 
 def test_argument_errors_are_reported_before_launch(lib):
@@ -121,6 +121,14 @@ def test_argument_errors_are_reported_before_launch(lib):
     # 16 tokens of K = 8192 normed rows do not fit in shared memory
     assert lib.qw_add_rmsnorm_gemm(fake, None, None, fake, 1e-6, fake, fake, 16, 64, 8192, 1, 0, L.QW_BF16,
                                    None) == L.QW_ERR_SHAPE
+    # sampler: bf16 only, V a multiple of 8, a workspace of the queried size
+    assert lib.qw_sample(fake, 4, 151936, fake, fake, fake, fake, fake, 1 << 30, L.QW_F32, None) == L.QW_ERR_DTYPE
+    assert lib.qw_sample(fake, 4, 100, fake, fake, fake, fake, fake, 1 << 30, L.QW_BF16, None) == L.QW_ERR_INVALID_ARG
+    assert lib.qw_sample(fake, 4, 151936, fake, fake, fake, fake, None, 0, L.QW_BF16, None) == L.QW_ERR_WORKSPACE
+    need = lib.qw_sample_workspace_size(4, 151936)
+    assert need >= 64 * 1024 + 4 * 65536 * 4
+    assert lib.qw_sample(fake, 4, 151936, fake, fake, fake, fake, fake, need - 1, L.QW_BF16, None) == L.QW_ERR_WORKSPACE
+    assert lib.qw_sample(None, 0, 151936, None, None, None, None, None, 0, L.QW_BF16, None) == L.QW_OK
     # lm_head: V not divisible by tp
     assert lib.qw_lm_head(fake, 4, None, 4, fake, 10, 64, 4, fake, None, None, 0, L.QW_BF16,
                           None) == L.QW_ERR_SHAPE
