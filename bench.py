@@ -281,7 +281,10 @@ class Workload:
         gemm_b = lambda M_, N_, K_: 2.0 * (N_ * K_ + M_ * K_ + M_ * N_)  # noqa: E731
         return {
             "prefill.gemm_qkv": ("tensor", 2.0 * T * qkvw * H),
+            "prefill.gemm_qkv_norm_rope_store_kv": ("tensor", 2.0 * T * qkvw * H),
             "prefill.gemm_o": ("tensor", 2.0 * T * H * nh * hd),
+            "prefill.gemm_o_add_rmsnorm": ("tensor", 2.0 * T * H * nh * hd),
+            "prefill.gemm_down_add_rmsnorm": ("tensor", 2.0 * T * H * I),
             "prefill.gemm_gate_up_silu": ("tensor", 2.0 * T * 2 * I * H),
             "prefill.gemm_down": ("tensor", 2.0 * T * H * I),
             "prefill.attention": ("tensor", 4.0 * hd * nh * causal_pairs),
@@ -312,6 +315,8 @@ class Workload:
     def launches_per_step(self, kind):
         nl = self.m.n_layers
         fused_norm = self.fwd.norm_fusion_ok(self.B)
+        if kind == "prefill.add_rmsnorm" and self.fwd.prefill_fusion_ok():
+            return 1   # before the first layer; the o_proj / down epilogues do the rest
         per_layer = {"add_rmsnorm": 0 if fused_norm and kind.startswith("decode.") else 2}
         base = kind.split(".", 1)[-1]
         if kind == "lm_head":
@@ -715,6 +720,10 @@ def count_launches(wl):
         dec_layer -= 1
     # split-K sums and the split-KV merge happen inside the GEMM and attention kernels
     prefill = 1 + m.n_layers * per_layer + 1 + 3     # embed, layers, final norm, gather + gemm + argmax
+    if wl.fwd.prefill_fusion_ok():
+        # embed, one add+RMSNorm, 5 per layer (QKV + norm/RoPE/KV store, attention, o_proj + add + norm,
+        # gate_up + SiluAndMul, down + add + norm), gather + gemm + argmax
+        prefill = 1 + 1 + m.n_layers * 5 + 3
     lm_dec = 2                                       # gemm + argmax
     if wl.fwd.fused_decode_ok(wl.B):
         decode = 1 + 1 + lm_dec                      # embed, all layers in one kernel, lm_head

@@ -88,7 +88,7 @@ typedef enum {
   QW_EPI_SILU_MUL = 1     /* fused SiluAndMul on a merged gate_up output ([SK] §4) */
 } qw_epilogue;
 
-/* Version of this ABI (increments on any signature change); this is version 6. */
+/* Version of this ABI (increments on any signature change); this is version 8. */
 int qw_abi_version(void);
 
 /* Description of the last failure on the calling thread ("" if none). */
@@ -159,6 +159,49 @@ int qw_qkv_norm_rope_store_kv(const void* qkv, int64_t T, int n_heads, int n_kv_
                               int64_t max_position, const void* q_gamma, const void* k_gamma, float eps,
                               const int64_t* slot_mapping, void* k_cache, void* v_cache, int64_t num_slots,
                               void* q_out, int32_t* err_count, int dtype, void* stream);
+
+/*
+ * A row-parallel Linear whose output joins the residual stream, followed by
+ * the next RMSNorm ([SK] §1-§2 add_rms_forward, [TP] §3 Y = sum_r X_r W_r^T):
+ * qw_gemm (ROW_REDUCE) then qw_add_rmsnorm, in one launch for many tokens
+ * (prefill o_proj and down_proj):
+ *   residual <- round(round(A W^T) + residual)            (in place)
+ *   y        <- round(residual * rsqrt(mean(residual^2) + eps) * gamma)
+ *   A bf16 [M, K];  W bf16 [tp, N, K/tp] (shard r = input columns r);
+ *   residual bf16 [M, N] (read and written);  gamma bf16 [N];  y bf16 [M, N]
+ * The N/256 column tiles of a 128-row block run as one thread-block cluster
+ * and add their rows' sums of squares in tile order over distributed shared
+ * memory.  Rounding points as qw_gemm + qw_add_rmsnorm; the sum of squares is
+ * accumulated in another order (fp32), so y may differ from that pair of
+ * calls by one bf16 step where it lies next to a rounding midpoint.
+ * Rules: bf16; N a multiple of 256 up to 2048; K % tp == 0, (K/tp) % 8 == 0;
+ * 16-byte aligned pointers; y must not alias residual.  Errors: QW_ERR_DTYPE,
+ * QW_ERR_SHAPE, QW_ERR_INVALID_ARG.
+ */
+int qw_gemm_add_rmsnorm(const void* A, const void* W, int64_t M, int64_t N, int64_t K, int tp, void* residual,
+                        const void* gamma, float eps, void* y, int dtype, void* stream);
+
+/*
+ * The merged QKV projection with its per-head QK-RMSNorm, RoPE and KV-cache
+ * store as the GEMM's epilogue ([SK] §5 QKVParallelLinear, §8 ①, §3, §7.1):
+ * qw_gemm (COLUMN) of A [T, H] by W followed by qw_qkv_norm_rope_store_kv,
+ * with the same results bit for bit, except that the QKV output never goes
+ * to memory.  For many tokens (prefill): every token row runs on a 128-row
+ * tensor-core tile.
+ *   A bf16 [T, H];  W bf16 [tp * (nh/tp + 2*nkv/tp) * 128, H], shard r's rows
+ *   [q_r; k_r; v_r] (the layout of qw_qkv_norm_rope_store_kv's qkv columns);
+ *   positions, cos_sin, max_position, q_gamma, k_gamma, eps, slot_mapping,
+ *   k_cache, v_cache, num_slots, q_out, err_count: as for
+ *   qw_qkv_norm_rope_store_kv (head_dim 128).
+ * Rules: bf16; head_dim 128; tp divides nh and nkv; (nh + 2*nkv)/tp even (a
+ * 256-column tile holds two whole heads of one shard); H % 8 == 0; 16-byte
+ * aligned pointers.  Errors: QW_ERR_DTYPE, QW_ERR_SHAPE, QW_ERR_INVALID_ARG.
+ */
+int qw_qkv_gemm_norm_rope_store_kv(const void* A, const void* W, int64_t T, int64_t H, int n_heads, int n_kv_heads,
+                                   int head_dim, int tp, const int64_t* positions, const float* cos_sin,
+                                   int64_t max_position, const void* q_gamma, const void* k_gamma, float eps,
+                                   const int64_t* slot_mapping, void* k_cache, void* v_cache, int64_t num_slots,
+                                   void* q_out, int32_t* err_count, int dtype, void* stream);
 
 /*
  * Causal varlen GQA attention for prefill (flash_attn_varlen_func with

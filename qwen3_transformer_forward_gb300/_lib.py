@@ -34,6 +34,9 @@ SIGNATURES = {
     "qw_rope_cos_sin_table": (C.c_int, [_p, _i64, _i32, _f64]),
     "qw_qkv_norm_rope_store_kv": (C.c_int, [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _i64, _p, _p, _f32, _p, _p,
                                             _p, _i64, _p, _p, _i32, _p]),
+    "qw_gemm_add_rmsnorm": (C.c_int, [_p, _p, _i64, _i64, _i64, _i32, _p, _p, _f32, _p, _i32, _p]),
+    "qw_qkv_gemm_norm_rope_store_kv": (C.c_int, [_p, _p, _i64, _i64, _i32, _i32, _i32, _i32, _p, _p, _i64, _p, _p,
+                                                 _f32, _p, _p, _p, _i64, _p, _p, _i32, _p]),
     "qw_attention_prefill": (C.c_int, [_p, _p, _p, _i64, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _i32, _p]),
     "qw_attention_decode": (C.c_int, [_p, _p, _p, _i64, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32, _p, _p, _sz,
                                       _i32, _i32, _p]),
@@ -174,6 +177,27 @@ def qkv_norm_rope_store_kv(qkv, n_heads, n_kv_heads, head_dim, tp, positions, co
         _dev_ptr(cos_sin, "cos_sin"), cos_sin.shape[0], _dev_ptr(q_gamma, "q_gamma"), _dev_ptr(k_gamma, "k_gamma"),
         eps, _dev_ptr(slot_mapping, "slot_mapping"), _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"),
         k_cache.shape[0], _dev_ptr(q_out, "q_out"), _dev_ptr(err_count, "err_count"), dtype_code(qkv.dtype),
+        _stream(stream)))
+
+
+def gemm_add_rmsnorm(A, W, residual, gamma, eps, y, tp, stream=None):
+    """Row-parallel GEMM whose output is added to the residual in place, then RMSNorm into y (qw_gemm_add_rmsnorm)."""
+    M, K = A.shape
+    N = residual.shape[1]
+    _check(load().qw_gemm_add_rmsnorm(_dev_ptr(A, "A"), _dev_ptr(W, "W"), M, N, K, tp, _dev_ptr(residual, "residual"),
+                                      _dev_ptr(gamma, "gamma"), eps, _dev_ptr(y, "y"), dtype_code(A.dtype),
+                                      _stream(stream)))
+
+
+def qkv_gemm_norm_rope_store_kv(A, W, n_heads, n_kv_heads, head_dim, tp, positions, cos_sin, q_gamma, k_gamma, eps,
+                                slot_mapping, k_cache, v_cache, q_out, err_count=None, stream=None):
+    """Merged QKV GEMM with QK-RMSNorm + RoPE + KV store as its epilogue (qw_qkv_gemm_norm_rope_store_kv)."""
+    T, H = A.shape
+    _check(load().qw_qkv_gemm_norm_rope_store_kv(
+        _dev_ptr(A, "A"), _dev_ptr(W, "W"), T, H, n_heads, n_kv_heads, head_dim, tp, _dev_ptr(positions, "positions"),
+        _dev_ptr(cos_sin, "cos_sin"), cos_sin.shape[0], _dev_ptr(q_gamma, "q_gamma"), _dev_ptr(k_gamma, "k_gamma"), eps,
+        _dev_ptr(slot_mapping, "slot_mapping"), _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"),
+        k_cache.shape[0], _dev_ptr(q_out, "q_out"), _dev_ptr(err_count, "err_count"), dtype_code(A.dtype),
         _stream(stream)))
 
 

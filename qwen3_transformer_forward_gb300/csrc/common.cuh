@@ -55,6 +55,34 @@ __device__ __forceinline__ void split_p(const float (&p)[4], uint32_t& a0, uint3
   a3 = pack_bf16(p[2] - bf16_lo(a2), p[3] - bf16_hi(a2));
 }
 
+// QK-RMSNorm + RoPE of one 128-wide head ([SK] §3, §8 ①), pairing element i
+// with i + 64.  Used by the standalone kernel (eight lanes per head) and by the
+// QKV GEMM epilogue (one thread per head); every step is an explicit
+// round-to-nearest fp32 operation, so no contraction into FMA can make the
+// two differ.  Sum of squares: eight partials, partial p over the pairs
+// (8p + e, 64 + 8p + e) for e = 0..7 in order, combined as a balanced tree.
+__device__ __forceinline__ float qk_ss8(const float (&x1)[8], const float (&x2)[8]) {
+  float ss = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ss = __fadd_rn(ss, __fadd_rn(__fmul_rn(x1[e], x1[e]), __fmul_rn(x2[e], x2[e])));
+  return ss;
+}
+__device__ __forceinline__ float qk_ss_tree(const float (&p)[8]) {
+  return __fadd_rn(__fadd_rn(__fadd_rn(p[0], p[1]), __fadd_rn(p[2], p[3])),
+                   __fadd_rn(__fadd_rn(p[4], p[5]), __fadd_rn(p[6], p[7])));
+}
+__device__ __forceinline__ float qk_inv_rms(float ss, float eps) {
+  return rsqrtf(__fadd_rn(__fmul_rn(ss, 1.0f / 128.0f), eps));
+}
+// normed (rounded to bf16 as the q_norm / k_norm output) then rotated; zero when the position is invalid
+__device__ __forceinline__ void qk_rope_pair(float x1, float x2, float inv, float g1, float g2, float c, float sn,
+                                             bool pos_ok, float& y1, float& y2) {
+  const float n1 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(x1, inv), g1)));
+  const float n2 = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(x2, inv), g2)));
+  y1 = pos_ok ? __fsub_rn(__fmul_rn(n1, c), __fmul_rn(n2, sn)) : 0.0f;
+  y2 = pos_ok ? __fadd_rn(__fmul_rn(n2, c), __fmul_rn(n1, sn)) : 0.0f;
+}
+
 // 16-byte vector load into floats
 __device__ __forceinline__ void load16(const bf16* p, float* f) {
   uint4 u = *reinterpret_cast<const uint4*>(p);

@@ -253,13 +253,12 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_hd128_kernel(
   float x1[8], x2[8];
   load16(src + i0, x1);
   load16(src + HALF + i0, x2);
-  float ss = 0.0f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) ss += x1[e] * x1[e] + x2[e] * x2[e];
-  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-  const float inv = rsqrtf(ss / float(HD) + eps);
+  // lane `sub` holds partial `sub`; the xor tree forms qk_ss_tree's balanced sum in every lane
+  float ss = qk_ss8(x1, x2);
+  ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 1));
+  ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 2));
+  ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 4));
+  const float inv = qk_inv_rms(ss, eps);
   const int64_t pos = positions[tok];
   const bool pos_ok = pos >= 0 && pos < max_pos;
   if (!pos_ok && sub == 0 && h == 0 && err != nullptr) atomicAdd(err, 1);
@@ -274,12 +273,7 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_hd128_kernel(
   *reinterpret_cast<float4*>(sn + 4) = *reinterpret_cast<const float4*>(cs + HALF + i0 + 4);
   float y1[8], y2[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float n1 = round_t<bf16>((x1[e] * inv) * g1[e]);   // q_norm / k_norm output
-    const float n2 = round_t<bf16>((x2[e] * inv) * g2[e]);
-    y1[e] = pos_ok ? n1 * c[e] - n2 * sn[e] : 0.0f;          // RoPE on the halves
-    y2[e] = pos_ok ? n2 * c[e] + n1 * sn[e] : 0.0f;
-  }
+  for (int e = 0; e < 8; ++e) qk_rope_pair(x1[e], x2[e], inv, g1[e], g2[e], c[e], sn[e], pos_ok, y1[e], y2[e]);
   if (is_q) {
     bf16* o = q_out + (tok * nh + h) * int64_t(HD);
     store16(o + i0, y1);

@@ -66,7 +66,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-constexpr int EPI_NONE = 0, EPI_SILU = 1;
+constexpr int EPI_NONE = 0, EPI_SILU = 1, EPI_QKV = 2, EPI_ADDNORM = 3;
 constexpr int kMaxCluster = 8;   // portable cluster size: K-splits per weight tile
 
 struct TcArgs {
@@ -83,6 +83,25 @@ struct TcArgs {
   int64_t k_shard;      // K / tp
   int64_t i_l;          // intermediate per shard (SILU)
   int silu_tps;         // output tiles per shard (SILU)
+  // EPI_QKV: per-head QK-RMSNorm + RoPE + KV-cache store on the merged QKV output
+  const int64_t* positions;
+  const float* cos_sin;  // [max_pos, 128]: cos | sin
+  int64_t max_pos;
+  const bf16* q_gamma;
+  const bf16* k_gamma;
+  float eps;
+  const int64_t* slots;  // cache row per token, -1 = not stored
+  bf16* k_cache;
+  bf16* v_cache;
+  int64_t num_slots;
+  bf16* q_out;           // [M, nh, 128]
+  int32_t* err;
+  int nh, nkv, tp;
+  // EPI_ADDNORM: resid <- round(round(C) + resid); y = RMSNorm(resid) * norm_gamma (the
+  // row's N columns span the cluster's CTAs; eps as above)
+  bf16* resid;
+  bf16* y_out;
+  const bf16* norm_gamma;
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -351,6 +370,123 @@ __global__ void __launch_bounds__(192, 1)
             }
           }
         }
+      } else if (EPI == EPI_ADDNORM) {
+        // pass 1: the new residual s = round(round(acc) + resid) of this CTA's
+        // 256 columns, written back in place, and its sum of squares (in column
+        // order) left in shared memory for the cluster
+        float ss = 0.0f;
+        const bool row_ok = m < a.M;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(trow + c, r);
+          tmem_ld_wait();
+          if (!row_ok) continue;
+          const int64_t n0 = int64_t(tile_q) * BN + c;
+          bf16* rp = a.resid + m * a.ldc + n0;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float x[8], f[8];
+            load16(rp + 8 * v, x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float o = (ok && has_acc) ? round_t<bf16>(__uint_as_float(r[8 * v + e])) : 0.0f;
+              f[e] = round_t<bf16>(__fadd_rn(o, x[e]));
+              ss = __fadd_rn(ss, __fmul_rn(f[e], f[e]));
+            }
+            store16(rp + 8 * v, f);
+          }
+        }
+        reinterpret_cast<float*>(sA)[quarter * 32 + lane] = ss;   // the ring is free: every MMA has completed
+      } else if (EPI == EPI_QKV) {
+        // The tile's 256 columns are two whole heads of the merged QKV output
+        // (shard r = [q_r | k_r | v_r], 128 columns per head).  Each thread owns
+        // one token: it rounds the accumulator to the bf16 QKV value, then a q or
+        // k head is normed, rotated and written (q_out / k cache), a v head is
+        // copied into the v cache, with the arithmetic of the standalone kernel.
+        const bool row_ok = m < a.M && ok && has_acc;
+        int64_t pos = 0, slot = -1;
+        if (m < a.M) {
+          pos = a.positions[m];
+          slot = a.slots[m];
+        }
+        const bool pos_ok = pos >= 0 && pos < a.max_pos;
+        const int nh_l = a.nh / a.tp, nkv_l = a.nkv / a.tp;
+        const int64_t width_r = int64_t(nh_l + 2 * nkv_l) * 128;
+#pragma unroll 1
+        for (int hh = 0; hh < BN / 128; ++hh) {
+          const int64_t n0 = int64_t(tile_q) * BN + 128 * hh;
+          if (n0 >= a.N) break;   // uniform over the CTA
+          float x[128];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld32(trow + uint32_t(128 * hh + 32 * c), r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[32 * c + e] = round_t<bf16>(__uint_as_float(r[e]));
+          }
+          if (!row_ok) continue;
+          const int shard = int(n0 / width_r);
+          const int loc = int((n0 % width_r) / 128);
+          if (loc < nh_l + nkv_l) {
+            const bool is_q = loc < nh_l;
+            const int hidx = is_q ? shard * nh_l + loc : shard * nkv_l + (loc - nh_l);
+            bf16* dst;
+            if (is_q) {
+              if (hidx == 0 && !pos_ok && a.err != nullptr) atomicAdd(a.err, 1);   // once per token
+              dst = a.q_out + (m * a.nh + hidx) * 128;
+            } else {
+              if (slot == -1) continue;                                           // padding: not stored
+              if (slot < 0 || slot >= a.num_slots) {
+                if (hidx == 0 && a.err != nullptr) atomicAdd(a.err, 1);
+                continue;
+              }
+              if (!pos_ok) continue;
+              dst = a.k_cache + (slot * a.nkv + hidx) * 128;
+            }
+            float part[8];
+#pragma unroll
+            for (int pp = 0; pp < 8; ++pp) {
+              float x1[8], x2[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                x1[e] = x[8 * pp + e];
+                x2[e] = x[64 + 8 * pp + e];
+              }
+              part[pp] = qk_ss8(x1, x2);
+            }
+            const float inv = qk_inv_rms(qk_ss_tree(part), a.eps);
+            const bf16* gamma = is_q ? a.q_gamma : a.k_gamma;
+            const float* cs = a.cos_sin + (pos_ok ? pos : 0) * 128;
+#pragma unroll
+            for (int pp = 0; pp < 8; ++pp) {
+              float g1[8], g2[8], cc[8], sn[8], y1[8], y2[8];
+              load16(gamma + 8 * pp, g1);
+              load16(gamma + 64 + 8 * pp, g2);
+              *reinterpret_cast<float4*>(cc) = *reinterpret_cast<const float4*>(cs + 8 * pp);
+              *reinterpret_cast<float4*>(cc + 4) = *reinterpret_cast<const float4*>(cs + 8 * pp + 4);
+              *reinterpret_cast<float4*>(sn) = *reinterpret_cast<const float4*>(cs + 64 + 8 * pp);
+              *reinterpret_cast<float4*>(sn + 4) = *reinterpret_cast<const float4*>(cs + 64 + 8 * pp + 4);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                qk_rope_pair(x[8 * pp + e], x[64 + 8 * pp + e], inv, g1[e], g2[e], cc[e], sn[e], pos_ok, y1[e], y2[e]);
+              store16(dst + 8 * pp, y1);
+              store16(dst + 64 + 8 * pp, y2);
+            }
+          } else {   // v head: the rounded QKV values, a bit copy into the cache
+            const int g = shard * nkv_l + (loc - nh_l - nkv_l);
+            if (slot < 0 || slot >= a.num_slots || !pos_ok) continue;
+            bf16* dst = a.v_cache + (slot * a.nkv + g) * 128;
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = x[8 * v + e];
+              store16(dst + 8 * v, f);
+            }
+          }
+        }
       } else {  // EPI_SILU
         const int r_s = tile_q / a.silu_tps;
         const int64_t jl0 = int64_t(tile_q % a.silu_tps) * (BN / 2);
@@ -411,6 +547,36 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     }
+  }
+
+  if (!SWAP && EPI == EPI_ADDNORM) {
+    // the row's sum of squares over the cluster's CTAs (rank order), then pass 2:
+    // y = round(s * rsqrt(mean(s^2) + eps) * gamma) over this CTA's columns
+    __syncwarp();
+    cluster_sync_all();
+    if (warp >= 2) {
+      const int quarter = warp & 3;
+      const int row = quarter * 32 + lane;
+      const int64_t m = int64_t(tile_p) * BM + row;
+      const uint32_t base = smem_u32(sA) + uint32_t(row) * 4u;
+      float tot = 0.0f;
+      for (int r = 0; r < a.q_tiles; ++r) tot = __fadd_rn(tot, ld_cluster_f32(map_to_rank(base, uint32_t(r))));
+      const float inv = rsqrtf(__fadd_rn(__fdiv_rn(tot, float(a.N)), a.eps));
+      if (m < a.M) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 8) {
+          const int64_t n0 = int64_t(tile_q) * BN + c;
+          float x[8], g[8], y[8];
+          load16(a.resid + m * a.ldc + n0, x);
+          load16(a.norm_gamma + n0, g);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(x[e], inv), g[e]);
+          store16(a.y_out + m * a.ldc + n0, y);
+        }
+      }
+    }
+    // keep every CTA's shared memory alive until all ranks have read it
+    cluster_sync_all();
   }
 
   if (SWAP && (a.splits > 1 || EPI == EPI_SILU)) {
@@ -1566,6 +1732,138 @@ extern "C" int qw_add_rmsnorm_gemm(const void* x, const void* residual_in, void*
                     static_cast<const bf16*>(gamma), eps};
   return norm_gemm_bf16(static_cast<const bf16*>(x), na, static_cast<const bf16*>(W), static_cast<bf16*>(C), int(M),
                         int(N), int(K), tp, epilogue, static_cast<cudaStream_t>(stream));
+}
+
+// A row-parallel Linear (o_proj, down_proj) whose output joins the residual
+// stream, followed by the next RMSNorm ([SK] §1-§2 add_rms_forward, [TP] §3):
+// the tcgen05 GEMM of many tokens with an epilogue that adds the residual and
+// normalises the row.  The N / 256 tiles of a 128-row block form one thread-
+// block cluster and exchange their rows' sums of squares over distributed
+// shared memory.
+extern "C" int qw_gemm_add_rmsnorm(const void* A, const void* W, int64_t M, int64_t N, int64_t K, int tp,
+                                   void* residual, const void* gamma, float eps, void* y, int dtype, void* stream) {
+  if (dtype != QW_BF16) return set_error(QW_ERR_DTYPE, "qw_gemm_add_rmsnorm: bf16 only");
+  if (M < 0 || N <= 0 || K <= 0 || tp <= 0) return set_error(QW_ERR_INVALID_ARG, "qw_gemm_add_rmsnorm: bad sizes");
+  if (N % 256 || N / 256 > tc::kMaxCluster || K % tp || (K / tp) % 8)
+    return set_error(QW_ERR_SHAPE, "qw_gemm_add_rmsnorm: needs N a multiple of 256 up to 2048 and K/tp %% 8 == 0");
+  if (M == 0) return QW_OK;
+  if (!A || !W || !residual || !gamma || !y) return set_error(QW_ERR_INVALID_ARG, "qw_gemm_add_rmsnorm: null pointer");
+  const uintptr_t al = reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(W) |
+                       reinterpret_cast<uintptr_t>(residual) | reinterpret_cast<uintptr_t>(gamma) |
+                       reinterpret_cast<uintptr_t>(y);
+  if (al % 16) return set_error(QW_ERR_INVALID_ARG, "qw_gemm_add_rmsnorm: pointers must be 16-byte aligned");
+  if (y == residual) return set_error(QW_ERR_INVALID_ARG, "qw_gemm_add_rmsnorm: y must not alias the residual");
+  const int64_t Kl = K / tp;
+  const int kpb = int((Kl + tc::BK - 1) / tc::BK);
+  CUtensorMap mA, mW;
+  int rc = make_map(&mA, A, 2, uint64_t(K), uint64_t(M), 1, uint64_t(K) * 2, 0, tc::BM);
+  if (rc) return rc;
+  rc = make_map(&mW, W, 3, uint64_t(Kl), uint64_t(N), uint64_t(tp), uint64_t(Kl) * 2, uint64_t(Kl) * 2 * uint64_t(N),
+                256u);
+  if (rc) return rc;
+  tc::TcArgs a{};
+  a.C = nullptr;
+  a.ldc = N;
+  a.M = M;
+  a.N = N;
+  a.kpb = kpb;
+  a.kblocks_total = kpb * tp;
+  a.kblocks = kpb * tp;
+  a.k_shard = Kl;
+  a.splits = 1;
+  a.p_tiles = int((M + tc::BM - 1) / tc::BM);
+  a.q_tiles = int(N / 256);
+  a.p_fastest = 0;   // the tiles of one row block are consecutive: one cluster
+  a.eps = eps;
+  a.resid = static_cast<bf16*>(residual);
+  a.y_out = static_cast<bf16*>(y);
+  a.norm_gamma = static_cast<const bf16*>(gamma);
+  auto kern = tc::gemm_tc_kernel<256, 4, false, tc::EPI_ADDNORM, true>;
+  constexpr size_t smem = tc::smem_bytes<256, 4>();
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(a.p_tiles * a.q_tiles), 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(a.q_tiles);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mA, mW, a);
+  if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "gemm_tc_kernel (add + RMSNorm) launch: %s", cudaGetErrorString(e));
+  return check_launch("gemm_tc_kernel (add + RMSNorm)");
+}
+
+// The merged QKV projection of many tokens with its QK-RMSNorm + RoPE + KV
+// store as the tcgen05 GEMM's epilogue (prefill): the QKV output never goes
+// to memory.  Same results, bit for bit, as qw_gemm (COLUMN) followed by
+// qw_qkv_norm_rope_store_kv.
+extern "C" int qw_qkv_gemm_norm_rope_store_kv(const void* A, const void* W, int64_t T, int64_t H, int n_heads,
+                                              int n_kv_heads, int head_dim, int tp, const int64_t* positions,
+                                              const float* cos_sin, int64_t max_position, const void* q_gamma,
+                                              const void* k_gamma, float eps, const int64_t* slot_mapping,
+                                              void* k_cache, void* v_cache, int64_t num_slots, void* q_out,
+                                              int32_t* err_count, int dtype, void* stream) {
+  if (dtype != QW_BF16) return set_error(QW_ERR_DTYPE, "qw_qkv_gemm_norm_rope_store_kv: bf16 only");
+  if (T < 0 || H <= 0 || n_heads <= 0 || n_kv_heads <= 0 || tp <= 0 || max_position <= 0 || num_slots < 0)
+    return set_error(QW_ERR_INVALID_ARG, "qw_qkv_gemm_norm_rope_store_kv: bad sizes");
+  if (head_dim != 128 || n_heads % tp || n_kv_heads % tp || ((n_heads + 2 * n_kv_heads) / tp) % 2 || H % 8)
+    return set_error(QW_ERR_SHAPE,
+                     "qw_qkv_gemm_norm_rope_store_kv: needs head_dim 128, tp | nh and nkv, an even number of heads "
+                     "per shard and H %% 8 == 0");
+  if (T == 0) return QW_OK;
+  if (!A || !W || !positions || !cos_sin || !q_gamma || !k_gamma || !slot_mapping || !k_cache || !v_cache || !q_out)
+    return set_error(QW_ERR_INVALID_ARG, "qw_qkv_gemm_norm_rope_store_kv: null pointer");
+  const uintptr_t al = reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(W) |
+                       reinterpret_cast<uintptr_t>(cos_sin) | reinterpret_cast<uintptr_t>(q_gamma) |
+                       reinterpret_cast<uintptr_t>(k_gamma) | reinterpret_cast<uintptr_t>(k_cache) |
+                       reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(q_out);
+  if (al % 16) return set_error(QW_ERR_INVALID_ARG, "qw_qkv_gemm_norm_rope_store_kv: pointers must be 16-byte aligned");
+  const int64_t N = int64_t(n_heads + 2 * n_kv_heads) * 128;
+  const int kblocks = int((H + tc::BK - 1) / tc::BK);   // one 128 x 256 tile per CTA over the whole K
+  CUtensorMap mA, mW;
+  int rc = make_map(&mA, A, 2, uint64_t(H), uint64_t(T), 1, uint64_t(H) * 2, 0, tc::BM);
+  if (rc) return rc;
+  rc = make_map(&mW, W, 2, uint64_t(H), uint64_t(N), 1, uint64_t(H) * 2, 0, 256u);
+  if (rc) return rc;
+  tc::TcArgs a{};
+  a.C = nullptr;
+  a.ldc = N;
+  a.M = T;
+  a.N = N;
+  a.kblocks_total = kblocks;
+  a.kpb = kblocks;
+  a.k_shard = H;
+  a.splits = 1;
+  a.p_tiles = int((T + tc::BM - 1) / tc::BM);
+  a.q_tiles = int(N / 256);
+  a.p_fastest = (T * H * 2) <= (int64_t(48) << 20) ? 1 : 0;
+  a.kblocks = kblocks;
+  a.positions = positions;
+  a.cos_sin = cos_sin;
+  a.max_pos = max_position;
+  a.q_gamma = static_cast<const bf16*>(q_gamma);
+  a.k_gamma = static_cast<const bf16*>(k_gamma);
+  a.eps = eps;
+  a.slots = slot_mapping;
+  a.k_cache = static_cast<bf16*>(k_cache);
+  a.v_cache = static_cast<bf16*>(v_cache);
+  a.num_slots = num_slots;
+  a.q_out = static_cast<bf16*>(q_out);
+  a.err = err_count;
+  a.nh = n_heads;
+  a.nkv = n_kv_heads;
+  a.tp = tp;
+  return launch_tc<256, 4, false, tc::EPI_QKV, false>(mA, mW, a, 1, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int qw_selftest_wait_timeout(void* stream) {

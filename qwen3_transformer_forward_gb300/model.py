@@ -197,6 +197,9 @@ class Qwen3Forward:
         # the next layer's QKV); off by default
         self.l2_prefetch = False
         self._pf_stream = None
+        # prefill in five kernels per layer: QK-norm + RoPE + KV store in the QKV GEMM's
+        # epilogue, residual add + RMSNorm in the o_proj and down GEMMs' epilogues
+        self.fused_prefill = True
 
     def _around(self, name: str, layer: int):
         if self.probe is None:
@@ -209,6 +212,52 @@ class Qwen3Forward:
                 (M, m.hidden, m.n_heads * m.head_dim, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE),
                 (M, 2 * m.intermediate, m.hidden, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL),
                 (M, m.hidden, m.intermediate, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE)]
+
+    def prefill_fusion_ok(self) -> bool:
+        """Prefill through the fused epilogues: QK-norm + RoPE + KV store in the QKV
+        GEMM (two whole heads of one shard per 256-column tile), residual add +
+        RMSNorm in the o_proj and down GEMMs (a row's hidden columns in one
+        cluster of 256-column tiles)."""
+        m = self.m
+        return (self.fused_prefill and self.dtype == torch.bfloat16 and m.head_dim == 128
+                and ((m.n_heads + 2 * m.n_kv_heads) // m.tp) % 2 == 0 and m.hidden % 256 == 0
+                and m.hidden <= 2048 and (m.n_heads * m.head_dim // m.tp) % 8 == 0
+                and (m.intermediate // m.tp) % 8 == 0 and len(self.p.layers) > 0)
+
+    def _prefill_layer(self, l: int, T: int, ctx, first: bool, next_gamma, stream=None):
+        """One decoder layer of a prefill in five kernels ([SK] §1, §8).
+
+        On entry y holds input_layernorm(residual) (for the first layer it is
+        computed here from the embedding).  On exit the residual holds the
+        stream after the layer and y = RMSNorm(residual) * next_gamma (the next
+        layer's input_layernorm, or the final norm); with next_gamma None, h
+        holds the MLP output and the residual the stream before it, as the
+        unfused layer leaves them."""
+        m, p = self.m, self.p.layers[l]
+        tp = m.tp
+        h, res, y = self.h[:T], self.res[:T], self.y[:T]
+        q, attn, act = self.q[:T], self.attn[:T], self.act[:T]
+        if first:
+            with self._around("prefill.add_rmsnorm", l):
+                L.add_rmsnorm(h, None, res, p.input_ln, m.eps, y, stream)
+        with self._around("prefill.gemm_qkv_norm_rope_store_kv", l):
+            L.qkv_gemm_norm_rope_store_kv(y, p.qkv, m.n_heads, m.n_kv_heads, m.head_dim, tp, ctx.positions,
+                                          self.cos_sin, p.q_norm, p.k_norm, m.eps, ctx.slot_mapping, self.k_cache[l],
+                                          self.v_cache[l], q, self.err, stream)
+        with self._around("prefill.attention", l):
+            L.attention_prefill(q, self.k_cache[l], self.v_cache[l], ctx.cu_seqlens, ctx.cu_seqlens, ctx.seq_base,
+                                ctx.max_seqlen, m.n_heads, m.n_kv_heads, m.head_dim, self.scale, attn, stream)
+        with self._around("prefill.gemm_o_add_rmsnorm", l):
+            L.gemm_add_rmsnorm(attn, p.o, res, p.post_ln, m.eps, y, tp, stream)
+        with self._around("prefill.gemm_gate_up_silu", l):
+            L.gemm(y, p.gate_up, act, 2 * m.intermediate, tp, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL, self.workspace,
+                   stream)
+        if next_gamma is None:
+            with self._around("prefill.gemm_down", l):
+                L.gemm(act, p.down, h, m.hidden, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, self.workspace, stream)
+        else:
+            with self._around("prefill.gemm_down_add_rmsnorm", l):
+                L.gemm_add_rmsnorm(act, p.down, res, next_gamma, m.eps, y, tp, stream)
 
     def norm_fusion_ok(self, T: int) -> bool:
         """Few bf16 tokens: each add+RMSNorm runs as the prologue of the GEMM it feeds."""
@@ -342,7 +391,15 @@ class Qwen3Forward:
                 L.embed_vocab(ctx.ids, self.p.embed, m.tp, self.h[:T], self.err, stream)
         else:
             self.h[:T].copy_(hidden_in)
-        for l in range(len(self.p.layers)):
+        nl = len(self.p.layers)
+        if not decode and self.prefill_fusion_ok():
+            for l in range(nl):
+                nxt = self.p.layers[l + 1].input_ln if l + 1 < nl else (self.p.final_norm if final_norm else None)
+                self._prefill_layer(l, T, ctx, l == 0, nxt, stream)
+            if final_norm:
+                return self.y[:T]   # the last down GEMM applied the final norm
+            return self.h[:T], self.res[:T]
+        for l in range(nl):
             self._layer(l, T, ctx, l == 0, decode, stream)
         if decode and self.l2_prefetch and self._pf_stream is not None:
             torch.cuda.current_stream().wait_stream(self._pf_stream)

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.qw_abi_version() == 6
+    assert lib.qw_abi_version() == 8
 
 
 def test_argument_errors_are_reported_before_launch(lib):
@@ -121,6 +121,20 @@ def test_argument_errors_are_reported_before_launch(lib):
     # 16 tokens of K = 8192 normed rows do not fit in shared memory
     assert lib.qw_add_rmsnorm_gemm(fake, None, None, fake, 1e-6, fake, fake, 16, 64, 8192, 1, 0, L.QW_BF16,
                                    None) == L.QW_ERR_SHAPE
+    # QKV GEMM with the QK-norm / RoPE / KV-store epilogue: bf16, head_dim 128, an even number of heads per shard
+    qg = lambda nh, nkv, hd, tp, dt: (fake, fake, 300, 1024, nh, nkv, hd, tp, fake, fake, 4096, fake, fake, 1e-6,  # noqa: E731
+                                      fake, fake, fake, 100, fake, None, dt, None)
+    assert lib.qw_qkv_gemm_norm_rope_store_kv(*qg(16, 8, 128, 2, L.QW_F32)) == L.QW_ERR_DTYPE
+    assert lib.qw_qkv_gemm_norm_rope_store_kv(*qg(16, 8, 64, 2, L.QW_BF16)) == L.QW_ERR_SHAPE
+    assert lib.qw_qkv_gemm_norm_rope_store_kv(*qg(16, 8, 128, 3, L.QW_BF16)) == L.QW_ERR_SHAPE
+    assert lib.qw_qkv_gemm_norm_rope_store_kv(*qg(5, 1, 128, 1, L.QW_BF16)) == L.QW_ERR_SHAPE   # 7 heads: odd
+    # row-parallel GEMM + residual add + RMSNorm: bf16, N a multiple of 256 up to 2048, y not the residual
+    ga = lambda N, K, tp, y, dt: (fake, fake, 300, N, K, tp, C.c_void_p(32), fake, 1e-6, y, dt, None)  # noqa: E731
+    assert lib.qw_gemm_add_rmsnorm(*ga(1024, 2048, 2, fake, L.QW_F32)) == L.QW_ERR_DTYPE
+    assert lib.qw_gemm_add_rmsnorm(*ga(1000, 2048, 2, fake, L.QW_BF16)) == L.QW_ERR_SHAPE
+    assert lib.qw_gemm_add_rmsnorm(*ga(4096, 2048, 2, fake, L.QW_BF16)) == L.QW_ERR_SHAPE
+    assert lib.qw_gemm_add_rmsnorm(*ga(1024, 2052, 2, fake, L.QW_BF16)) == L.QW_ERR_SHAPE
+    assert lib.qw_gemm_add_rmsnorm(*ga(1024, 2048, 2, C.c_void_p(32), L.QW_BF16)) == L.QW_ERR_INVALID_ARG
     # sampler: bf16 only, V a multiple of 8, a workspace of the queried size
     assert lib.qw_sample(fake, 4, 151936, fake, fake, fake, fake, fake, 1 << 30, L.QW_F32, None) == L.QW_ERR_DTYPE
     assert lib.qw_sample(fake, 4, 100, fake, fake, fake, fake, fake, 1 << 30, L.QW_BF16, None) == L.QW_ERR_INVALID_ARG

@@ -754,3 +754,90 @@ def test_lm_head_with_last_token_select(L, tp, n_out):
     acc = 2.0 ** -18 * (np.abs(hidden.double().numpy()[last.numpy()]) @ np.abs(table.double().numpy()).T)
     assert_within_ulps(got, ref, 1.0, 0.9, "logits", atol=acc)
     assert np.array_equal(nt.cpu().numpy(), O.greedy(got))     # argmax of the kernel's own logits: exact
+
+
+@pytest.mark.parametrize("T,nh,nkv,tp", [(1, 16, 8, 2), (300, 16, 8, 2), (1000, 16, 8, 1), (257, 8, 8, 2),
+                                         (129, 32, 8, 2)])
+def test_qkv_gemm_epilogue_equals_two_step_path(L, T, nh, nkv, tp):
+    """qw_qkv_gemm_norm_rope_store_kv against qw_gemm + qw_qkv_norm_rope_store_kv:
+    q, both caches (NaN-poisoned rows left alone) and the error count identical
+    bit for bit, including invalid positions, slot -1 and out-of-range slots.
+    (The reference GEMM runs on at least 128 rows so that it takes the same
+    128 x 256 tile path, whose rows do not depend on one another.)"""
+    H, hd = 1024, 128
+    N = (nh + 2 * nkv) * hd
+    A = si.normal(0, f"qe.{T}.{nh}.a", (T, H), 1.0, "bf16")
+    W = dev(si.normal(0, f"qe.{T}.{nh}.w", (N, H), 0.05, "bf16"))
+    qg = dev((si.normal(0, f"qe.{T}.qg", (hd,), 0.2, "f32") + 1.0).to(torch.bfloat16))
+    kg = dev((si.normal(0, f"qe.{T}.kg", (hd,), 0.2, "f32") + 1.0).to(torch.bfloat16))
+    max_pos = 4096
+    pos = si.uniform_int(0, f"qe.{T}.pos", (T,), 0, max_pos)
+    slots = torch.randperm(T + 10, generator=torch.Generator().manual_seed(T))[:T].to(torch.int64)
+    if T > 4:
+        pos[1], pos[3] = -1, max_pos + 7          # invalid positions: q row zero, nothing stored
+        slots[2], slots[4] = -1, T + 10 + 3       # not stored; out of range (counted)
+    cs = L.rope_cos_sin_table(max_pos, hd, 1e6).cuda()
+    num_slots = T + 10
+    caches = [torch.full((num_slots, nkv, hd), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    q1 = torch.full((T, nh * hd), 5.0, dtype=torch.bfloat16, device="cuda")
+    q2 = q1.clone()
+    e1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    e2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # reference: the two calls
+    Tp = max(T, 128)
+    Ap = torch.zeros(Tp, H, dtype=torch.bfloat16)
+    Ap[:T] = A
+    qkv = torch.empty(Tp, N, dtype=torch.bfloat16, device="cuda")
+    L.gemm(dev(Ap), W, qkv, N, tp, L.QW_GEMM_COLUMN, L.QW_EPI_NONE)
+    L.qkv_norm_rope_store_kv(qkv[:T], nh, nkv, hd, tp, dev(pos), cs, qg, kg, 1e-6, dev(slots), caches[0], caches[1],
+                             q1, e1)
+    # fused
+    L.qkv_gemm_norm_rope_store_kv(dev(A), W, nh, nkv, hd, tp, dev(pos), cs, qg, kg, 1e-6, dev(slots), caches[2],
+                                  caches[3], q2, e2)
+    sync_ok(L)
+    assert torch.equal(q1.view(torch.int16), q2.view(torch.int16))
+    assert torch.equal(caches[0].view(torch.int16), caches[2].view(torch.int16))
+    assert torch.equal(caches[1].view(torch.int16), caches[3].view(torch.int16))
+    assert int(e1.item()) == int(e2.item()) == (3 if T > 4 else 0)   # two positions, one slot
+
+
+@pytest.mark.parametrize("M,N,K,tp", [(1, 1024, 2048, 2), (300, 1024, 2048, 2), (130, 1024, 3072, 2),
+                                      (200, 512, 1024, 1), (257, 2048, 1024, 4)])
+def test_gemm_add_rmsnorm(L, M, N, K, tp):
+    """Row-parallel GEMM + residual add + RMSNorm in one launch, against the two
+    calls it replaces (qw_gemm ROW_REDUCE on at least 128 rows, the same tile
+    path, then qw_add_rmsnorm) and against the oracle.  The new residual is the
+    same bits; y rounds a sum of squares taken in another order, so it may sit
+    one bf16 step away where it lies next to a rounding midpoint."""
+    A = si.normal(0, f"gar.{M}.{N}.a", (M, K), 1.0, "bf16")
+    Wf = si.normal(0, f"gar.{M}.{N}.w", (N, K), 0.05, "bf16")           # checkpoint [N, K]
+    W = torch.stack([Wf[:, r * (K // tp):(r + 1) * (K // tp)] for r in range(tp)]).contiguous()
+    R = si.normal(0, f"gar.{M}.{N}.r", (M, N), 1.0, "bf16")
+    g = (si.normal(0, f"gar.{M}.{N}.g", (N,), 0.1, "f32") + 1.0).to(torch.bfloat16)
+    eps = 1e-6
+    res = dev(R.clone())
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    L.gemm_add_rmsnorm(dev(A), dev(W), res, dev(g), eps, y, tp)
+    # the two calls, on a copy padded to 128 rows
+    Mp = max(M, 128)
+    Ap = torch.zeros(Mp, K, dtype=torch.bfloat16)
+    Ap[:M] = A
+    o = torch.empty(Mp, N, dtype=torch.bfloat16, device="cuda")
+    L.gemm(dev(Ap), dev(W), o, N, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE)
+    res2 = dev(R.clone())
+    y2 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    L.add_rmsnorm(o[:M], res2, res2, dev(g), eps, y2)
+    sync_ok(L)
+    assert torch.equal(res.view(torch.int16), res2.view(torch.int16))
+    assert_within_ulps(to_np(y), to_np(y2), 1.0, 0.99, "y vs two calls")
+    # the oracle: o = row-parallel linear (one rounding), then add_rms_forward
+    xs = [A.double().numpy()[:, r * (K // tp):(r + 1) * (K // tp)] for r in range(tp)]
+    o_ref = O.row_parallel_linear(xs, Wf.double().numpy(), tp, "bf16")
+    y_ref, s_ref = O.add_rms_norm(o_ref, R.double().numpy(), g.double().numpy(), eps, "bf16")
+    acc = 2.0 ** -18 * (np.abs(A.double().numpy()) @ np.abs(Wf.double().numpy()).T)
+    assert_within_ulps(to_np(res), s_ref, 1.0, 0.95, "residual", atol=acc + bf16_ulp(o_ref))
+    # y = s * inv * gamma: a residual one step of o away (o and r can nearly cancel) moves
+    # y by that step times the row's 1/rms and gamma
+    inv = 1.0 / np.sqrt(np.mean(s_ref * s_ref, axis=1, keepdims=True) + eps)
+    slack = (acc + bf16_ulp(o_ref)) * inv * np.abs(g.double().numpy())[None, :]
+    assert_within_ulps(to_np(y), y_ref, 2.0, 0.95, "y", atol=slack + 2.0 ** -9)
