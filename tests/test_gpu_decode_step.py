@@ -4,8 +4,9 @@ against the per-operation entry points (needs a GB300).
 Shapes vary what the kernel partitions differently: GQA group sizes 1, 2
 and 4, one and two tp shards, batches of 1, 5 and 16 tokens, contexts from
 a single key (the token itself) to several attention chunks.  Tolerances
-are those of tests/test_gpu_model.py (bf16 models against the oracle's own
-bf16-softmax sensitivity).
+are those of tests/test_gpu_model.py (the stated bf16 bound, or twice the
+model's fp32-accumulation noise floor where that is higher; argmax agreement
+on decisive rows).
 """
 import numpy as np
 import pytest
@@ -14,8 +15,8 @@ import torch
 import oracle as O
 import seeded_inputs as si
 from tests._util import assert_within_ulps, to_np
-from tests.model_parity import bf16_softmax_weights, forced_tokens, run_gpu, run_oracle
-from tests.test_gpu_model import check_bf16_step
+from tests.model_parity import forced_tokens, run_gpu, run_oracle
+from tests.test_gpu_model import Parity, check_bf16_step
 
 pytestmark = pytest.mark.gpu
 
@@ -47,13 +48,11 @@ def test_decode_step_against_oracle(case):
     fwds = []
     g = run_gpu(m, seq_lens, steps, forced=forced, fused_decode=True, fwd_out=fwds)
     assert fwds[0].fused_decode_ok(len(seq_lens)), "the fused path must be the one under test"
-    w = O.load_weights(m)
-    o = run_oracle(m, seq_lens, steps, forced=forced, weights=w)
-    with bf16_softmax_weights():
-        n = run_oracle(m, seq_lens, steps, forced=forced, weights=w)
+    o = run_oracle(m, seq_lens, steps, forced=forced, weights=O.load_weights(m))
+    par = Parity(f"fused2_{case}")
     for s in range(1, steps + 1):
-        check_bf16_step(g.logits[s], o.logits[s], g.hidden[s], o.hidden[s], n.logits[s], n.hidden[s],
-                        f"{case} step {s}")
+        check_bf16_step(g.logits[s], o.logits[s], g.hidden[s], o.hidden[s], f"{case} step {s}", par)
+    par.check()
 
 
 def test_decode_step_matches_per_operation_path():

@@ -2,16 +2,22 @@
 
 * embedding + lm_head, vocab 151936 x 1024, 8192 tokens: the embedding is
   compared bit for bit on every row at 1/2/4 shards; the full [8192, 151936]
-  logits on sampled rows (the oracle recomputes those rows one by one).
+  logits on 64 rows spread over the batch (the oracle recomputes those rows).
 * the 28-layer decode step for 64 sequences with synthetic cache history:
-  sampled sequences (shortest, longest, one in between) through the oracle.
-* the 28-layer two-shard model, prefill 8 x 2048 then 128 decode steps:
-  sequence 0 through the oracle with the same forced decode inputs, every
-  step compared; and the bench's CUDA-graph path (greedy feedback on the
-  device) equal bit for bit to the same kernels launched one by one.
+  every sequence through the oracle.
+* the 28-layer two-shard model, prefill 8 x 2048 then 128 decode steps with
+  forced decode inputs:
+  - every sequence at the prefill and at decode steps 0, 63 and 127, the
+    oracle running each sequence's 2048 prompt tokens plus its 128 forced
+    tokens as one causal prefill (position 2048 + t of it is decode step t);
+  - sequence 0 at every step through the oracle's own decode path;
+  - the bench's CUDA-graph path (greedy feedback on the device) equal bit for
+    bit to the same kernels launched one by one.
 
-Tolerances are those of tests/test_gpu_model.py (bf16 models, measured
-against the oracle's own sensitivity to bf16 softmax weights).
+Tolerances are those of tests/test_gpu_model.py: the stated 2e-2, or twice the
+model's fp32-accumulation noise floor over the same rows where that is
+higher (28 layers of random-init weights: about 0.1 on the decode logits),
+and greedy argmax agreement on at least 99 % of the decisive rows.
 """
 import numpy as np
 import pytest
@@ -20,8 +26,8 @@ import torch
 import oracle as O
 import seeded_inputs as si
 from tests._util import assert_within_ulps, to_np
-from tests.model_parity import bf16_softmax_weights, forced_tokens
-from tests.test_gpu_model import check_bf16_step
+from tests.model_parity import forced_tokens, oracle_decode_layerwise, oracle_prefill_layerwise
+from tests.test_gpu_model import Parity, check_bf16_step
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -55,7 +61,12 @@ def test_embed_and_lm_head_full_size(oracle_weights):
         assert int(err.item()) == 0
         assert np.array_equal(to_np(out), O.vocab_parallel_embedding(ids.numpy(), tab64, tp)), tp
     hidden = si.normal(0, "embed_lm_head.hidden", (w.n_tokens, m.hidden), 1.0, "bf16")
-    rows = np.array([0, 1, 127, 128, 4095, 4096, 8000, 8191])
+    # 64 rows: both ends, the 128-row tile edges near them and rows spread over the batch
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 8063, 8064, 8190, 8191],
+                                     np.linspace(2, 8189, 56).astype(np.int64)]))
+    assert len(rows) == 64
+    h = hidden.double().numpy()[rows]
+    acc = 2.0 ** -18 * (np.abs(h) @ np.abs(tab64).T)
     for tp in w.tps:
         logits = torch.empty(w.n_tokens, m.vocab, dtype=torch.bfloat16, device="cuda")
         ws = torch.zeros(L.lm_head_workspace_size(w.n_tokens, m.vocab, m.hidden, tp, torch.bfloat16),
@@ -63,37 +74,9 @@ def test_embed_and_lm_head_full_size(oracle_weights):
         L.lm_head(hidden.cuda(), None, w.n_tokens, table, tp, logits, None, ws)
         torch.cuda.synchronize()
         L.device_error()
-        h = hidden.double().numpy()[rows]
         ref = O.compute_logits(m.replace(tp=tp), tab64, h, tp)
         got = to_np(logits[torch.from_numpy(rows).cuda()])
-        acc = 2.0 ** -18 * (np.abs(h) @ np.abs(tab64).T)
         assert_within_ulps(got, ref, 1.0, 0.9, f"lm_head tp{tp}", atol=acc)
-
-
-def _decode_fullsize_oracle(m, ow, b_idx, ctx_lens):
-    """Oracle decode step for the sequences b_idx (each alone, with its own cache history)."""
-    cos_sin = O.rope_cos_sin(m.max_position, m.head_dim, m.rope_theta)
-    batch = si.decode_batch(m, ctx_lens)
-    outs = []
-    for b in b_idx:
-        L = ctx_lens[b]
-        gslots = torch.arange(int(batch.seq_base[b]), int(batch.seq_base[b]) + L - 1, dtype=torch.int64)
-        hist = [(si.kv_history(m, l, "k", gslots).double().numpy(), si.kv_history(m, l, "v", gslots).double().numpy())
-                for l in range(m.n_layers)]
-        ctx = O.AttnContext(False, np.array([L - 1]), seq_base=np.array([0]), context_lens=np.array([L]))
-        res = []
-        for rounded in (False, True):
-            cache = O.KVCache(m.n_layers, L, m.n_kv_heads, m.head_dim, m.tp)
-            for l in range(m.n_layers):
-                cache.k[0][l][:L - 1], cache.v[0][l][:L - 1] = hist[l]
-            if rounded:
-                with bf16_softmax_weights():
-                    h = O.model_forward(m, ow, batch.ids.numpy()[b:b + 1], np.array([L - 1]), ctx, cache, cos_sin)
-            else:
-                h = O.model_forward(m, ow, batch.ids.numpy()[b:b + 1], np.array([L - 1]), ctx, cache, cos_sin)
-            res += [h[0], O.compute_logits(m, ow.embed, h, m.tp)[0]]
-        outs.append(tuple(res))
-    return outs
 
 
 def test_model_decode_64_sequences_full_size(oracle_weights):
@@ -118,12 +101,27 @@ def test_model_decode_64_sequences_full_size(oracle_weights):
     logits, _ = fwd.compute_logits(h, None, w.batch)
     torch.cuda.synchronize()
     L.device_error()
-    order = np.argsort(ctx_lens)
-    picks = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
     gh, gl = to_np(h), to_np(logits)
-    for b, (oh, ol, nh, nl) in zip(picks, _decode_fullsize_oracle(m, oracle_weights, picks, ctx_lens)):
-        check_bf16_step(gl[b:b + 1], ol[None], gh[b:b + 1], oh[None], nl[None], nh[None],
-                        f"seq {b} ctx {ctx_lens[b]}")
+    del fwd, kc, vc
+    torch.cuda.empty_cache()
+
+    def history(l):
+        # the seeded history generator, evaluated on the device for speed (its
+        # values are bit-identical on CPU and GPU), then placed at its slots
+        k = np.zeros((batch.num_slots, m.n_kv_heads, m.head_dim))
+        v = np.zeros_like(k)
+        rows = hist.cpu().numpy()
+        k[rows] = si.kv_history(m, l, "k", hist).double().cpu().numpy()
+        v[rows] = si.kv_history(m, l, "v", hist).double().cpu().numpy()
+        return k, v
+
+    oh, ol = oracle_decode_layerwise(m, oracle_weights, batch.ids.numpy(), batch.positions.numpy(),
+                                     batch.context_lens.numpy(), batch.slot_mapping.numpy(),
+                                     batch.seq_base.numpy(), batch.num_slots, history)
+    par = Parity("model_decode_64")
+    for b in range(w.batch):
+        check_bf16_step(gl[b:b + 1], ol[b:b + 1], gh[b:b + 1], oh[b:b + 1], f"seq {b} ctx {ctx_lens[b]}", par)
+    par.check()
 
 
 def test_model_prefill_decode_full_size(oracle_weights):
@@ -137,16 +135,16 @@ def test_model_prefill_decode_full_size(oracle_weights):
     forced = forced_tokens(m, S, B)
     hid, log = [], []
     h = fwd.run_layers(wl.pctx, decode=False)
-    hid.append(h[wl.pctx.last_idx.long()].clone())
+    hid.append(to_np(h[wl.pctx.last_idx.long()]))
     lg, nt = fwd.compute_logits(h, wl.pctx.last_idx, B)
-    log.append(lg.clone())
+    log.append(to_np(lg))
     greedy0 = nt.clone()
     for s in range(S):
         ctx = M.DecodeContext(forced[s].cuda(), wl.dpos[s], wl.dcl[s], wl.dslots[s], wl.dbase, wl.max_context)
         h = fwd.run_layers(ctx, decode=True)
-        hid.append(h.clone())
+        hid.append(to_np(h))
         lg, _ = fwd.compute_logits(h, None, B)
-        log.append(lg.clone())
+        log.append(to_np(lg))
     torch.cuda.synchronize()
     L.device_error()
     # (2) the bench's graphs (greedy feedback) against the same kernels launched eagerly
@@ -165,28 +163,36 @@ def test_model_prefill_decode_full_size(oracle_weights):
         eager.append(nt.clone())
     torch.cuda.synchronize()
     assert torch.equal(torch.stack(eager), gen_graph)
-    # (3) sequence 0 through the oracle with the same forced inputs
-    ow = oracle_weights
-    L0 = seq_lens[0]
-    ids0 = si.prefill_batch(m, seq_lens, extra_capacity=S).ids.numpy()[:L0]
-    cos_sin = O.rope_cos_sin(m.max_position, m.head_dim, m.rope_theta)
+    del wl, fwd
+    torch.cuda.empty_cache()
 
-    def run():
-        cache = O.KVCache(m.n_layers, L0 + S, m.n_kv_heads, m.head_dim, m.tp)
-        ctx = O.AttnContext(True, np.arange(L0), cu_seqlens=np.array([0, L0]))
-        hh = O.model_forward(m, ow, ids0, np.arange(L0), ctx, cache, cos_sin)
-        out_h = [hh[-1]]
-        out_l = [O.compute_logits(m, ow.embed, hh, m.tp, np.array([0, L0]))[0]]
-        for s in range(S):
-            pos = L0 + s
-            dctx = O.AttnContext(False, np.array([pos]), seq_base=np.array([0]), context_lens=np.array([pos + 1]))
-            hh = O.model_forward(m, ow, forced[s].numpy()[:1], np.array([pos]), dctx, cache, cos_sin)
-            out_h.append(hh[0])
-            out_l.append(O.compute_logits(m, ow.embed, hh, m.tp)[0])
-        return out_h, out_l
-    oh, ol = run()
-    with bf16_softmax_weights():
-        nh, nl = run()
-    for s in range(S + 1):
-        check_bf16_step(to_np(log[s][0:1]), ol[s][None], to_np(hid[s][0:1]), oh[s][None], nl[s][None], nh[s][None],
-                        f"step {s}")
+    ow = oracle_weights
+    prompt = si.prefill_batch(m, seq_lens, extra_capacity=S).ids.numpy()
+    cu = np.concatenate([[0], np.cumsum(seq_lens)])
+    par = Parity("model_prefill_decode")
+    # (3) every sequence: prompt + forced tokens as one causal prefill; its rows
+    # at the last prompt token and at decode steps 0, 63 and 127
+    steps = [0, 63, 127]
+    ids = np.concatenate([np.concatenate([prompt[cu[b]:cu[b + 1]], forced[:, b].numpy()]) for b in range(B)])
+    lens = [L0 + S for L0 in seq_lens]
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    rows = np.array([starts[b] + seq_lens[b] - 1 + k for b in range(B) for k in [0] + [1 + t for t in steps]])
+    oh, ol = oracle_prefill_layerwise(m, ow, ids, lens, rows)
+    for i, (b, k) in enumerate((b, k) for b in range(B) for k in [0] + [1 + t for t in steps]):
+        what = f"seq {b} " + ("prefill" if k == 0 else f"decode step {k - 1}")
+        check_bf16_step(log[k][b:b + 1], ol[i:i + 1], hid[k][b:b + 1], oh[i:i + 1], what, par)
+    # (4) sequence 0 at every step through the oracle's decode path
+    L0 = seq_lens[0]
+    cos_sin = O.rope_cos_sin(m.max_position, m.head_dim, m.rope_theta)
+    cache = O.KVCache(m.n_layers, L0 + S, m.n_kv_heads, m.head_dim, m.tp)
+    ctx = O.AttnContext(True, np.arange(L0), cu_seqlens=np.array([0, L0]))
+    hh = O.model_forward(m, ow, prompt[:L0], np.arange(L0), ctx, cache, cos_sin)
+    check_bf16_step(log[0][0:1], O.compute_logits(m, ow.embed, hh, m.tp, np.array([0, L0])), hid[0][0:1],
+                    hh[-1:], "seq 0 prefill (decode path)", par)
+    for s in range(S):
+        pos = L0 + s
+        dctx = O.AttnContext(False, np.array([pos]), seq_base=np.array([0]), context_lens=np.array([pos + 1]))
+        hh = O.model_forward(m, ow, forced[s].numpy()[:1], np.array([pos]), dctx, cache, cos_sin)
+        check_bf16_step(log[s + 1][0:1], O.compute_logits(m, ow.embed, hh, m.tp), hid[s + 1][0:1], hh,
+                        f"seq 0 decode step {s} (decode path)", par)
+    par.check()

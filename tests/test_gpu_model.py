@@ -1,29 +1,30 @@
 """End-to-end parity of the CUDA forward pass with the oracle (needs a GB300).
 
-Tolerances (from the stated targets, read as explained here):
+Tolerances (the stated targets, read as explained here):
   * fp32 model: normwise relative error <= 1e-4 on the final hidden state and
     the logits (max |g - o| / max |o| per tensor).
-  * bf16 models: |g - o| <= B + ulp(o) on the logits, where ulp(o) is the
-    bf16 spacing at the oracle's value (the last rounding to bf16, taken
-    independently on both sides, may land one step apart) and the budget
-    B = max(2e-2, 2 * S).  S is the model's own bf16 sensitivity, measured
-    in the test: the largest change of the oracle's output when the only
-    change to it is rounding the softmax weights P to bf16 before the PV
-    product, which every flash-style tensor-core kernel does.  On random-
-    init weights that change alone reaches 0.026 on the logits 3 layers
-    deep and 0.14 at 28 layers, above the 2e-2 target, so the target cannot
-    be met literally by any bf16 flash-attention kernel.  The bulk of the
-    error must match the noise floor closely: mean absolute errors at most
-    max(one bf16 ulp at 1.0 (7.8e-3), 1.25x the sensitivity's mean).  The
-    maximum over ~1.5e5 logits is a tail statistic of the same noise; the
-    logits are projections of one perturbed 1024-wide hidden state, so the
-    maxima of two noise draws differ by tens of percent even when their
-    means agree (28 layers: means 7.05e-3 vs 6.77e-3, maxima 0.055 vs
-    0.039): hence 2x on the maximum.
-    On the final hidden state (RMS 1, |x| up to ~5) the same rule applies
-    with the 2e-2 relative to max(1, |o|).
-    Greedy argmax agreement >= 99 %, every disagreement a near-tie (the
-    oracle's logits of the two tokens within the logit tolerance).
+  * one bf16 layer: max |g - o| <= 2e-2 relative to max(1, |o|) plus ulp(o),
+    the bf16 spacing at the oracle's value (the last rounding to bf16, taken
+    independently on both sides, may land one step apart).
+  * multi-layer bf16 models: the stated 2e-2 on logits (2e-2 relative to
+    max(1, |o|) on the final hidden state), unless the model's own noise
+    floor is above it.  The floor is the oracle's deviation from itself when
+    its Linear products are accumulated in fp32, as every tensor-core GEMM
+    accumulates them (tests/golden/noise_floor.py writes it, from the oracle
+    alone, into tests/golden/noise_floor.json for exactly the rows each test
+    compares).  On these random-init models a single bf16 value rounded the
+    other way changes the RMS of its row, which flips the rounding of other
+    normalised values, so any fp32-accumulating implementation lands on the
+    floor after a few layers (28 layers: about 0.1 max on the 64-sequence
+    decode logits).  The bound is then twice the floor's maximum (a maximum
+    over a few hundred rows is a tail statistic: two implementations with
+    equal means differ there by tens of percent), plus ulp(o); the mean
+    |g - o| over the test's rows must stay within max(2^-8, 2 x the floor's
+    mean).
+  * greedy argmax: agreement with the oracle on at least 99 % of the
+    decisive rows, those whose oracle top-2 logit gap exceeds the logit
+    bound; on the others (near-ties at that tolerance) either token is a
+    correct greedy choice.  The raw agreement is printed beside the floor's.
 """
 import numpy as np
 import pytest
@@ -31,8 +32,11 @@ import torch
 
 import oracle as O
 import seeded_inputs as si
+import json
+import os
+
 from tests._util import bf16_ulp, normwise_rel_err
-from tests.model_parity import argmax_agreement, bf16_softmax_weights, forced_tokens, run_gpu, run_oracle
+from tests.model_parity import forced_tokens, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -86,31 +90,76 @@ def test_small_bf16_model_prefill_and_decode(tp, fused):
     steps = 3
     forced = forced_tokens(m, steps, len(seq_lens))
     g = run_gpu(m, seq_lens, steps, forced=forced, fused_decode=fused)
-    w = O.load_weights(m)
-    o = run_oracle(m, seq_lens, steps, forced=forced, weights=w)
-    with bf16_softmax_weights():
-        n = run_oracle(m, seq_lens, steps, forced=forced, weights=w)
+    o = run_oracle(m, seq_lens, steps, forced=forced, weights=O.load_weights(m))
+    par = Parity(f"small3_tp{tp}")
     for s in range(steps + 1):
-        check_bf16_step(g.logits[s], o.logits[s], g.hidden[s], o.hidden[s], n.logits[s], n.hidden[s], f"step {s}")
+        check_bf16_step(g.logits[s], o.logits[s], g.hidden[s], o.hidden[s], f"step {s}", par)
+    par.check()
 
 
-def check_bf16_step(gl, ol, gh, oh, nl, nh, what):
-    """gl/gh: CUDA logits/hidden; ol/oh: oracle; nl/nh: oracle with bf16 softmax weights."""
-    dl = _report(f"{what} logits", gl, ol)
-    dh = _report(f"{what} hidden", gh, oh)
-    sl = np.abs(nl - ol)
-    sh = np.abs(nh - oh)
-    print(f"{what} sensitivity: logits max {sl.max():.3e} mean {sl.mean():.3e}; hidden max {sh.max():.3e} "
-          f"mean {sh.mean():.3e}")
-    bl = max(LOGIT_TOL, 2.0 * float(sl.max()))
-    bh = max(LOGIT_TOL, 2.0 * float(sh.max()))
-    assert np.all(dl <= bl + bf16_ulp(ol)), what
-    assert np.all(dh <= bh * np.maximum(1.0, np.abs(oh)) + bf16_ulp(oh)), what
-    assert dl.mean() <= max(2.0 ** -7, 1.25 * sl.mean()), what
-    assert dh.mean() <= max(2.0 ** -7, 1.25 * sh.mean()), what
-    agree, bad = argmax_agreement(gl, ol, bl + float(bf16_ulp(np.abs(ol).max())))
-    assert len(bad) == 0, what
-    return agree
+NOISE_FLOOR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "noise_floor.json")
+
+
+class Parity:
+    """Tolerances of one test's bf16 model comparison, and its population statistics.
+
+    floor: name of the workload in tests/golden/noise_floor.json, or None for
+    the literal bound."""
+
+    def __init__(self, floor=None):
+        self.floor = None
+        self.logits = self.hidden = LOGIT_TOL
+        self.mean_logits = self.mean_hidden = 2.0 ** -8
+        if floor is not None:
+            with open(NOISE_FLOOR) as f:
+                self.floor = json.load(f)["workloads"][floor]
+            self.logits = max(LOGIT_TOL, 2.0 * self.floor["logits_max"])
+            self.hidden = max(LOGIT_TOL, 2.0 * self.floor["hidden_max"])
+            self.mean_logits = max(self.mean_logits, 2.0 * self.floor["logits_mean"])
+            self.mean_hidden = max(self.mean_hidden, 2.0 * self.floor["hidden_mean"])
+        self.rows = self.same = self.decisive = self.decisive_same = 0
+        self.sum_l = self.sum_h = 0.0
+        self.n_l = self.n_h = 0
+
+    def add(self, gl, ol, gh, oh):
+        dl, dh = np.abs(gl - ol), np.abs(gh - oh)
+        self.sum_l += float(dl.sum())
+        self.n_l += dl.size
+        self.sum_h += float(dh.sum())
+        self.n_h += dh.size
+        g, o = O.greedy(gl), O.greedy(ol)
+        rows = np.arange(len(g))
+        top2 = np.sort(ol, axis=-1)[:, -2:]
+        decisive = (top2[:, 1] - top2[:, 0]) > self.logits + bf16_ulp(top2[:, 1])
+        self.rows += len(g)
+        self.same += int(np.sum(g == o))
+        self.decisive += int(np.sum(decisive))
+        self.decisive_same += int(np.sum((g == o) & decisive))
+        return dl, dh, g, o, rows
+
+    def check(self):
+        fl = self.floor or {}
+        print(f"argmax agreement {self.same}/{self.rows}, decisive rows {self.decisive_same}/{self.decisive}"
+              f" (floor's agreement {fl.get('argmax_agreement', 'n/a')}); mean |err| logits "
+              f"{self.sum_l / max(self.n_l, 1):.3e} (bound {self.mean_logits:.3e}), hidden "
+              f"{self.sum_h / max(self.n_h, 1):.3e} (bound {self.mean_hidden:.3e})")
+        assert self.decisive_same >= 0.99 * self.decisive, "argmax agreement on decisive rows below 99 %"
+        assert self.sum_l / max(self.n_l, 1) <= self.mean_logits
+        assert self.sum_h / max(self.n_h, 1) <= self.mean_hidden
+
+
+def check_bf16_step(gl, ol, gh, oh, what, par: Parity):
+    """gl/gh: CUDA logits/hidden; ol/oh: oracle.  Every element within the bound;
+    every argmax disagreement a near-tie within the logit bound."""
+    _report(f"{what} logits", gl, ol)
+    _report(f"{what} hidden", gh, oh)
+    dl, dh, g, o, rows = par.add(gl, ol, gh, oh)
+    assert np.all(dl <= par.logits + bf16_ulp(ol)), (what, float(dl.max()), par.logits)
+    hb = np.maximum(LOGIT_TOL * np.maximum(1.0, np.abs(oh)), par.hidden)
+    assert np.all(dh <= hb + bf16_ulp(oh)), (what, float(dh.max()), par.hidden)
+    gap = ol[rows, o] - ol[rows, g]
+    bad = (g != o) & (gap > par.logits + bf16_ulp(np.abs(ol).max(axis=-1)))
+    assert not bad.any(), (what, np.nonzero(bad)[0], gap[bad])
 
 
 def test_single_layer_prefill_full_size():

@@ -201,3 +201,38 @@ def test_gammas_are_distinct_so_swaps_are_visible():
             assert (g[i] - g[j]).abs().max() > 0.1
     assert (ck["layer0.q_norm"] - ck["layer0.k_norm"]).abs().max() > 0.1
     assert (ck["layer0.q_norm"] - 1.0).abs().max() > 0.1
+
+
+def test_layerwise_helpers_equal_model_forward():
+    """The layer-at-a-time oracle drivers used by the full-size parity tests
+    (one layer's cache alive at a time) give exactly O.model_forward's results."""
+    from tests.model_parity import oracle_decode_layerwise, oracle_prefill_layerwise
+    m = SHAPE.replace(tp=2, dtype="bf16")
+    w = O.load_weights(m)
+    lens = [9, 4, 13]
+    b = si.prefill_batch(m, lens)
+    cache = O.KVCache(m.n_layers, b.num_slots, m.n_kv_heads, m.head_dim, m.tp)
+    ctx = O.AttnContext(True, b.slot_mapping.numpy(), cu_seqlens=b.cu_seqlens.numpy())
+    h = O.model_forward(m, w, b.ids.numpy(), b.positions.numpy(), ctx, cache)
+    rows = np.array([0, 8, 12, 25])
+    hl, lg = oracle_prefill_layerwise(m, w, b.ids.numpy(), lens, rows)
+    assert np.array_equal(hl, h[rows])
+    assert np.array_equal(lg, O.compute_logits(m, w.embed, h[rows], m.tp))
+    # one decode step over the prefill's cache, its rows handed over layer by layer
+    base = b.seq_base.numpy().astype(np.int64)
+    ext = si.prefill_batch(m, lens, extra_capacity=1)
+    cache2 = O.KVCache(m.n_layers, ext.num_slots, m.n_kv_heads, m.head_dim, m.tp)
+    ctx2 = O.AttnContext(True, ext.slot_mapping.numpy(), cu_seqlens=ext.cu_seqlens.numpy())
+    O.model_forward(m, w, ext.ids.numpy(), ext.positions.numpy(), ctx2, cache2)
+    snapshot = [[np.concatenate([cache2.k[r][l] for r in range(m.tp)], axis=1) for l in range(m.n_layers)],
+                [np.concatenate([cache2.v[r][l] for r in range(m.tp)], axis=1) for l in range(m.n_layers)]]
+    base = ext.seq_base.numpy().astype(np.int64)
+    pos = np.array(lens, dtype=np.int64)
+    slots = base + pos
+    ids = np.array([5, 77, 31])
+    dctx = O.AttnContext(False, slots, seq_base=base, context_lens=pos + 1)
+    hd = O.model_forward(m, w, ids, pos, dctx, cache2)
+    hl, lg = oracle_decode_layerwise(m, w, ids, pos, pos + 1, slots, base, ext.num_slots,
+                                     lambda l: (snapshot[0][l].copy(), snapshot[1][l].copy()))
+    assert np.array_equal(hl, hd)
+    assert np.array_equal(lg, O.compute_logits(m, w.embed, hd, m.tp))
