@@ -88,7 +88,7 @@ typedef enum {
   QW_EPI_SILU_MUL = 1     /* fused SiluAndMul on a merged gate_up output ([SK] §4) */
 } qw_epilogue;
 
-/* Version of this ABI (increments on any signature change); this is version 8. */
+/* Version of this ABI (increments on any signature change); this is version 9. */
 int qw_abi_version(void);
 
 /* Description of the last failure on the calling thread ("" if none). */
@@ -358,24 +358,6 @@ int qw_attention_decode_static(const void* q, const void* k_cache, const void* v
                                int n_heads, int n_kv_heads, int head_dim, float scale, void* out, int dtype,
                                void* stream);
 size_t qw_attention_decode_static_scratch_bytes(void);
-
-/*
- * L2 prefetch of up to 8 device ranges: a hint, with no output and no effect
- * on any result.  It has no counterpart in the cited sources; it serves the decode step, whose
- * kernels each stream one weight matrix while the attention before them is
- * bound by the K/V stream.  Launched on a side stream while one layer's
- * attention runs, it warms the L2 cache with the weights the next kernels
- * read (o_proj, gate_up, down, the next layer's QKV).
- *   ptrs, sizes: HOST arrays of n device pointers and byte counts; each
- *                pointer 16-byte aligned, each size a multiple of 16 (a zero
- *                size is skipped).  0 <= n <= 8.  The library keeps neither
- *                array after the call.
- *   One small kernel; each 64 KB piece of the ranges is one bulk prefetch
- *   request.  The ranges must stay allocated until the kernel has run.
- * Errors: QW_ERR_INVALID_ARG for n outside [0, 8], a null array, a null or
- * misaligned pointer with a non-zero size, or a size not a multiple of 16.
- */
-int qw_prefetch_l2(const void* const* ptrs, const size_t* sizes, int n, void* stream);
 
 /*
  * Self-test of the failure path: launches one thread that waits on an

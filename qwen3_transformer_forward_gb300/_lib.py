@@ -58,7 +58,6 @@ SIGNATURES = {
     "qw_argmax": (C.c_int, [_p, _i64, _i64, _p, _i32, _p]),
     "qw_sample": (C.c_int, [_p, _i64, _i64, _p, _p, _p, _p, _p, _sz, _i32, _p]),
     "qw_sample_workspace_size": (C.c_size_t, [_i64, _i64]),
-    "qw_prefetch_l2": (C.c_int, [_p, _p, _i32, _p]),
     "qw_selftest_wait_timeout": (C.c_int, [_p]),
     "qw_add_rmsnorm_gemm": (C.c_int, [_p, _p, _p, _p, _f32, _p, _p, _i64, _i64, _i64, _i32, _i32, _i32, _p]),
     "qw_decode_layers": (C.c_int, [_p, _i32, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _p,
@@ -330,14 +329,6 @@ def sample(logits, temperature, top_p, uniforms, out, workspace, stream=None):
                             _dev_ptr(top_p, "top_p"), _dev_ptr(uniforms, "uniforms"), _dev_ptr(out, "out"),
                             _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
                             dtype_code(logits.dtype), _stream(stream)))
-
-
-def prefetch_l2(tensors, stream=None):
-    """L2 prefetch hint for the bytes of up to 8 CUDA tensors (no output)."""
-    n = len(tensors)
-    ptrs = (C.c_void_p * max(n, 1))(*[_dev_ptr(t, "tensor") for t in tensors])
-    sizes = (C.c_size_t * max(n, 1))(*[t.numel() * t.element_size() for t in tensors])
-    _check(load().qw_prefetch_l2(C.cast(ptrs, C.c_void_p), C.cast(sizes, C.c_void_p), n, _stream(stream)))
 
 
 def selftest_wait_timeout(stream=None):

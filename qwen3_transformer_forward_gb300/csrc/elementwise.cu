@@ -586,57 +586,3 @@ extern "C" int qw_argmax(const void* logits, int64_t M, int64_t V, int64_t* out,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return dtype == QW_BF16 ? launch_argmax<bf16>(logits, M, V, out, st) : launch_argmax<float>(logits, M, V, out, st);
 }
-
-// ---------------------------------------------------------------------------
-// L2 prefetch of weight ranges (a hint: no output).  Each CTA takes a strided
-// share of the 64 KB pieces, and its first thread issues one bulk prefetch per
-// piece; nothing waits for the data.
-// ---------------------------------------------------------------------------
-namespace qw {
-constexpr int kPrefetchMax = 8;
-constexpr uint64_t kPrefetchPiece = 64 * 1024;
-
-struct PrefetchRanges {
-  const uint8_t* p[kPrefetchMax];
-  uint64_t n[kPrefetchMax];
-  int count;
-};
-
-__global__ void __launch_bounds__(32) l2_prefetch_kernel(const PrefetchRanges r) {
-  if (threadIdx.x != 0) return;
-  for (int i = 0; i < r.count; ++i) {
-    const uint64_t pieces = (r.n[i] + kPrefetchPiece - 1) / kPrefetchPiece;
-    for (uint64_t j = blockIdx.x; j < pieces; j += gridDim.x) {
-      const uint64_t off = j * kPrefetchPiece;
-      const uint64_t left = r.n[i] - off;   // > 0, a multiple of 16
-      const uint32_t len = uint32_t(left < kPrefetchPiece ? left : kPrefetchPiece);
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(r.p[i] + off), "r"(len) : "memory");
-    }
-  }
-}
-}  // namespace qw
-
-extern "C" int qw_prefetch_l2(const void* const* ptrs, const size_t* sizes, int n, void* stream) {
-  if (n < 0 || n > kPrefetchMax) return set_error(QW_ERR_INVALID_ARG, "qw_prefetch_l2: n=%d outside [0, 8]", n);
-  if (n == 0) return QW_OK;
-  if (!ptrs || !sizes) return set_error(QW_ERR_INVALID_ARG, "qw_prefetch_l2: null host array");
-  PrefetchRanges r{};
-  uint64_t pieces = 0;
-  for (int i = 0; i < n; ++i) {
-    if (sizes[i] == 0) continue;
-    if (!ptrs[i] || !al16(ptrs[i]) || sizes[i] % 16)
-      return set_error(QW_ERR_INVALID_ARG, "qw_prefetch_l2: range %d null, misaligned or not a multiple of 16 bytes",
-                       i);
-    r.p[r.count] = static_cast<const uint8_t*>(ptrs[i]);
-    r.n[r.count] = sizes[i];
-    ++r.count;
-    pieces += (sizes[i] + kPrefetchPiece - 1) / kPrefetchPiece;
-  }
-  if (r.count == 0) return QW_OK;
-  int sms = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return set_error(QW_ERR_CUDA, "qw_prefetch_l2: no device");
-  const unsigned grid = unsigned(pieces < uint64_t(sms) ? pieces : uint64_t(sms));
-  l2_prefetch_kernel<<<grid, 32, 0, static_cast<cudaStream_t>(stream)>>>(r);
-  return check_launch("qw_prefetch_l2");
-}

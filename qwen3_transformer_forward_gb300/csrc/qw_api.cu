@@ -43,7 +43,7 @@ unsigned int take_dstep_errors();
 
 }  // namespace qw
 
-extern "C" int qw_abi_version(void) { return 8; }
+extern "C" int qw_abi_version(void) { return 9; }
 
 extern "C" const char* qw_last_error_string(void) { return qw::g_last_error.c_str(); }
 

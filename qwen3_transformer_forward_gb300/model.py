@@ -192,14 +192,12 @@ class Qwen3Forward:
         # folded KV store requires anyway)
         self._history_ready = True
         self._fused = None     # (layer table, workspace), built on first use
-        # decode: while layer l's attention streams its K/V, a side stream warms
-        # L2 with the weights read next (o_proj, gate_up, down of layer l and
-        # the next layer's QKV); off by default
-        self.l2_prefetch = False
-        self._pf_stream = None
-        # prefill in five kernels per layer: QK-norm + RoPE + KV store in the QKV GEMM's
-        # epilogue, residual add + RMSNorm in the o_proj and down GEMMs' epilogues
-        self.fused_prefill = True
+        # prefill in five kernels per layer (QK-norm + RoPE + KV store in the QKV GEMM's
+        # epilogue, residual add + RMSNorm in the o_proj and down GEMMs' epilogues);
+        # off by default: on GB300 the longer epilogues, run after each tile's
+        # mainloop with the tensor pipe idle, cost more than the kernels they
+        # replace (8 x 2048-token prefill: 25.1 ms fused, 21.8 ms unfused)
+        self.fused_prefill = False
 
     def _around(self, name: str, layer: int):
         if self.probe is None:
@@ -285,8 +283,6 @@ class Qwen3Forward:
                 L.add_rmsnorm(h, None if first else res, res, p.input_ln, m.eps, y, stream)
             with self._around(f"{ph}.gemm_qkv", l):
                 L.gemm(y, p.qkv, qkv, self.qkv_width, tp, L.QW_GEMM_COLUMN, L.QW_EPI_NONE, self.workspace, stream)
-        if decode and self.l2_prefetch:
-            self._prefetch_after_qkv(l, stream)
         q = self.q[:T]
         attn = self.attn[:T]
         if decode and self.dtype == torch.bfloat16 and m.head_dim == 128:
@@ -330,19 +326,6 @@ class Qwen3Forward:
                        self.workspace, stream)
         with self._around(f"{ph}.gemm_down", l):
             L.gemm(act, p.down, h, m.hidden, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, self.workspace, stream)
-
-    def _prefetch_after_qkv(self, l: int, stream):
-        """Forks the L2 prefetch of the weights after layer l's attention onto a
-        side stream; run_layers joins it at the end of the step."""
-        if stream is not None:
-            raise ValueError("l2_prefetch runs on the current stream only")
-        if self._pf_stream is None:
-            self._pf_stream = torch.cuda.Stream(device=self.device)
-        layers = self.p.layers
-        nxt = layers[(l + 1) % len(layers)]
-        self._pf_stream.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(self._pf_stream):
-            L.prefetch_l2([layers[l].o, layers[l].gate_up, layers[l].down, nxt.qkv])
 
     def fused_decode_ok(self, B: int) -> bool:
         m = self.m
@@ -401,8 +384,6 @@ class Qwen3Forward:
             return self.h[:T], self.res[:T]
         for l in range(nl):
             self._layer(l, T, ctx, l == 0, decode, stream)
-        if decode and self.l2_prefetch and self._pf_stream is not None:
-            torch.cuda.current_stream().wait_stream(self._pf_stream)
         nl = len(self.p.layers)
         res = self._res(2 * nl - 1, T) if decode and self.norm_fusion_ok(T) and nl > 0 else self.res[:T]
         if not final_norm:

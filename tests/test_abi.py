@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.qw_abi_version() == 8
+    assert lib.qw_abi_version() == 9
 
 
 def test_argument_errors_are_reported_before_launch(lib):
@@ -165,21 +165,3 @@ def test_workspace_sizes(lib):
     # max_context 0 (every sequence empty) still plans one key tile per pair
     assert L.attention_decode_workspace_size(8, 0, 16, 128) > 0
     assert L.attention_decode_workspace_size(8, -1, 16, 128) == 0
-
-
-def test_prefetch_l2_checks_its_ranges_on_the_host(lib):
-    """The L2 prefetch hint validates every range before its one launch; none of
-    these calls reaches the device."""
-    def call(ptrs, sizes, n):
-        pa = (C.c_void_p * max(len(ptrs), 1))(*ptrs)
-        sa = (C.c_size_t * max(len(sizes), 1))(*sizes)
-        return lib.qw_prefetch_l2(C.cast(pa, C.c_void_p), C.cast(sa, C.c_void_p), n, None)
-    assert call([], [], 0) == L.QW_OK                                       # nothing to do
-    assert call([16] * 9, [16] * 9, 9) == L.QW_ERR_INVALID_ARG                # more than 8 ranges
-    assert call([16], [16], -1) == L.QW_ERR_INVALID_ARG
-    assert lib.qw_prefetch_l2(None, None, 1, None) == L.QW_ERR_INVALID_ARG   # null host arrays
-    assert call([24], [64], 1) == L.QW_ERR_INVALID_ARG                        # misaligned pointer
-    assert call([32], [40], 1) == L.QW_ERR_INVALID_ARG                        # size not a multiple of 16
-    assert call([None], [64], 1) == L.QW_ERR_INVALID_ARG                      # null range
-    assert "qw_prefetch_l2" in lib.qw_last_error_string().decode()
-    assert call([None, 48], [0, 0], 2) == L.QW_OK                             # empty ranges are skipped
