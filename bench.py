@@ -724,6 +724,8 @@ def count_launches(wl):
         # embed, one add+RMSNorm, 5 per layer (QKV + norm/RoPE/KV store, attention, o_proj + add + norm,
         # gate_up + SiluAndMul, down + add + norm), gather + gemm + argmax
         prefill = 1 + 1 + m.n_layers * 5 + 3
+    elif wl.fwd.qkv_epilogue_ok():
+        prefill -= m.n_layers   # the QK-norm + RoPE + KV store runs in the QKV GEMM's epilogue
     lm_dec = 2                                       # gemm + argmax
     if wl.fwd.fused_decode_ok(wl.B):
         decode = 1 + 1 + lm_dec                      # embed, all layers in one kernel, lm_head

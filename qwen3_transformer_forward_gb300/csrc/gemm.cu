@@ -186,6 +186,98 @@ __device__ __forceinline__ float silu_mul_bf16(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
+// Epilogue of a QKV tile (EPI_QKV): the tile's 256 columns are two whole heads
+// of the merged QKV output (shard r = [q_r | k_r | v_r], 128 columns per
+// head).  Each thread owns one token row: it rounds the accumulator to the
+// bf16 QKV value, then a q or k head is normed, rotated and written (q_out /
+// k cache), a v head is copied into the v cache, with the arithmetic of the
+// standalone kernel.  trow: this thread's TMEM lane at the tile's column 0.
+__device__ __forceinline__ void epi_qkv_tile(const TcArgs& a, uint32_t trow, int64_t m, int tile_q, bool row_ok) {
+  constexpr int BN = 256;
+  int64_t pos = 0, slot = -1;
+  if (m < a.M) {
+    pos = a.positions[m];
+    slot = a.slots[m];
+  }
+  const bool pos_ok = pos >= 0 && pos < a.max_pos;
+  const int nh_l = a.nh / a.tp, nkv_l = a.nkv / a.tp;
+  const int64_t width_r = int64_t(nh_l + 2 * nkv_l) * 128;
+#pragma unroll 1
+  for (int hh = 0; hh < BN / 128; ++hh) {
+    const int64_t n0 = int64_t(tile_q) * BN + 128 * hh;
+    if (n0 >= a.N) break;   // uniform over the CTA
+    float x[128];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t r[32];
+      tmem_ld32(trow + uint32_t(128 * hh + 32 * c), r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[32 * c + e] = round_t<bf16>(__uint_as_float(r[e]));
+    }
+    if (!row_ok) continue;
+    const int shard = int(n0 / width_r);
+    const int loc = int((n0 % width_r) / 128);
+    if (loc < nh_l + nkv_l) {
+      const bool is_q = loc < nh_l;
+      const int hidx = is_q ? shard * nh_l + loc : shard * nkv_l + (loc - nh_l);
+      bf16* dst;
+      if (is_q) {
+        if (hidx == 0 && !pos_ok && a.err != nullptr) atomicAdd(a.err, 1);   // once per token
+        dst = a.q_out + (m * a.nh + hidx) * 128;
+      } else {
+        if (slot == -1) continue;                                           // padding: not stored
+        if (slot < 0 || slot >= a.num_slots) {
+          if (hidx == 0 && a.err != nullptr) atomicAdd(a.err, 1);
+          continue;
+        }
+        if (!pos_ok) continue;
+        dst = a.k_cache + (slot * a.nkv + hidx) * 128;
+      }
+      float part[8];
+#pragma unroll
+      for (int pp = 0; pp < 8; ++pp) {
+        float x1[8], x2[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          x1[e] = x[8 * pp + e];
+          x2[e] = x[64 + 8 * pp + e];
+        }
+        part[pp] = qk_ss8(x1, x2);
+      }
+      const float inv = qk_inv_rms(qk_ss_tree(part), a.eps);
+      const bf16* gamma = is_q ? a.q_gamma : a.k_gamma;
+      const float* cs = a.cos_sin + (pos_ok ? pos : 0) * 128;
+#pragma unroll
+      for (int pp = 0; pp < 8; ++pp) {
+        float g1[8], g2[8], cc[8], sn[8], y1[8], y2[8];
+        load16(gamma + 8 * pp, g1);
+        load16(gamma + 64 + 8 * pp, g2);
+        *reinterpret_cast<float4*>(cc) = *reinterpret_cast<const float4*>(cs + 8 * pp);
+        *reinterpret_cast<float4*>(cc + 4) = *reinterpret_cast<const float4*>(cs + 8 * pp + 4);
+        *reinterpret_cast<float4*>(sn) = *reinterpret_cast<const float4*>(cs + 64 + 8 * pp);
+        *reinterpret_cast<float4*>(sn + 4) = *reinterpret_cast<const float4*>(cs + 64 + 8 * pp + 4);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          qk_rope_pair(x[8 * pp + e], x[64 + 8 * pp + e], inv, g1[e], g2[e], cc[e], sn[e], pos_ok, y1[e], y2[e]);
+        store16(dst + 8 * pp, y1);
+        store16(dst + 64 + 8 * pp, y2);
+      }
+    } else {   // v head: the rounded QKV values, a bit copy into the cache
+      const int g = shard * nkv_l + (loc - nh_l - nkv_l);
+      if (slot < 0 || slot >= a.num_slots || !pos_ok) continue;
+      bf16* dst = a.v_cache + (slot * a.nkv + g) * 128;
+#pragma unroll
+      for (int v = 0; v < 16; ++v) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = x[8 * v + e];
+        store16(dst + 8 * v, f);
+      }
+    }
+  }
+}
+
 template <int BN>
 struct TileCfg {
   static constexpr uint32_t A_BYTES = BM * BK * 2;
@@ -399,94 +491,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         reinterpret_cast<float*>(sA)[quarter * 32 + lane] = ss;   // the ring is free: every MMA has completed
       } else if (EPI == EPI_QKV) {
-        // The tile's 256 columns are two whole heads of the merged QKV output
-        // (shard r = [q_r | k_r | v_r], 128 columns per head).  Each thread owns
-        // one token: it rounds the accumulator to the bf16 QKV value, then a q or
-        // k head is normed, rotated and written (q_out / k cache), a v head is
-        // copied into the v cache, with the arithmetic of the standalone kernel.
-        const bool row_ok = m < a.M && ok && has_acc;
-        int64_t pos = 0, slot = -1;
-        if (m < a.M) {
-          pos = a.positions[m];
-          slot = a.slots[m];
-        }
-        const bool pos_ok = pos >= 0 && pos < a.max_pos;
-        const int nh_l = a.nh / a.tp, nkv_l = a.nkv / a.tp;
-        const int64_t width_r = int64_t(nh_l + 2 * nkv_l) * 128;
-#pragma unroll 1
-        for (int hh = 0; hh < BN / 128; ++hh) {
-          const int64_t n0 = int64_t(tile_q) * BN + 128 * hh;
-          if (n0 >= a.N) break;   // uniform over the CTA
-          float x[128];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld32(trow + uint32_t(128 * hh + 32 * c), r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) x[32 * c + e] = round_t<bf16>(__uint_as_float(r[e]));
-          }
-          if (!row_ok) continue;
-          const int shard = int(n0 / width_r);
-          const int loc = int((n0 % width_r) / 128);
-          if (loc < nh_l + nkv_l) {
-            const bool is_q = loc < nh_l;
-            const int hidx = is_q ? shard * nh_l + loc : shard * nkv_l + (loc - nh_l);
-            bf16* dst;
-            if (is_q) {
-              if (hidx == 0 && !pos_ok && a.err != nullptr) atomicAdd(a.err, 1);   // once per token
-              dst = a.q_out + (m * a.nh + hidx) * 128;
-            } else {
-              if (slot == -1) continue;                                           // padding: not stored
-              if (slot < 0 || slot >= a.num_slots) {
-                if (hidx == 0 && a.err != nullptr) atomicAdd(a.err, 1);
-                continue;
-              }
-              if (!pos_ok) continue;
-              dst = a.k_cache + (slot * a.nkv + hidx) * 128;
-            }
-            float part[8];
-#pragma unroll
-            for (int pp = 0; pp < 8; ++pp) {
-              float x1[8], x2[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                x1[e] = x[8 * pp + e];
-                x2[e] = x[64 + 8 * pp + e];
-              }
-              part[pp] = qk_ss8(x1, x2);
-            }
-            const float inv = qk_inv_rms(qk_ss_tree(part), a.eps);
-            const bf16* gamma = is_q ? a.q_gamma : a.k_gamma;
-            const float* cs = a.cos_sin + (pos_ok ? pos : 0) * 128;
-#pragma unroll
-            for (int pp = 0; pp < 8; ++pp) {
-              float g1[8], g2[8], cc[8], sn[8], y1[8], y2[8];
-              load16(gamma + 8 * pp, g1);
-              load16(gamma + 64 + 8 * pp, g2);
-              *reinterpret_cast<float4*>(cc) = *reinterpret_cast<const float4*>(cs + 8 * pp);
-              *reinterpret_cast<float4*>(cc + 4) = *reinterpret_cast<const float4*>(cs + 8 * pp + 4);
-              *reinterpret_cast<float4*>(sn) = *reinterpret_cast<const float4*>(cs + 64 + 8 * pp);
-              *reinterpret_cast<float4*>(sn + 4) = *reinterpret_cast<const float4*>(cs + 64 + 8 * pp + 4);
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                qk_rope_pair(x[8 * pp + e], x[64 + 8 * pp + e], inv, g1[e], g2[e], cc[e], sn[e], pos_ok, y1[e], y2[e]);
-              store16(dst + 8 * pp, y1);
-              store16(dst + 64 + 8 * pp, y2);
-            }
-          } else {   // v head: the rounded QKV values, a bit copy into the cache
-            const int g = shard * nkv_l + (loc - nh_l - nkv_l);
-            if (slot < 0 || slot >= a.num_slots || !pos_ok) continue;
-            bf16* dst = a.v_cache + (slot * a.nkv + g) * 128;
-#pragma unroll
-            for (int v = 0; v < 16; ++v) {
-              float f[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) f[e] = x[8 * v + e];
-              store16(dst + 8 * v, f);
-            }
-          }
-        }
+        epi_qkv_tile(a, trow, m, tile_q, m < a.M && ok && has_acc);
       } else {  // EPI_SILU
         const int r_s = tile_q / a.silu_tps;
         const int64_t jl0 = int64_t(tile_q % a.silu_tps) * (BN / 2);
@@ -866,6 +871,8 @@ __global__ void __launch_bounds__(192, 1)
             }
           }
         }
+      } else if (EPI == EPI_QKV) {
+        epi_qkv_tile(a, trow, m, tile_q, m < a.M);
       } else {  // EPI_SILU: columns [0, 128) gate, [128, 256) up
         const int r_s = tile_q / a.silu_tps;
         const int64_t jl0 = int64_t(tile_q % a.silu_tps) * (BN / 2);
@@ -1863,7 +1870,9 @@ extern "C" int qw_qkv_gemm_norm_rope_store_kv(const void* A, const void* W, int6
   a.nh = n_heads;
   a.nkv = n_kv_heads;
   a.tp = tp;
-  return launch_tc<256, 4, false, tc::EPI_QKV, false>(mA, mW, a, 1, static_cast<cudaStream_t>(stream));
+  // persistent: one CTA per SM, two TMEM accumulators, so each tile's longer
+  // epilogue runs while the MMAs of the CTA's next tile proceed
+  return launch_tc_persist<tc::EPI_QKV, false>(mA, mW, a, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int qw_selftest_wait_timeout(void* stream) {

@@ -192,6 +192,10 @@ class Qwen3Forward:
         # folded KV store requires anyway)
         self._history_ready = True
         self._fused = None     # (layer table, workspace), built on first use
+        # prefill: QK-norm + RoPE + KV store in the QKV GEMM's epilogue (persistent
+        # tensor-core kernel; 8 x 2048 tokens: 166 us per layer against 197 us for the
+        # GEMM and the standalone kernel; the same results bit for bit)
+        self.fused_qkv = True
         # prefill in five kernels per layer (QK-norm + RoPE + KV store in the QKV GEMM's
         # epilogue, residual add + RMSNorm in the o_proj and down GEMMs' epilogues);
         # off by default: on GB300 the longer epilogues, run after each tile's
@@ -210,6 +214,13 @@ class Qwen3Forward:
                 (M, m.hidden, m.n_heads * m.head_dim, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE),
                 (M, 2 * m.intermediate, m.hidden, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL),
                 (M, m.hidden, m.intermediate, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE)]
+
+    def qkv_epilogue_ok(self) -> bool:
+        """Prefill: QK-norm + RoPE + KV store as the QKV GEMM's epilogue (bf16,
+        head_dim 128, two whole heads of one shard per 256-column tile)."""
+        m = self.m
+        return (self.fused_qkv and self.dtype == torch.bfloat16 and m.head_dim == 128
+                and ((m.n_heads + 2 * m.n_kv_heads) // m.tp) % 2 == 0 and m.hidden % 8 == 0)
 
     def prefill_fusion_ok(self) -> bool:
         """Prefill through the fused epilogues: QK-norm + RoPE + KV store in the QKV
@@ -281,11 +292,22 @@ class Qwen3Forward:
         else:
             with self._around(f"{ph}.add_rmsnorm", l):
                 L.add_rmsnorm(h, None if first else res, res, p.input_ln, m.eps, y, stream)
-            with self._around(f"{ph}.gemm_qkv", l):
-                L.gemm(y, p.qkv, qkv, self.qkv_width, tp, L.QW_GEMM_COLUMN, L.QW_EPI_NONE, self.workspace, stream)
+            if not decode and self.qkv_epilogue_ok():
+                # QK-norm + RoPE + KV store as the QKV GEMM's epilogue: no QKV round trip
+                with self._around(f"{ph}.gemm_qkv_norm_rope_store_kv", l):
+                    L.qkv_gemm_norm_rope_store_kv(y, p.qkv, m.n_heads, m.n_kv_heads, m.head_dim, tp, ctx.positions,
+                                                  self.cos_sin, p.q_norm, p.k_norm, m.eps, ctx.slot_mapping,
+                                                  self.k_cache[l], self.v_cache[l], self.q[:T], self.err, stream)
+            else:
+                with self._around(f"{ph}.gemm_qkv", l):
+                    L.gemm(y, p.qkv, qkv, self.qkv_width, tp, L.QW_GEMM_COLUMN, L.QW_EPI_NONE, self.workspace, stream)
         q = self.q[:T]
         attn = self.attn[:T]
-        if decode and self.dtype == torch.bfloat16 and m.head_dim == 128:
+        if not decode and self.qkv_epilogue_ok():
+            with self._around(f"{ph}.attention", l):
+                L.attention_prefill(q, self.k_cache[l], self.v_cache[l], ctx.cu_seqlens, ctx.cu_seqlens, ctx.seq_base,
+                                    ctx.max_seqlen, m.n_heads, m.n_kv_heads, m.head_dim, self.scale, attn, stream)
+        elif decode and self.dtype == torch.bfloat16 and m.head_dim == 128:
             # QK-norm + RoPE + KV store folded into decode attention.  Sequence b's
             # cache is contiguous from seq_base[b] and this step's k/v go to its last
             # row, so the kernel before (the QKV GEMV) writes none of the cached
