@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import contextlib
+import itertools
 import json
 import os
 import statistics
@@ -58,7 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--profile-window", action="store_true",
                     help="after the timed region, run one more step between cudaProfilerStart/Stop "
                          "(for ncu --profile-from-start off)")
-    ap.add_argument("--profile-kernel", choices=["decode.attention", "prefill.gemm_gate_up_silu"], default=None,
+    ap.add_argument("--profile-kernel", choices=["decode.attention", "prefill.gemm_gate_up_silu", "prefill.attention"],
+                    default=None,
                     help="launch only this kernel, --profile-reps times, on inputs of the workload's shape "
                          "(random values, mean decode context) and exit: a small case for ncu section captures")
     ap.add_argument("--profile-reps", type=int, default=3)
@@ -949,6 +951,14 @@ def profile_kernel(args):
                                                    torch.bfloat16), 16), dtype=torch.uint8, device="cuda")
         for _ in range(args.profile_reps):
             L.gemm(x, w, act, 2 * I, m.tp, L.QW_GEMM_COLUMN, L.QW_EPI_SILU_MUL, ws)
+    if args.profile_kernel == "prefill.attention":   # causal prefill over the prompts, keys from the cache
+        T = sum(seqs)
+        q = rnd(T, nh, hd)
+        kc, vc = rnd(T, nkv, hd), rnd(T, nkv, hd)
+        cu = torch.tensor([0] + list(itertools.accumulate(seqs)), dtype=torch.int32, device="cuda")
+        out = torch.empty(T, nh * hd, dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.profile_reps):
+            L.attention_prefill(q, kc, vc, cu, cu, cu[:-1].contiguous(), max(seqs), nh, nkv, hd, hd ** -0.5, out)
     torch.cuda.synchronize()
     L.device_error()
 

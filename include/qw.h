@@ -302,7 +302,10 @@ int qw_attention_prefill_paged(const void* q, const void* k_cache, const void* v
  *       slot_mapping int64 [B], err_count: as for qw_qkv_norm_rope_store_kv;
  *   k_cache, v_cache bf16 [num_slots, nkv, 128] (16-byte aligned);
  *   context_lens, seq_base, max_context, scale, out, workspace, flags: as for
- *       qw_attention_decode (workspace from qw_attention_decode_workspace_size).
+ *       qw_attention_decode (workspace from qw_attention_decode_workspace_size);
+ *       with QW_DECODE_HISTORY_READY the caller also states that positions were
+ *       complete before the previous kernel started, and the kernel reads them,
+ *       the gammas and cos_sin before it waits.
  * Sequence b's key positions 0 .. context_lens[b] - 1 sit at cache rows
  * seq_base[b] + position, and this step's k and v are the ones at position
  * context_lens[b] - 1: slot_mapping[b] must be seq_base[b] + context_lens[b]

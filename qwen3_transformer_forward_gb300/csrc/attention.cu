@@ -498,6 +498,17 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
   const int p_first = int(lo / T), p_last = int((hi - 1) / T);
   const int L_first = ctx_lens[p_first / nkv];   // loaded together with the base below
   const int base_first = pages.table == nullptr ? seq_base[p_first / nkv] : 0;
+  // the folded QK-norm + RoPE's constants, in the same round trip: the first
+  // sequence's position and both gammas (ahead of the wait with history_ready,
+  // which covers positions; the weights are constants)
+  const int d = tid;
+  int64_t pos_first = 0;
+  float gam_q = 0.0f, gam_k = 0.0f;
+  if (rp.qkv != nullptr) {
+    pos_first = rp.positions[p_first / nkv];
+    gam_q = __bfloat162float(rp.q_gamma[d]);
+    gam_k = __bfloat162float(rp.k_gamma[d]);
+  }
   // this CTA's tiles of pair p: the static range clipped to the sequence's own length (Tb tiles)
   auto seg_range = [&](int p, int& ta, int& tb, int& Tb) {
     const int ts = p == p_first ? int(lo - int64_t(p) * T) : 0;
@@ -554,6 +565,15 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
         if (!prod_next() || pt == pTb - 1) break;
         else issue(issued);
   }
+  // ... and the first sequence's cos / sin, after the copies are on their
+  // way, so that after the wait only the QKV row is a round trip
+  float rope_c = 0.0f, rope_s = 0.0f;
+  const bool pos_ok_first = pos_first >= 0 && pos_first < rp.max_pos;
+  if (rp.qkv != nullptr) {
+    const float* cs = rp.cos_sin + (pos_ok_first ? pos_first : 0) * DC_HD;
+    rope_c = cs[d & 63];
+    rope_s = cs[64 + (d & 63)];
+  }
   if (history_ready) {
     pdl_wait();      // q and the sequences' last rows are complete and visible
     pdl_trigger();   // only now may the next kernel start its prologue
@@ -564,30 +584,36 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
   float* nrm = sO;                                           // [G][128] normed values
   bf16* qs = reinterpret_cast<bf16*>(sO + G * DC_HD);        // [G][128] roped q
   float* red = sML;                                          // [G][4] sums of squares
-  const int d = tid;
   const int nh_l = nh / rp.tp, nkv_l = nkv / rp.tp;
   const int64_t width_r = int64_t(nh_l + 2 * nkv_l) * DC_HD;
-  auto norm_rope = [&](int b, const int64_t* h_off, const bf16* gamma, int nheads, float* y) {
-    const int64_t pos = rp.positions[b];
-    const bool pos_ok = pos >= 0 && pos < rp.max_pos;
+  auto norm_rope = [&](int b, const int64_t* h_off, float gm, int nheads, float* y) {
     const bf16* row = rp.qkv + int64_t(b) * width_r * rp.tp;
     float x[G];
-    for (int j = 0; j < nheads; ++j) {
-      x[j] = __bfloat162float(row[h_off[j] + d]);
-      const float ss = warp_sum(x[j] * x[j]);
-      if (lane == 0) red[j * 4 + warp] = ss;
+#pragma unroll
+    for (int j = 0; j < G; ++j)   // every head's element in flight at once
+      if (j < nheads) x[j] = __bfloat162float(row[h_off[j] + d]);
+    bool pos_ok = pos_ok_first;
+    float c = rope_c, sn = rope_s;
+    if (b != p_first / nkv) {   // a later sequence of this CTA's range
+      const int64_t pos = rp.positions[b];
+      pos_ok = pos >= 0 && pos < rp.max_pos;
+      const float* cs = rp.cos_sin + (pos_ok ? pos : 0) * DC_HD;
+      c = cs[d & 63];
+      sn = cs[64 + (d & 63)];
     }
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+      if (j < nheads) {
+        const float ss = warp_sum(x[j] * x[j]);
+        if (lane == 0) red[j * 4 + warp] = ss;
+      }
     __syncthreads();
-    const float gm = __bfloat162float(gamma[d]);
     for (int j = 0; j < nheads; ++j) {
       const float ss = red[j * 4] + red[j * 4 + 1] + red[j * 4 + 2] + red[j * 4 + 3];
       const float inv = rsqrtf(ss / float(DC_HD) + rp.eps);
       nrm[j * DC_HD + d] = round_t<bf16>((x[j] * inv) * gm);   // q_norm / k_norm output
     }
     __syncthreads();
-    const float* cs = rp.cos_sin + (pos_ok ? pos : 0) * DC_HD;
-    const int i = d & 63;
-    const float c = cs[i], sn = cs[64 + i];
     for (int j = 0; j < nheads; ++j) {
       const float n = nrm[j * DC_HD + d], np = nrm[j * DC_HD + (d ^ 64)];
       y[j] = pos_ok ? (d < 64 ? n * c - np * sn : n * c + np * sn) : 0.0f;
@@ -604,7 +630,7 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
       const int b = p / nkv, g = p % nkv;
       const int64_t k_off = int64_t(g / nkv_l) * width_r + int64_t(nh_l + g % nkv_l) * DC_HD;
       float y[G];
-      const bool pos_ok = norm_rope(b, &k_off, rp.k_gamma, 1, y);
+      const bool pos_ok = norm_rope(b, &k_off, gam_k, 1, y);
       const int64_t slot = rp.slots[b];
       if (slot != -1) {
         const bool slot_ok = slot >= 0 && slot < rp.num_slots;
@@ -649,7 +675,7 @@ __global__ void __launch_bounds__(DT_THREADS) attn_decode_tc_kernel(
           q_off[jh] = int64_t(h / nh_l) * width_r + int64_t(h % nh_l) * DC_HD;
         }
         float y[G];
-        norm_rope(b, q_off, rp.q_gamma, G, y);
+        norm_rope(b, q_off, gam_q, G, y);
 #pragma unroll
         for (int jh = 0; jh < G; ++jh) qs[jh * DC_HD + d] = __float2bfloat16_rn(y[jh]);
         __syncthreads();
