@@ -83,6 +83,7 @@ struct TcArgs {
   int64_t k_shard;      // K / tp
   int64_t i_l;          // intermediate per shard (SILU)
   int silu_tps;         // output tiles per shard (SILU)
+  int tma_store;        // persistent kernel: the epilogue stores 32 x 64 boxes through tmC
   // EPI_QKV: per-head QK-RMSNorm + RoPE + KV-cache store on the merged QKV output
   const int64_t* positions;
   const float* cos_sin;  // [max_pos, 128]: cos | sin
@@ -143,6 +144,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
           dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
+}
+// shared -> global tensor copy of one box (bulk async-group completion)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most one of this thread's bulk groups still reading its shared memory source
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// every bulk group of this thread complete (its writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
 }
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
   asm volatile(
@@ -674,11 +691,17 @@ __global__ void __launch_bounds__(192, 1)
 // ---------------------------------------------------------------------------
 constexpr int PBN = 256, PSTAGES = 4;
 constexpr uint32_t P_TMEM_COLS = 512;
+// epilogue staging: per epilogue warp two 32-row x 128-byte boxes (128B-swizzled),
+// 1 KB past the ring's barrier area
+constexpr uint32_t P_STAGE_BOX = 32 * 128;
+constexpr size_t psmem_bytes() {
+  return 1024 + size_t(PSTAGES) * (TileCfg<PBN>::A_BYTES + TileCfg<PBN>::B_BYTES) + 1024 + 4 * 2 * P_STAGE_BOX;
+}
 
 template <int EPI, bool WROW>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_persist_kernel(const __grid_constant__ CUtensorMap tmAct, const __grid_constant__ CUtensorMap tmW,
-                           TcArgs a) {
+                           const __grid_constant__ CUtensorMap tmC, TcArgs a) {
   constexpr int BN = PBN, STAGES = PSTAGES;
   constexpr uint32_t A_BYTES = TileCfg<BN>::A_BYTES, B_BYTES = TileCfg<BN>::B_BYTES;
   extern __shared__ uint8_t smem_dyn[];
@@ -832,6 +855,30 @@ __global__ void __launch_bounds__(192, 1)
     // ---------------- epilogue ----------------
     // waits and the abort check are warp-uniform: tcgen05.ld is .sync.aligned
     const int quarter = warp & 3;
+    // a.tma_store: each chunk of 32 rows x 64 columns is converted into one of
+    // this warp's two staging boxes and stored by a tensor copy, so the
+    // epilogue's global writes leave the load/store path to the mainloop's copies
+    const uint32_t stage = smem_u32(sm) + uint32_t(STAGES) * (A_BYTES + B_BYTES) + 1024u +
+                           uint32_t(quarter) * 2u * P_STAGE_BOX;
+    int nst = 0;   // tensor stores issued by this warp
+    // row `lane` of a staging box: 16-byte chunk v at its 128B-swizzled place
+    auto stage_chunk = [&](uint32_t buf, int v, uint4 u) {
+      st_shared_v4(buf + uint32_t(lane) * 128u + (uint32_t(v ^ (lane & 7)) << 4), u);
+    };
+    auto store_box = [&](uint32_t buf, int64_t x, int64_t y) {   // after the warp wrote buf
+      tcx::fence_proxy_async();   // these generic writes before the tensor copy reads them
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&tmC, buf, int(x), int(y));
+        bulk_commit();
+      }
+      ++nst;
+    };
+    auto next_buf = [&]() {   // a staging box whose previous store has read it
+      if (lane == 0) bulk_wait_read_1();
+      __syncwarp();
+      return stage + uint32_t(nst & 1) * P_STAGE_BOX;
+    };
     for (int j = 0; j < my_tiles; ++j) {
       const int b = j & 1;
       const uint32_t use = uint32_t(j >> 1) & 1u;
@@ -845,7 +892,62 @@ __global__ void __launch_bounds__(192, 1)
       tile_of(j, tile_p, tile_q);
       const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(b * BN);
       const int64_t m = int64_t(tile_p) * BM + quarter * 32 + lane;
-      if (EPI == EPI_NONE) {
+      const int64_t m0 = int64_t(tile_p) * BM + quarter * 32;   // this warp's first row
+      if (EPI == EPI_NONE && a.tma_store) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 64) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(trow + c, r0);
+          tmem_ld32(trow + c + 32, r1);
+          tmem_ld_wait();
+          const int64_t n0 = int64_t(tile_q) * BN + c;
+          if (m0 < a.M && n0 < a.N) {   // (warp-uniform; the copy clips rows >= M, columns >= N)
+            const uint32_t buf = next_buf();
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const uint32_t* q = v < 4 ? r0 + 8 * v : r1 + 8 * (v - 4);
+              uint4 u;
+              u.x = pack_bf16(__uint_as_float(q[0]), __uint_as_float(q[1]));
+              u.y = pack_bf16(__uint_as_float(q[2]), __uint_as_float(q[3]));
+              u.z = pack_bf16(__uint_as_float(q[4]), __uint_as_float(q[5]));
+              u.w = pack_bf16(__uint_as_float(q[6]), __uint_as_float(q[7]));
+              stage_chunk(buf, v, u);
+            }
+            store_box(buf, n0, m0);
+          }
+        }
+      } else if (EPI == EPI_SILU && a.tma_store) {   // (i_l % 64 == 0: a box never crosses a shard)
+        const int r_s = tile_q / a.silu_tps;
+        const int64_t jl0 = int64_t(tile_q % a.silu_tps) * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 64) {
+          const int64_t j0 = jl0 + c;
+          const bool live = m0 < a.M && j0 < a.i_l;   // (warp-uniform)
+          const uint32_t buf = live ? next_buf() : 0u;
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            uint32_t g[32], u[32];
+            tmem_ld32(trow + c + 32 * h, g);
+            tmem_ld32(trow + BN / 2 + c + 32 * h, u);
+            tmem_ld_wait();
+            if (!live) continue;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float o[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                o[e] = silu_mul_bf16(__uint_as_float(g[8 * v + e]), __uint_as_float(u[8 * v + e]));
+              uint4 w;
+              w.x = pack_bf16(o[0], o[1]);
+              w.y = pack_bf16(o[2], o[3]);
+              w.z = pack_bf16(o[4], o[5]);
+              w.w = pack_bf16(o[6], o[7]);
+              stage_chunk(buf, 4 * h + v, w);
+            }
+          }
+          if (live) store_box(buf, int64_t(r_s) * a.i_l + j0, m0);
+        }
+      } else if (EPI == EPI_NONE) {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t r[32];
@@ -914,6 +1016,8 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) tcx::mbar_arrive(bar_acc_empty(b));
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
     }
+    if (lane == 0) bulk_wait_all();   // the tensor stores are complete before the CTA exits
+    __syncwarp();
   }
 
   __syncwarp();
@@ -1384,10 +1488,34 @@ bool tc_persistent_enabled() {
   return v && v[0] == '1';
 }
 
+// args.C as rows of args.ldc bf16 in boxes of 32 rows x 64 columns, the
+// persistent epilogue's tensor stores; args.tma_store says whether they apply
+// (SiluAndMul: only when no 64-column box crosses a shard's i_l columns)
+template <int EPI>
+int output_map(CUtensorMap* mC, tc::TcArgs& args) {
+  args.tma_store = 0;
+  if (EPI == tc::EPI_QKV || args.M <= 0) return QW_OK;
+  if (EPI == tc::EPI_SILU && args.i_l % 64 != 0) return QW_OK;
+  if ((reinterpret_cast<uintptr_t>(args.C) & 15u) != 0 || (args.ldc * 2) % 16 != 0) return QW_OK;
+  const uint64_t dims[2] = {uint64_t(args.ldc), uint64_t(args.M)};
+  const uint64_t strides[1] = {uint64_t(args.ldc) * 2};
+  const uint32_t box[2] = {64u, 32u};
+  const int rc = make_tensor_map(mC, args.C, 2, dims, strides, box);
+  if (rc) return rc;
+  args.tma_store = 1;
+  return QW_OK;
+}
+
 template <int EPI, bool WROW>
-int launch_tc_persist(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArgs& args, cudaStream_t st) {
+int launch_tc_persist(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArgs& args_in, cudaStream_t st) {
   auto kern = tc::gemm_tc_persist_kernel<EPI, WROW>;
-  constexpr size_t smem = tc::smem_bytes<tc::PBN, tc::PSTAGES>();
+  constexpr size_t smem = tc::psmem_bytes();
+  tc::TcArgs args = args_in;
+  CUtensorMap mC = act;   // (unused unless args.tma_store)
+  {
+    const int rc = output_map<EPI>(&mC, args);
+    if (rc) return rc;
+  }
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
@@ -1406,7 +1534,7 @@ int launch_tc_persist(const CUtensorMap& act, const CUtensorMap& w, const tc::Tc
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.numAttrs = 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, act, w, args);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, act, w, mC, args);
   if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "gemm_tc_persist_kernel launch: %s", cudaGetErrorString(e));
   return check_launch("gemm_tc_persist_kernel");
 }
@@ -1449,11 +1577,6 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
   if (!p.swap) {
     rc = make_map(&mA, A, 2, uint64_t(K), uint64_t(M), 1, uint64_t(K) * 2, 0, tc::BM);
     if (rc) return rc;
-    const uint32_t wrows = epi == QW_EPI_SILU_MUL ? uint32_t(p.bn / 2) : uint32_t(p.bn);
-    if (wrow) rc = make_map(&mW, W, 3, uint64_t(Kl), uint64_t(N), uint64_t(tp), uint64_t(Kl) * 2,
-                            uint64_t(Kl) * 2 * uint64_t(N), wrows);
-    else rc = make_map(&mW, W, 2, uint64_t(K), uint64_t(N), 1, uint64_t(K) * 2, 0, wrows);
-    if (rc) return rc;
     a.p_tiles = int((M + tc::BM - 1) / tc::BM);
     if (epi == QW_EPI_SILU_MUL) {
       a.silu_tps = int((a.i_l + p.bn / 2 - 1) / (p.bn / 2));
@@ -1461,9 +1584,15 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
     } else {
       a.q_tiles = int((N + p.bn - 1) / p.bn);
     }
+    const bool persistent = tc_persistent_enabled();
+    const uint32_t wrows = epi == QW_EPI_SILU_MUL ? uint32_t(p.bn / 2) : uint32_t(p.bn);
+    if (wrow) rc = make_map(&mW, W, 3, uint64_t(Kl), uint64_t(N), uint64_t(tp), uint64_t(Kl) * 2,
+                            uint64_t(Kl) * 2 * uint64_t(N), wrows);
+    else rc = make_map(&mW, W, 2, uint64_t(K), uint64_t(N), 1, uint64_t(K) * 2, 0, wrows);
+    if (rc) return rc;
     a.p_fastest = (M * K * 2) <= (int64_t(48) << 20) ? 1 : 0;
     a.kblocks = p.kblocks_total;
-    if (tc_persistent_enabled()) {
+    if (persistent) {
       if (epi == QW_EPI_SILU_MUL) return launch_tc_persist<tc::EPI_SILU, false>(mA, mW, a, st);
       if (wrow) return launch_tc_persist<tc::EPI_NONE, true>(mA, mW, a, st);
       return launch_tc_persist<tc::EPI_NONE, false>(mA, mW, a, st);

@@ -290,6 +290,7 @@ def test_add_rmsnorm_gemm(L, M, N, K, tp, epi, with_res):
     (300, 528, 192, 1, 0, 0),       # ragged M and N, one tile per CTA
     (200, 272, 256, 2, 1, 0),       # row split
     (333, 800, 128, 2, 0, 1),       # SiluAndMul, I/tp = 200: a half-filled last tile per shard
+    (333, 512, 128, 2, 0, 1),       # SiluAndMul, I/tp = 128: tensor-store epilogue, ragged rows
     (4096, 4096, 64, 1, 0, 0),      # one k-block per tile: the ring spans tile boundaries
     (16384, 6144, 1024, 2, 0, 1),   # the 0.6B prefill gate_up: 20 tiles per CTA
 ])
