@@ -161,6 +161,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::
@@ -201,6 +202,104 @@ __device__ __forceinline__ float silu_mul_bf16(float g, float u) {
   g = round_t<bf16>(g);
   u = round_t<bf16>(u);
   return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+// Epilogue tensor stores.  An epilogue warp owns 32 accumulator rows (TMEM
+// lanes); it converts 32 rows x 64 columns at a time into one of its two
+// staging boxes in shared memory (row r at 128 r bytes, 16-byte chunk v at
+// (v ^ (r & 7)) * 16: the 128-byte swizzle of the output tensor map) and
+// stores the box with one tensor copy, which clips rows and columns past the
+// tensor.  The copies write whole lines and leave the load/store path free;
+// direct stores of one row per thread touch 32 rows per instruction.
+constexpr uint32_t P_STAGE_BOX = 32 * 128;   // one staging box
+struct BoxStore {
+  uint32_t stage;   // this warp's two boxes (1024-byte aligned)
+  int lane;
+  int n = 0;        // boxes stored
+  __device__ uint32_t next() {   // a box whose previous copy has read it
+    if (lane == 0) bulk_wait_read_1();
+    __syncwarp();
+    return stage + uint32_t(n & 1) * P_STAGE_BOX;
+  }
+  __device__ void put(uint32_t box, int v, uint4 u) const {
+    st_shared_v4(box + uint32_t(lane) * 128u + (uint32_t(v ^ (lane & 7)) << 4), u);
+  }
+  __device__ void store(const CUtensorMap* map, uint32_t box, int64_t x, int64_t y) {
+    tcx::fence_proxy_async();   // the warp's generic writes before the tensor copy reads them
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, box, int(x), int(y));
+      bulk_commit();
+    }
+    ++n;
+  }
+  __device__ void finish() const {   // the copies have written global memory
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+};
+__device__ __forceinline__ uint4 pack8(const uint32_t* q) {
+  uint4 u;
+  u.x = pack_bf16(__uint_as_float(q[0]), __uint_as_float(q[1]));
+  u.y = pack_bf16(__uint_as_float(q[2]), __uint_as_float(q[3]));
+  u.z = pack_bf16(__uint_as_float(q[4]), __uint_as_float(q[5]));
+  u.w = pack_bf16(__uint_as_float(q[6]), __uint_as_float(q[7]));
+  return u;
+}
+// C[m0 .. m0+31, n_base .. n_base+ncols) = the warp's accumulator columns [0, ncols), as bf16
+// (zero: store zeros instead, for a tile with no k-blocks or after a timeout)
+__device__ __forceinline__ void epi_store_tma(BoxStore& bs, const CUtensorMap* map, uint32_t trow, int ncols,
+                                              int64_t m0, int64_t M, int64_t n_base, int64_t N, bool zero) {
+#pragma unroll 1
+  for (int c = 0; c < ncols; c += 64) {
+    uint32_t r0[32], r1[32];
+    tmem_ld32(trow + c, r0);
+    tmem_ld32(trow + c + 32, r1);
+    tmem_ld_wait();
+    if (m0 >= M || n_base + c >= N) continue;   // (warp-uniform)
+    if (zero) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r0[e] = r1[e] = 0u;
+    }
+    const uint32_t box = bs.next();
+#pragma unroll
+    for (int v = 0; v < 8; ++v) bs.put(box, v, pack8(v < 4 ? r0 + 8 * v : r1 + 8 * (v - 4)));
+    bs.store(map, box, n_base + c, m0);
+  }
+}
+// SiluAndMul: gate columns [0, half), up columns [half, 2 half) of the warp's
+// accumulator rows -> C[m0 .., col_base + j) for j < half with jl0 + j < i_l
+// (i_l % 64 == 0, so that a box never crosses into the next shard's columns)
+__device__ __forceinline__ void epi_silu_tma(BoxStore& bs, const CUtensorMap* map, uint32_t trow, int half,
+                                             int64_t m0, int64_t M, int64_t col_base, int64_t jl0, int64_t i_l,
+                                             bool zero) {
+#pragma unroll 1
+  for (int c = 0; c < half; c += 64) {
+    const bool live = m0 < M && jl0 + c < i_l;   // (warp-uniform)
+    const uint32_t box = live ? bs.next() : 0u;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      uint32_t g[32], u[32];
+      tmem_ld32(trow + c + 32 * h, g);
+      tmem_ld32(trow + half + c + 32 * h, u);
+      tmem_ld_wait();
+      if (!live) continue;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          o[e] = zero ? 0.0f : silu_mul_bf16(__uint_as_float(g[8 * v + e]), __uint_as_float(u[8 * v + e]));
+        uint4 w;
+        w.x = pack_bf16(o[0], o[1]);
+        w.y = pack_bf16(o[2], o[3]);
+        w.z = pack_bf16(o[4], o[5]);
+        w.w = pack_bf16(o[6], o[7]);
+        bs.put(box, 4 * h + v, w);
+      }
+    }
+    if (live) bs.store(map, box, col_base + c, m0);
+  }
 }
 
 // Epilogue of a QKV tile (EPI_QKV): the tile's 256 columns are two whole heads
@@ -311,7 +410,8 @@ constexpr size_t smem_bytes() {
 // SWAP=true : MMA-A = weight rows (N),      MMA-B = token rows (M, padded to BN).
 template <int BN, int STAGES, bool SWAP, int EPI, bool WROW>
 __global__ void __launch_bounds__(192, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmAct, const __grid_constant__ CUtensorMap tmW, TcArgs a) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmAct, const __grid_constant__ CUtensorMap tmW,
+                   const __grid_constant__ CUtensorMap tmC, TcArgs a) {
   using Cfg = TileCfg<BN>;
   constexpr uint32_t A_BYTES = Cfg::A_BYTES, B_BYTES = Cfg::B_BYTES;
   extern __shared__ uint8_t smem_dyn[];
@@ -449,7 +549,13 @@ __global__ void __launch_bounds__(192, 1)
     const bool has_acc = kb1 > kb0;
     if (!SWAP) {
       const int64_t m = int64_t(tile_p) * BM + quarter * 32 + lane;
-      if (EPI == EPI_NONE) {
+      const int64_t m0 = int64_t(tile_p) * BM + quarter * 32;   // this warp's first row
+      // a.tma_store: staged in the ring's shared memory, free now that every MMA has completed
+      BoxStore bs{smem_u32(sA) + uint32_t(quarter) * 2u * P_STAGE_BOX, lane};
+      if (EPI == EPI_NONE && a.tma_store) {
+        epi_store_tma(bs, &tmC, trow, BN, m0, a.M, int64_t(tile_q) * BN, a.N, !ok || !has_acc);
+        bs.finish();
+      } else if (EPI == EPI_NONE) {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t r[32];
@@ -691,9 +797,7 @@ __global__ void __launch_bounds__(192, 1)
 // ---------------------------------------------------------------------------
 constexpr int PBN = 256, PSTAGES = 4;
 constexpr uint32_t P_TMEM_COLS = 512;
-// epilogue staging: per epilogue warp two 32-row x 128-byte boxes (128B-swizzled),
-// 1 KB past the ring's barrier area
-constexpr uint32_t P_STAGE_BOX = 32 * 128;
+// epilogue staging (BoxStore): two boxes per epilogue warp, 1 KB past the ring's barrier area
 constexpr size_t psmem_bytes() {
   return 1024 + size_t(PSTAGES) * (TileCfg<PBN>::A_BYTES + TileCfg<PBN>::B_BYTES) + 1024 + 4 * 2 * P_STAGE_BOX;
 }
@@ -855,30 +959,9 @@ __global__ void __launch_bounds__(192, 1)
     // ---------------- epilogue ----------------
     // waits and the abort check are warp-uniform: tcgen05.ld is .sync.aligned
     const int quarter = warp & 3;
-    // a.tma_store: each chunk of 32 rows x 64 columns is converted into one of
-    // this warp's two staging boxes and stored by a tensor copy, so the
-    // epilogue's global writes leave the load/store path to the mainloop's copies
-    const uint32_t stage = smem_u32(sm) + uint32_t(STAGES) * (A_BYTES + B_BYTES) + 1024u +
-                           uint32_t(quarter) * 2u * P_STAGE_BOX;
-    int nst = 0;   // tensor stores issued by this warp
-    // row `lane` of a staging box: 16-byte chunk v at its 128B-swizzled place
-    auto stage_chunk = [&](uint32_t buf, int v, uint4 u) {
-      st_shared_v4(buf + uint32_t(lane) * 128u + (uint32_t(v ^ (lane & 7)) << 4), u);
-    };
-    auto store_box = [&](uint32_t buf, int64_t x, int64_t y) {   // after the warp wrote buf
-      tcx::fence_proxy_async();   // these generic writes before the tensor copy reads them
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(&tmC, buf, int(x), int(y));
-        bulk_commit();
-      }
-      ++nst;
-    };
-    auto next_buf = [&]() {   // a staging box whose previous store has read it
-      if (lane == 0) bulk_wait_read_1();
-      __syncwarp();
-      return stage + uint32_t(nst & 1) * P_STAGE_BOX;
-    };
+    // a.tma_store: stores through tmC (BoxStore)
+    BoxStore bs{smem_u32(sm) + uint32_t(STAGES) * (A_BYTES + B_BYTES) + 1024u + uint32_t(quarter) * 2u * P_STAGE_BOX,
+                lane};
     for (int j = 0; j < my_tiles; ++j) {
       const int b = j & 1;
       const uint32_t use = uint32_t(j >> 1) & 1u;
@@ -894,59 +977,11 @@ __global__ void __launch_bounds__(192, 1)
       const int64_t m = int64_t(tile_p) * BM + quarter * 32 + lane;
       const int64_t m0 = int64_t(tile_p) * BM + quarter * 32;   // this warp's first row
       if (EPI == EPI_NONE && a.tma_store) {
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 64) {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(trow + c, r0);
-          tmem_ld32(trow + c + 32, r1);
-          tmem_ld_wait();
-          const int64_t n0 = int64_t(tile_q) * BN + c;
-          if (m0 < a.M && n0 < a.N) {   // (warp-uniform; the copy clips rows >= M, columns >= N)
-            const uint32_t buf = next_buf();
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const uint32_t* q = v < 4 ? r0 + 8 * v : r1 + 8 * (v - 4);
-              uint4 u;
-              u.x = pack_bf16(__uint_as_float(q[0]), __uint_as_float(q[1]));
-              u.y = pack_bf16(__uint_as_float(q[2]), __uint_as_float(q[3]));
-              u.z = pack_bf16(__uint_as_float(q[4]), __uint_as_float(q[5]));
-              u.w = pack_bf16(__uint_as_float(q[6]), __uint_as_float(q[7]));
-              stage_chunk(buf, v, u);
-            }
-            store_box(buf, n0, m0);
-          }
-        }
-      } else if (EPI == EPI_SILU && a.tma_store) {   // (i_l % 64 == 0: a box never crosses a shard)
+        epi_store_tma(bs, &tmC, trow, BN, m0, a.M, int64_t(tile_q) * BN, a.N, false);
+      } else if (EPI == EPI_SILU && a.tma_store) {
         const int r_s = tile_q / a.silu_tps;
         const int64_t jl0 = int64_t(tile_q % a.silu_tps) * (BN / 2);
-#pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 64) {
-          const int64_t j0 = jl0 + c;
-          const bool live = m0 < a.M && j0 < a.i_l;   // (warp-uniform)
-          const uint32_t buf = live ? next_buf() : 0u;
-#pragma unroll 1
-          for (int h = 0; h < 2; ++h) {
-            uint32_t g[32], u[32];
-            tmem_ld32(trow + c + 32 * h, g);
-            tmem_ld32(trow + BN / 2 + c + 32 * h, u);
-            tmem_ld_wait();
-            if (!live) continue;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              float o[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                o[e] = silu_mul_bf16(__uint_as_float(g[8 * v + e]), __uint_as_float(u[8 * v + e]));
-              uint4 w;
-              w.x = pack_bf16(o[0], o[1]);
-              w.y = pack_bf16(o[2], o[3]);
-              w.z = pack_bf16(o[4], o[5]);
-              w.w = pack_bf16(o[6], o[7]);
-              stage_chunk(buf, 4 * h + v, w);
-            }
-          }
-          if (live) store_box(buf, int64_t(r_s) * a.i_l + j0, m0);
-        }
+        epi_silu_tma(bs, &tmC, trow, BN / 2, m0, a.M, int64_t(r_s) * a.i_l + jl0, jl0, a.i_l, false);
       } else if (EPI == EPI_NONE) {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -1016,8 +1051,7 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) tcx::mbar_arrive(bar_acc_empty(b));
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
     }
-    if (lane == 0) bulk_wait_all();   // the tensor stores are complete before the CTA exits
-    __syncwarp();
+    bs.finish();   // the tensor stores are complete before the CTA exits
   }
 
   __syncwarp();
@@ -1451,9 +1485,37 @@ Plan plan_bf16(int64_t M, int64_t N, int64_t K, int tp, int mode, int epi) {
   return p;
 }
 
+// args.C as rows of args.ldc bf16 in boxes of 32 rows x 64 columns, the
+// epilogue's tensor stores (BoxStore); args.tma_store says whether they apply
+// (SiluAndMul: only when no 64-column box crosses a shard's i_l columns)
+template <int EPI>
+int output_map(CUtensorMap* mC, tc::TcArgs& args) {
+  args.tma_store = 0;
+  if (EPI == tc::EPI_QKV || args.M <= 0) return QW_OK;
+  if (EPI == tc::EPI_SILU && args.i_l % 64 != 0) return QW_OK;
+  if ((reinterpret_cast<uintptr_t>(args.C) & 15u) != 0 || (args.ldc * 2) % 16 != 0) return QW_OK;
+  const uint64_t dims[2] = {uint64_t(args.ldc), uint64_t(args.M)};
+  const uint64_t strides[1] = {uint64_t(args.ldc) * 2};
+  const uint32_t box[2] = {64u, 32u};
+  const int rc = make_tensor_map(mC, args.C, 2, dims, strides, box);
+  if (rc) return rc;
+  args.tma_store = 1;
+  return QW_OK;
+}
+
 template <int BN, int STAGES, bool SWAP, int EPI, bool WROW>
-int launch_tc(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArgs& args, int splits, cudaStream_t st) {
+int launch_tc(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArgs& args_in, int splits, cudaStream_t st) {
   auto kern = tc::gemm_tc_kernel<BN, STAGES, SWAP, EPI, WROW>;
+  tc::TcArgs args = args_in;
+  CUtensorMap mC = act;   // (unused unless args.tma_store)
+  args.tma_store = 0;
+  // tensor-store epilogue for plain outputs (measured: QKV 134 -> 122 us, o_proj
+  // 71 -> 68 us, down 95 -> 93 us for 8 x 2048 tokens; the SiluAndMul tile
+  // stores directly: 211 us against 303 us with tensor stores)
+  if (!SWAP && splits == 1 && EPI == tc::EPI_NONE) {
+    const int rc = output_map<EPI>(&mC, args);
+    if (rc) return rc;
+  }
   constexpr size_t smem = tc::smem_bytes<BN, STAGES>();
   static bool configured = false;
   if (!configured) {
@@ -1473,7 +1535,7 @@ int launch_tc(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArgs& ar
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = splits > 1 ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, act, w, args);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, act, w, mC, args);
   if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "gemm_tc_kernel launch: %s", cudaGetErrorString(e));
   return check_launch("gemm_tc_kernel");
 }
@@ -1486,24 +1548,6 @@ static int gv_device_sms();
 bool tc_persistent_enabled() {
   const char* v = getenv("QW_TC_PERSISTENT");
   return v && v[0] == '1';
-}
-
-// args.C as rows of args.ldc bf16 in boxes of 32 rows x 64 columns, the
-// persistent epilogue's tensor stores; args.tma_store says whether they apply
-// (SiluAndMul: only when no 64-column box crosses a shard's i_l columns)
-template <int EPI>
-int output_map(CUtensorMap* mC, tc::TcArgs& args) {
-  args.tma_store = 0;
-  if (EPI == tc::EPI_QKV || args.M <= 0) return QW_OK;
-  if (EPI == tc::EPI_SILU && args.i_l % 64 != 0) return QW_OK;
-  if ((reinterpret_cast<uintptr_t>(args.C) & 15u) != 0 || (args.ldc * 2) % 16 != 0) return QW_OK;
-  const uint64_t dims[2] = {uint64_t(args.ldc), uint64_t(args.M)};
-  const uint64_t strides[1] = {uint64_t(args.ldc) * 2};
-  const uint32_t box[2] = {64u, 32u};
-  const int rc = make_tensor_map(mC, args.C, 2, dims, strides, box);
-  if (rc) return rc;
-  args.tma_store = 1;
-  return QW_OK;
 }
 
 template <int EPI, bool WROW>
@@ -1934,7 +1978,8 @@ extern "C" int qw_gemm_add_rmsnorm(const void* A, const void* W, int64_t M, int6
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mA, mW, a);
+  a.tma_store = 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mA, mW, mA, a);
   if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "gemm_tc_kernel (add + RMSNorm) launch: %s", cudaGetErrorString(e));
   return check_launch("gemm_tc_kernel (add + RMSNorm)");
 }
