@@ -322,50 +322,66 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const T* __restrict__ x, 
 // ===========================================================================
 // greedy argmax over a logits row, lowest index on ties
 // ===========================================================================
+// A row is split over a cluster of AM_CLUSTER CTAs (contiguous index ranges
+// in rank order); each CTA reduces its range, and cluster rank 0 combines the
+// CTAs' (max, index) pairs in rank order over distributed shared memory.  Every
+// comparison keeps the lower index on equal values, so the result is the
+// first maximum of the row.
+constexpr int AM_CLUSTER = 8, AM_THREADS = 256, AM_UNROLL = 4;
 template <typename T>
-__global__ void __launch_bounds__(1024) argmax_kernel(const T* __restrict__ logits, int64_t V,
-                                                      int64_t* __restrict__ out) {
+__global__ void __launch_bounds__(AM_THREADS) argmax_kernel(const T* __restrict__ logits, int64_t V,
+                                                           int64_t* __restrict__ out) {
   pdl_wait();      // inputs of this kernel are complete and visible
   pdl_trigger();   // only now may the next kernel start its prologue
   constexpr int N = V16<T>::N;
-  const T* p = logits + int64_t(blockIdx.x) * V;
+  const int64_t row = blockIdx.x / AM_CLUSTER;
+  const uint32_t rank = cluster_rank();
+  const T* p = logits + row * V;
+  const int64_t nv = V / N;   // (V * sizeof(T) is a multiple of 16 bytes)
+  const int64_t per = (nv + AM_CLUSTER - 1) / AM_CLUSTER;
+  const int64_t v0 = int64_t(rank) * per, v1 = min(nv, v0 + per);
   float best = -INFINITY;
   int64_t bidx = V;
-  const int64_t nv = V / N;
-  for (int64_t vi = threadIdx.x; vi < nv; vi += blockDim.x) {
-    float f[N];
-    load16(p + vi * N, f);
-#pragma unroll
-    for (int e = 0; e < N; ++e)
-      if (f[e] > best) { best = f[e]; bidx = vi * N + e; }
-  }
-  for (int64_t i = nv * N + threadIdx.x; i < V; i += blockDim.x) {
-    const float f = to_f(p[i]);
-    if (f > best || (f == best && i < bidx)) { best = f; bidx = i; }
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-    const int64_t oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+  auto take = [&](float ob, int64_t oi) {
     if (ob > best || (ob == best && oi < bidx)) { best = ob; bidx = oi; }
+  };
+  for (int64_t vi = v0 + threadIdx.x; vi < v1; vi += AM_THREADS * AM_UNROLL) {
+    float f[AM_UNROLL][N];
+#pragma unroll
+    for (int u = 0; u < AM_UNROLL; ++u)   // the loads of a pass in flight together
+      if (vi + u * AM_THREADS < v1) load16(p + (vi + u * AM_THREADS) * N, f[u]);
+#pragma unroll
+    for (int u = 0; u < AM_UNROLL; ++u)
+      if (vi + u * AM_THREADS < v1)
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+          if (f[u][e] > best) { best = f[u][e]; bidx = (vi + u * AM_THREADS) * N + e; }   // increasing index
   }
-  __shared__ float sb[32];
-  __shared__ int64_t si[32];
+#pragma unroll
+  for (int o = 16; o; o >>= 1) take(__shfl_xor_sync(0xffffffffu, best, o), __shfl_xor_sync(0xffffffffu, bidx, o));
+  __shared__ float sb[AM_THREADS / 32];
+  __shared__ int64_t si[AM_THREADS / 32];
+  __shared__ float cb;      // this CTA's result, read by cluster rank 0
+  __shared__ int64_t ci;
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) { sb[wid] = best; si[wid] = bidx; }
   __syncthreads();
-  if (wid == 0) {
-    const int nw = blockDim.x >> 5;
-    best = lane < nw ? sb[lane] : -INFINITY;
-    bidx = lane < nw ? si[lane] : V;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-      const int64_t oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-      if (ob > best || (ob == best && oi < bidx)) { best = ob; bidx = oi; }
-    }
-    if (lane == 0) out[blockIdx.x] = bidx < V ? bidx : 0;
+  if (threadIdx.x == 0) {
+    best = sb[0];
+    bidx = si[0];
+    for (int w = 1; w < AM_THREADS / 32; ++w) take(sb[w], si[w]);
+    cb = best;
+    ci = bidx;
   }
+  cluster_sync_all();   // every CTA's result is visible to the cluster
+  if (rank == 0 && threadIdx.x == 0) {
+    best = -INFINITY;
+    bidx = V;
+    for (uint32_t r = 0; r < AM_CLUSTER; ++r)
+      take(ld_cluster_f32(map_to_rank(smem_u32(&cb), r)), ld_cluster_s64(map_to_rank(smem_u32(&ci), r)));
+    out[row] = bidx < V ? bidx : 0;
+  }
+  cluster_sync_all();   // rank 0 has read every CTA's shared memory
 }
 
 // ===========================================================================
@@ -407,7 +423,22 @@ template int launch_gather_rows<float>(const void*, int64_t, const int32_t*, int
 
 template <typename T>
 int launch_argmax(const void* logits, int64_t M, int64_t V, int64_t* out, cudaStream_t st) {
-  launch_pdl(argmax_kernel<T>, unsigned(M), 1024, 0, st, static_cast<const T*>(logits), V, out);
+  if (M <= 0) return QW_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(M * AM_CLUSTER));
+  cfg.blockDim = dim3(AM_THREADS);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = AM_CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, argmax_kernel<T>, static_cast<const T*>(logits), V, out);
+  if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "argmax launch: %s", cudaGetErrorString(e));
   return check_launch("argmax");
 }
 template int launch_argmax<bf16>(const void*, int64_t, int64_t, int64_t*, cudaStream_t);

@@ -724,16 +724,37 @@ def test_attention_prefill_paged_prefix(L, Lk, Lq, nh, nkv):
 # ----------------------------------------------------------------------------
 
 def test_argmax_lowest_index_on_ties(L):
-    x = si.normal(0, "am.x", (5, 4096), 1.0, "bf16")
+    """A row is split over several CTAs (contiguous ranges of 512 columns
+    here): ties inside one range and across ranges both go to the lowest index."""
+    x = si.normal(0, "am.x", (6, 4096), 1.0, "bf16")
     x[0, 100] = 9.0
-    x[0, 50] = 9.0          # tie: 50 wins
-    x[1, 4095] = 9.0
+    x[0, 50] = 9.0          # tie inside one range: 50 wins
+    x[1, 4095] = 9.0        # the last column of the last range
     x[2, :] = -1.0          # all equal: 0 wins
-    out = torch.empty(5, dtype=torch.int64, device="cuda")
+    x[3, 3000] = 9.0
+    x[3, 600] = 9.0         # tie across ranges: 600 wins
+    x[4, 511] = 9.0
+    x[4, 512] = 9.0         # tie at a range boundary: 511 wins
+    x[5, :] = float("-inf")
+    x[5, 4000] = -3.0
+    out = torch.empty(6, dtype=torch.int64, device="cuda")
     L.argmax(dev(x), out)
     sync_ok(L)
     assert list(out.cpu().numpy()) == list(O.greedy(x.double().numpy()))
-    assert out[0].item() == 50 and out[2].item() == 0
+    assert out[0].item() == 50 and out[2].item() == 0 and out[3].item() == 600 and out[4].item() == 511
+
+
+def test_argmax_full_vocabulary_rows(L):
+    """Rows of the lm_head's width (151936, ragged over the CTAs of a row)."""
+    x = si.normal(0, "am.full", (9, 151936), 1.0, "bf16")
+    x[1, 151935] = 9.0
+    x[2, 0] = 9.0
+    x[3, 75968] = 9.0
+    x[3, 75967] = 9.0
+    out = torch.empty(9, dtype=torch.int64, device="cuda")
+    L.argmax(dev(x), out)
+    sync_ok(L)
+    assert list(out.cpu().numpy()) == list(O.greedy(x.double().numpy()))
 
 
 @pytest.mark.parametrize("tp", [1, 2, 4])
