@@ -281,6 +281,68 @@ __device__ __forceinline__ void epi_silu_tma(BoxStore& bs, const CUtensorMap* ma
   }
 }
 
+// Direct stores, one row per thread: row m of the warp's accumulator columns
+// [0, ncols) -> C[m, n_base + c] for n_base + c < N (zero: zeros instead)
+__device__ __forceinline__ void epi_store_direct(uint32_t trow, int ncols, int64_t m, const TcArgs& a, int64_t n_base,
+                                                 bool zero) {
+#pragma unroll 1
+  for (int c = 0; c < ncols; c += 32) {
+    uint32_t r[32];
+    tmem_ld32(trow + c, r);
+    tmem_ld_wait();
+    if (zero) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = 0u;
+    }
+    const int64_t n0 = n_base + c;
+    if (m < a.M) {
+      bf16* dst = a.C + m * a.ldc + n0;
+      if (n0 + 32 <= a.N) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) d4[v] = pack8(r + 8 * v);
+      } else {
+        for (int e = 0; e < 32; ++e)
+          if (n0 + e < a.N) dst[e] = __float2bfloat16_rn(__uint_as_float(r[e]));
+      }
+    }
+  }
+}
+// SiluAndMul, direct stores: gate columns [0, half), up [half, 2 half) of row m
+// -> C[m, r_s * i_l + jl0 + j] for jl0 + j < i_l (nothing when !live)
+__device__ __forceinline__ void epi_silu_direct(uint32_t trow, int half, int64_t m, const TcArgs& a, int r_s,
+                                                int64_t jl0, bool live) {
+#pragma unroll 1
+  for (int c = 0; c < half; c += 32) {
+    uint32_t g[32], u[32];
+    tmem_ld32(trow + c, g);
+    tmem_ld32(trow + half + c, u);
+    tmem_ld_wait();
+    if (m < a.M && live) {
+      const int64_t j0 = jl0 + c;
+      bf16* dst = a.C + m * a.ldc + int64_t(r_s) * a.i_l + j0;
+      if (j0 + 32 <= a.i_l) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          float o[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = silu_mul_bf16(__uint_as_float(g[8 * v + e]), __uint_as_float(u[8 * v + e]));
+          uint4 w;
+          w.x = pack_bf16(o[0], o[1]);
+          w.y = pack_bf16(o[2], o[3]);
+          w.z = pack_bf16(o[4], o[5]);
+          w.w = pack_bf16(o[6], o[7]);
+          d4[v] = w;
+        }
+      } else {
+        for (int e = 0; e < 32; ++e)
+          if (j0 + e < a.i_l) dst[e] = __float2bfloat16_rn(silu_mul_bf16(__uint_as_float(g[e]), __uint_as_float(u[e])));
+      }
+    }
+  }
+}
+
 // Epilogue of a QKV tile (EPI_QKV): the tile's 256 columns are two whole heads
 // of the merged QKV output (shard r = [q_r | k_r | v_r], 128 columns per
 // head).  Each thread owns one token row: it rounds the accumulator to the
@@ -752,6 +814,178 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 256 x 256 prefill tiles.  A CTA covers 256 token rows as two 128-row MMA
+// halves that share every weight slab: per 64-wide k-block, 32 KB of
+// activations and 32 KB of weights feed 2 x 128 x 256 x 64 MACs.  That is 1.5
+// times the work per byte of a 128 x 256 tile, for GEMMs bound by L2 -> SM
+// operand traffic.  TMEM holds both accumulators (all 512 columns); the TMA
+// ring has 3 stages of 64 KB; one tile per CTA.  Same producer / MMA /
+// epilogue roles as gemm_tc_kernel.
+// ---------------------------------------------------------------------------
+constexpr int M2_ROWS = 256, M2_STAGES = 3;
+constexpr uint32_t M2_A_BYTES = M2_ROWS * BK * 2, M2_B_BYTES = 256 * BK * 2;
+constexpr size_t m2_smem_bytes() { return 1024 + size_t(M2_STAGES) * (M2_A_BYTES + M2_B_BYTES) + 256; }
+
+template <int EPI, bool WROW>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_m256_kernel(const __grid_constant__ CUtensorMap tmAct, const __grid_constant__ CUtensorMap tmW,
+                        const __grid_constant__ CUtensorMap tmC, TcArgs a) {
+  static_assert(EPI == EPI_NONE || EPI == EPI_SILU, "plain or SiluAndMul epilogue");
+  constexpr int BN = 256, STAGES = M2_STAGES;
+  constexpr uint32_t A_BYTES = M2_A_BYTES, B_BYTES = M2_B_BYTES, TMEM_COLS = 512;
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = sm;
+  uint8_t* sB = sm + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* consumed = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  auto bar_full = [&](int s) { return smem_u32(bars + s); };
+  auto bar_empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  const uint32_t bar_done = smem_u32(bars + 2 * STAGES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lin = blockIdx.x;
+  const int tile_p = a.p_fastest ? lin % a.p_tiles : lin / a.q_tiles;   // 256-row block
+  const int tile_q = a.p_fastest ? lin / a.p_tiles : lin % a.q_tiles;
+  const int nk = a.kblocks_total;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    *consumed = 0;
+    fence_mbar_init();
+    prefetch_map(&tmAct);
+    prefetch_map(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_trigger();   // the next kernel may start its prologue
+  int issued = 0;
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    int r_s = 0;
+    int64_t jl0 = 0;
+    if (EPI == EPI_SILU) {
+      r_s = tile_q / a.silu_tps;
+      jl0 = int64_t(tile_q % a.silu_tps) * (BN / 2);
+    }
+    auto load_w = [&](int kb, int s) {   // weight slab (constants)
+      int xw, rw = 0;
+      if (WROW) {
+        rw = kb / a.kpb;
+        xw = (kb % a.kpb) * BK;
+      } else {
+        xw = kb * BK;
+      }
+      const uint32_t dW = smem_u32(sB + s * B_BYTES);
+      if (EPI == EPI_SILU) {
+        const int64_t g0 = int64_t(r_s) * 2 * a.i_l + jl0;
+        tma_load_2d(dW, &tmW, bar_full(s), xw, int(g0));
+        tma_load_2d(dW + B_BYTES / 2, &tmW, bar_full(s), xw, int(g0 + a.i_l));
+      } else if (WROW) {
+        tma_load_3d(dW, &tmW, bar_full(s), xw, tile_q * BN, rw);
+      } else {
+        tma_load_2d(dW, &tmW, bar_full(s), xw, tile_q * BN);
+      }
+    };
+    auto load_act = [&](int kb, int s) {   // 256 activation rows (written by the previous kernel)
+      const int xa = WROW ? int((kb / a.kpb) * a.k_shard) + (kb % a.kpb) * BK : kb * BK;
+      tma_load_2d(smem_u32(sA + s * A_BYTES), &tmAct, bar_full(s), xa, tile_p * M2_ROWS);
+    };
+    const int npre = nk < STAGES ? nk : STAGES;
+    for (int i = 0; i < npre; ++i) {
+      mbar_expect_tx(bar_full(i), A_BYTES + B_BYTES);
+      load_w(i, i);
+    }
+    pdl_wait();
+    for (int i = 0; i < npre; ++i) load_act(i, i);
+    issued = npre;
+    for (int kb = npre; kb < nk; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = (kb / STAGES) & 1;
+      if (!mbar_wait(bar_empty(s), ph ^ 1, 1u)) {
+        *abort_flag = 1;
+        break;
+      }
+      if (*abort_flag) break;
+      mbar_expect_tx(bar_full(s), A_BYTES + B_BYTES);
+      load_w(kb, s);
+      load_act(kb, s);
+      issued = kb + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer: two 128-row halves per weight slab ----------------
+    constexpr uint32_t idesc = idesc_bf16(BM, BN);
+    int kb = 0;
+    for (; kb < nk; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = (kb / STAGES) & 1;
+      if (!mbar_wait(bar_full(s), ph, 2u)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t da0 = sw128_desc(smem_u32(sA + s * A_BYTES));
+      const uint64_t da1 = sw128_desc(smem_u32(sA + s * A_BYTES) + uint32_t(BM) * 128u);   // rows 128 .. 255
+      const uint64_t db = sw128_desc(smem_u32(sB + s * B_BYTES));
+#pragma unroll
+      for (int k = 0; k < BK / UMMA_K; ++k) {
+        umma_bf16(tmem, da0 + uint64_t(2 * k), db + uint64_t(2 * k), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        umma_bf16(tmem + uint32_t(BN), da1 + uint64_t(2 * k), db + uint64_t(2 * k), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+      }
+      umma_commit(bar_empty(s));
+    }
+    *consumed = kb;
+    umma_commit(bar_done);
+  } else if (warp >= 2) {
+    // ---------------- epilogue: both halves ----------------
+    const bool ok = mbar_wait(bar_done, 0, 4u);
+    tc_fence_after();
+    const int quarter = warp & 3;
+    const bool zero = !ok || nk <= 0;
+    BoxStore bs{smem_u32(sA) + uint32_t(quarter) * 2u * P_STAGE_BOX, lane};   // the drained ring
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(h * BN);
+      const int64_t m0 = int64_t(tile_p) * M2_ROWS + h * BM + quarter * 32;   // this warp's first row
+      if (EPI == EPI_NONE) {
+        if (a.tma_store) epi_store_tma(bs, &tmC, trow, BN, m0, a.M, int64_t(tile_q) * BN, a.N, zero);
+        else epi_store_direct(trow, BN, m0 + lane, a, int64_t(tile_q) * BN, zero);
+      } else {
+        epi_silu_direct(trow, BN / 2, m0 + lane, a, tile_q / a.silu_tps, int64_t(tile_q % a.silu_tps) * (BN / 2), !zero);
+      }
+    }
+    if (EPI == EPI_NONE) bs.finish();
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // drain copies that were issued but never consumed
+    for (int kb = *consumed; kb < issued; ++kb) mbar_wait(bar_full(kb % STAGES), (kb / STAGES) & 1, 8u);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -1519,6 +1753,34 @@ int launch_tc(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArgs& ar
   return check_launch("gemm_tc_kernel");
 }
 
+template <int EPI, bool WROW>
+int launch_tc_m256(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArgs& args_in, cudaStream_t st) {
+  auto kern = tc::gemm_tc_m256_kernel<EPI, WROW>;
+  constexpr size_t smem = tc::m2_smem_bytes();
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    configured = true;
+  }
+  tc::TcArgs args = args_in;
+  CUtensorMap mC = act;   // (unused unless args.tma_store)
+  args.tma_store = 0;
+  if (EPI == tc::EPI_NONE) {
+    const int rc = output_map<EPI>(&mC, args);
+    if (rc) return rc;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(args.p_tiles * args.q_tiles), 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.numAttrs = 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, act, w, mC, args);
+  if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "gemm_tc_m256_kernel launch: %s", cudaGetErrorString(e));
+  return check_launch("gemm_tc_m256_kernel");
+}
+
 static int gv_device_sms();
 
 // The persistent prefill GEMM (gemm_tc_persist_kernel) replaces the one-tile-
@@ -1619,6 +1881,16 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
       if (epi == QW_EPI_SILU_MUL) return launch_tc_persist<tc::EPI_SILU, false>(mA, mW, a, st);
       if (wrow) return launch_tc_persist<tc::EPI_NONE, true>(mA, mW, a, st);
       return launch_tc_persist<tc::EPI_NONE, false>(mA, mW, a, st);
+    }
+    // 256-row tiles while they still fill every SM at least once
+    const int64_t p256 = (M + tc::M2_ROWS - 1) / tc::M2_ROWS;
+    if (p256 * a.q_tiles >= gv_device_sms()) {
+      rc = make_map(&mA, A, 2, uint64_t(K), uint64_t(M), 1, uint64_t(K) * 2, 0, uint32_t(tc::M2_ROWS));
+      if (rc) return rc;
+      a.p_tiles = int(p256);
+      if (epi == QW_EPI_SILU_MUL) return launch_tc_m256<tc::EPI_SILU, false>(mA, mW, a, st);
+      if (wrow) return launch_tc_m256<tc::EPI_NONE, true>(mA, mW, a, st);
+      return launch_tc_m256<tc::EPI_NONE, false>(mA, mW, a, st);
     }
     if (epi == QW_EPI_SILU_MUL) return launch_tc<256, 4, false, tc::EPI_SILU, false>(mA, mW, a, 1, st);
     if (wrow) return launch_tc<256, 4, false, tc::EPI_NONE, true>(mA, mW, a, 1, st);

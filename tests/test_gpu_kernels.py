@@ -292,12 +292,17 @@ def test_add_rmsnorm_gemm(L, M, N, K, tp, epi, with_res):
     (333, 800, 128, 2, 0, 1),       # SiluAndMul, I/tp = 200: a half-filled last tile per shard
     (333, 512, 128, 2, 0, 1),       # SiluAndMul, I/tp = 128: tensor-store epilogue, ragged rows
     (4096, 4096, 64, 1, 0, 0),      # one k-block per tile: the ring spans tile boundaries
-    (16384, 6144, 1024, 2, 0, 1),   # the 0.6B prefill gate_up: 20 tiles per CTA
+    (16384, 6144, 1024, 2, 0, 1),   # the 0.6B prefill gate_up: 20 tiles per CTA (256-row tiles by default)
+    (2000, 5120, 256, 1, 0, 0),     # 256-row tiles: the last one's second half partly past M
+    (1800, 5200, 128, 1, 0, 0),     # 256-row tiles: second half wholly past M, ragged N
+    (2000, 4864, 512, 2, 1, 0),     # 256-row tiles, row split
+    (2100, 8192, 256, 2, 0, 1),     # 256-row tiles, SiluAndMul
+    (2560, 4000, 128, 2, 0, 1),     # 256-row tiles, SiluAndMul with I/tp = 1000 (ragged per shard)
 ])
 def test_gemm_persistent_equals_one_tile_kernel(L, monkeypatch, M, N, K, tp, mode, epi):
     """The persistent prefill GEMM (QW_TC_PERSISTENT=1) accumulates each tile
-    in the same k order as the one-tile-per-CTA kernel, which the oracle tests
-    above cover: the outputs must agree bit for bit."""
+    in the same k order as the default kernels (one 128- or 256-row tile per
+    CTA), which the oracle tests above cover: the outputs must agree bit for bit."""
     g = torch.Generator(device="cuda").manual_seed(7)
     A = (torch.randn(M, K, device="cuda", generator=g) * 0.5).to(torch.bfloat16)
     W = (torch.randn(*((tp, N, K // tp) if mode == 1 else (N, K)), device="cuda", generator=g) * 0.05).to(torch.bfloat16)
