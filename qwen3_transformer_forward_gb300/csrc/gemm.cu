@@ -2297,6 +2297,9 @@ extern "C" int qw_qkv_gemm_norm_rope_store_kv(const void* A, const void* W, int6
   a.tp = tp;
   // persistent: one CTA per SM, two TMEM accumulators, so each tile's longer
   // epilogue runs while the MMAs of the CTA's next tile proceed
+  // (on the persistent kernel, where the epilogue overlaps the next tile's
+  // mainloop; a one-tile 256-row version measured slower: 20.5 against 19.6 ms
+  // for the 8 x 2048 prefill)
   return launch_tc_persist<tc::EPI_QKV, false>(mA, mW, a, static_cast<cudaStream_t>(stream));
 }
 

@@ -193,9 +193,10 @@ class Qwen3Forward:
         self._history_ready = True
         self._fused = None     # (layer table, workspace), built on first use
         # prefill: QK-norm + RoPE + KV store in the QKV GEMM's epilogue (persistent
-        # tensor-core kernel; 8 x 2048 tokens: 166 us per layer against 197 us for the
-        # GEMM and the standalone kernel; the same results bit for bit)
-        self.fused_qkv = True
+        # tensor-core kernel, the same results bit for bit); off by default: once
+        # the plain QKV GEMM ran on 256-row tiles, it and the standalone kernel
+        # took 19.4 ms per 8 x 2048-token prefill against 19.6 ms fused
+        self.fused_qkv = False
         # prefill in five kernels per layer (QK-norm + RoPE + KV store in the QKV GEMM's
         # epilogue, residual add + RMSNorm in the o_proj and down GEMMs' epilogues);
         # off by default: on GB300 the longer epilogues, run after each tile's

@@ -30,7 +30,9 @@ def decode_meta(seq_lens, step: int, extra: int):
 
 
 def run_gpu(m, seq_lens, decode_steps: int, params=None, forced=None, device="cuda", fused_decode=False,
-            fwd_out=None) -> Trace:
+            fwd_out=None, prefill_fusion=False) -> Trace:
+    """prefill_fusion: the opt-in prefill epilogues (QK-norm + RoPE + KV store in
+    the QKV GEMM, residual add + RMSNorm in the o_proj and down GEMMs)."""
     from qwen3_transformer_forward_gb300 import model as M
     from qwen3_transformer_forward_gb300 import _lib as L
     params = params or M.load_params(m, device=device)
@@ -39,6 +41,7 @@ def run_gpu(m, seq_lens, decode_steps: int, params=None, forced=None, device="cu
     fwd = M.Qwen3Forward(m, params, max_tokens=sum(seq_lens), num_slots=b.num_slots, max_seqs=B,
                          max_context=max(seq_lens) + decode_steps)
     fwd.fused_decode = fused_decode
+    fwd.fused_qkv = fwd.fused_prefill = prefill_fusion
     if fwd_out is not None:
         fwd_out.append(fwd)
     ctx = M.to_device_prefill(b, device)

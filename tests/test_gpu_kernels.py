@@ -784,7 +784,9 @@ def test_lm_head_with_last_token_select(L, tp, n_out):
 
 
 @pytest.mark.parametrize("T,nh,nkv,tp", [(1, 16, 8, 2), (300, 16, 8, 2), (1000, 16, 8, 1), (257, 8, 8, 2),
-                                         (129, 32, 8, 2)])
+                                         (129, 32, 8, 2),
+                                         (2500, 16, 8, 2),    # 256-row tiles, the last one's second half partial
+                                         (4200, 32, 8, 2)])   # 256-row tiles, the last one's second half past T
 def test_qkv_gemm_epilogue_equals_two_step_path(L, T, nh, nkv, tp):
     """qw_qkv_gemm_norm_rope_store_kv against qw_gemm + qw_qkv_norm_rope_store_kv:
     q, both caches (NaN-poisoned rows left alone) and the error count identical

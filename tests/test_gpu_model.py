@@ -81,15 +81,17 @@ def test_tiny_fp32_model_prefill_and_decode():
 SMALL_BF16 = si.QWEN3_0_6B.replace(vocab=8192, n_layers=3, tp=2, gamma_sigma=0.1)
 
 
-@pytest.mark.parametrize("tp,fused", [(1, True), (2, True), (2, False)])
-def test_small_bf16_model_prefill_and_decode(tp, fused):
+@pytest.mark.parametrize("tp,fused,prefill_fusion", [(1, True, False), (2, True, False), (2, False, False),
+                                                     (2, False, True)])
+def test_small_bf16_model_prefill_and_decode(tp, fused, prefill_fusion):
     """fused: decode steps through the one-kernel decode step (qw_decode_layers),
-    else through the per-operation entry points."""
+    else through the per-operation entry points.  prefill_fusion: the prefill
+    through the opt-in fused epilogues (five kernels per layer)."""
     m = SMALL_BF16.replace(tp=tp)
     seq_lens = [37, 130, 1, 64]
     steps = 3
     forced = forced_tokens(m, steps, len(seq_lens))
-    g = run_gpu(m, seq_lens, steps, forced=forced, fused_decode=fused)
+    g = run_gpu(m, seq_lens, steps, forced=forced, fused_decode=fused, prefill_fusion=prefill_fusion)
     o = run_oracle(m, seq_lens, steps, forced=forced, weights=O.load_weights(m))
     par = Parity(f"small3_tp{tp}")
     for s in range(steps + 1):
