@@ -823,15 +823,16 @@ __global__ void __launch_bounds__(192, 1)
 // activations and 32 KB of weights feed 2 x 128 x 256 x 64 MACs.  That is 1.5
 // times the work per byte of a 128 x 256 tile, for GEMMs bound by L2 -> SM
 // operand traffic.  TMEM holds both accumulators (all 512 columns); the TMA
-// ring has 3 stages of 64 KB; one tile per CTA.  Same producer / MMA /
-// epilogue roles as gemm_tc_kernel.
+// ring has 3 stages of 64 KB; one tile per CTA.  Same producer / MMA roles as
+// gemm_tc_kernel, with two epilogue warpgroups draining the halves side by side.
+constexpr int M2_THREADS = 320;
 // ---------------------------------------------------------------------------
 constexpr int M2_ROWS = 256, M2_STAGES = 3;
 constexpr uint32_t M2_A_BYTES = M2_ROWS * BK * 2, M2_B_BYTES = 256 * BK * 2;
 constexpr size_t m2_smem_bytes() { return 1024 + size_t(M2_STAGES) * (M2_A_BYTES + M2_B_BYTES) + 256; }
 
 template <int EPI, bool WROW>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(M2_THREADS, 1)
     gemm_tc_m256_kernel(const __grid_constant__ CUtensorMap tmAct, const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmC, TcArgs a) {
   static_assert(EPI == EPI_NONE || EPI == EPI_SILU, "plain or SiluAndMul epilogue");
@@ -955,14 +956,15 @@ __global__ void __launch_bounds__(192, 1)
     *consumed = kb;
     umma_commit(bar_done);
   } else if (warp >= 2) {
-    // ---------------- epilogue: both halves ----------------
+    // ---------------- epilogue: warps 2-5 drain half 0, warps 6-9 half 1 ----------------
     const bool ok = mbar_wait(bar_done, 0, 4u);
     tc_fence_after();
-    const int quarter = warp & 3;
+    const int quarter = warp & 3;   // TMEM lanes this warp may access
+    const int h = (warp - 2) >> 2;
     const bool zero = !ok || nk <= 0;
-    BoxStore bs{smem_u32(sA) + uint32_t(quarter) * 2u * P_STAGE_BOX, lane};   // the drained ring
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
+    // staging boxes in the drained ring, two per warp
+    BoxStore bs{smem_u32(sA) + uint32_t(warp - 2) * 2u * P_STAGE_BOX, lane};
+    {
       const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(h * BN);
       const int64_t m0 = int64_t(tile_p) * M2_ROWS + h * BM + quarter * 32;   // this warp's first row
       if (EPI == EPI_NONE) {
@@ -1772,7 +1774,7 @@ int launch_tc_m256(const CUtensorMap& act, const CUtensorMap& w, const tc::TcArg
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(args.p_tiles * args.q_tiles), 1, 1);
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(tc::M2_THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.numAttrs = 0;
