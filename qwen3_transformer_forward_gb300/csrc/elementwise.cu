@@ -250,27 +250,36 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_hd128_kernel(
     gamma = k_gamma;
   }
   const int i0 = 8 * sub;
+  // every load that does not depend on another first: the position, the slot
+  // and v (kv heads), the head's elements and gamma; then the RoPE row
+  const int64_t pos = positions[tok];
+  const int64_t slot = is_q ? -1 : slots[tok];
+  uint4 va = make_uint4(0u, 0u, 0u, 0u), vb = va;
+  if (!is_q) {
+    const bf16* vs = src + int64_t(nkv_l) * HD;   // v: bit copy
+    va = *reinterpret_cast<const uint4*>(vs + 2 * i0);
+    vb = *reinterpret_cast<const uint4*>(vs + 2 * i0 + 8);
+  }
   float x1[8], x2[8];
   load16(src + i0, x1);
   load16(src + HALF + i0, x2);
+  float g1[8], g2[8];
+  load16(gamma + i0, g1);
+  load16(gamma + HALF + i0, g2);
+  const bool pos_ok = pos >= 0 && pos < max_pos;
+  const float* cs = cos_sin + (pos_ok ? pos : 0) * HD;
+  float c[8], sn[8];
+  *reinterpret_cast<float4*>(c) = *reinterpret_cast<const float4*>(cs + i0);
+  *reinterpret_cast<float4*>(c + 4) = *reinterpret_cast<const float4*>(cs + i0 + 4);
+  *reinterpret_cast<float4*>(sn) = *reinterpret_cast<const float4*>(cs + HALF + i0);
+  *reinterpret_cast<float4*>(sn + 4) = *reinterpret_cast<const float4*>(cs + HALF + i0 + 4);
   // lane `sub` holds partial `sub`; the xor tree forms qk_ss_tree's balanced sum in every lane
   float ss = qk_ss8(x1, x2);
   ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 1));
   ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 2));
   ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 4));
   const float inv = qk_inv_rms(ss, eps);
-  const int64_t pos = positions[tok];
-  const bool pos_ok = pos >= 0 && pos < max_pos;
   if (!pos_ok && sub == 0 && h == 0 && err != nullptr) atomicAdd(err, 1);
-  const float* cs = cos_sin + (pos_ok ? pos : 0) * HD;
-  float g1[8], g2[8];
-  load16(gamma + i0, g1);
-  load16(gamma + HALF + i0, g2);
-  float c[8], sn[8];
-  *reinterpret_cast<float4*>(c) = *reinterpret_cast<const float4*>(cs + i0);
-  *reinterpret_cast<float4*>(c + 4) = *reinterpret_cast<const float4*>(cs + i0 + 4);
-  *reinterpret_cast<float4*>(sn) = *reinterpret_cast<const float4*>(cs + HALF + i0);
-  *reinterpret_cast<float4*>(sn + 4) = *reinterpret_cast<const float4*>(cs + HALF + i0 + 4);
   float y1[8], y2[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) qk_rope_pair(x1[e], x2[e], inv, g1[e], g2[e], c[e], sn[e], pos_ok, y1[e], y2[e]);
@@ -280,7 +289,6 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_hd128_kernel(
     store16(o + HALF + i0, y2);
     return;
   }
-  const int64_t slot = slots[tok];
   if (slot == -1) return;                                                    // padding: not stored
   if (slot < 0 || slot >= num_slots || !pos_ok) {
     if (sub == 0 && g == 0 && err != nullptr && (slot < 0 || slot >= num_slots)) atomicAdd(err, 1);
@@ -290,9 +298,8 @@ __global__ void __launch_bounds__(256) qkv_norm_rope_hd128_kernel(
   bf16* vd = v_cache + (slot * nkv + g) * int64_t(HD);
   store16(kd + i0, y1);
   store16(kd + HALF + i0, y2);
-  const bf16* vs = src + int64_t(nkv_l) * HD;                                // v: bit copy
-  *reinterpret_cast<uint4*>(vd + 2 * i0) = *reinterpret_cast<const uint4*>(vs + 2 * i0);
-  *reinterpret_cast<uint4*>(vd + 2 * i0 + 8) = *reinterpret_cast<const uint4*>(vs + 2 * i0 + 8);
+  *reinterpret_cast<uint4*>(vd + 2 * i0) = va;
+  *reinterpret_cast<uint4*>(vd + 2 * i0 + 8) = vb;
 }
 
 // ===========================================================================
