@@ -835,7 +835,7 @@ template <int EPI, bool WROW>
 __global__ void __launch_bounds__(M2_THREADS, 1)
     gemm_tc_m256_kernel(const __grid_constant__ CUtensorMap tmAct, const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmC, TcArgs a) {
-  static_assert(EPI == EPI_NONE || EPI == EPI_SILU, "plain or SiluAndMul epilogue");
+  static_assert(EPI == EPI_NONE || EPI == EPI_SILU || EPI == EPI_ADDNORM, "plain, SiluAndMul or add + RMSNorm");
   constexpr int BN = 256, STAGES = M2_STAGES;
   constexpr uint32_t A_BYTES = M2_A_BYTES, B_BYTES = M2_B_BYTES, TMEM_COLS = 512;
   extern __shared__ uint8_t smem_dyn[];
@@ -970,11 +970,67 @@ __global__ void __launch_bounds__(M2_THREADS, 1)
       if (EPI == EPI_NONE) {
         if (a.tma_store) epi_store_tma(bs, &tmC, trow, BN, m0, a.M, int64_t(tile_q) * BN, a.N, zero);
         else epi_store_direct(trow, BN, m0 + lane, a, int64_t(tile_q) * BN, zero);
+      } else if (EPI == EPI_ADDNORM) {
+        // pass 1: the new residual s = round(round(acc) + resid) of this CTA's 256
+        // columns, written back in place, and its sum of squares (in column order)
+        // left in shared memory for the cluster (the ring is free: every MMA has completed)
+        const int64_t m = m0 + lane;
+        float ss = 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(trow + c, r);
+          tmem_ld_wait();
+          if (m >= a.M) continue;
+          bf16* rp = a.resid + m * a.ldc + int64_t(tile_q) * BN + c;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float x[8], f[8];
+            load16(rp + 8 * v, x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float o = zero ? 0.0f : round_t<bf16>(__uint_as_float(r[8 * v + e]));
+              f[e] = round_t<bf16>(__fadd_rn(o, x[e]));
+              ss = __fadd_rn(ss, __fmul_rn(f[e], f[e]));
+            }
+            store16(rp + 8 * v, f);
+          }
+        }
+        reinterpret_cast<float*>(sA)[h * BM + quarter * 32 + lane] = ss;
       } else {
         epi_silu_direct(trow, BN / 2, m0 + lane, a, tile_q / a.silu_tps, int64_t(tile_q % a.silu_tps) * (BN / 2), !zero);
       }
     }
     if (EPI == EPI_NONE) bs.finish();
+  }
+
+  if (EPI == EPI_ADDNORM) {
+    // the row's sum of squares over the cluster's CTAs (rank order), then pass 2:
+    // y = round(s * rsqrt(mean(s^2) + eps) * gamma) over this CTA's columns
+    __syncwarp();
+    cluster_sync_all();
+    if (warp >= 2) {
+      const int row = ((warp - 2) >> 2) * BM + (warp & 3) * 32 + lane;
+      const int64_t m = int64_t(tile_p) * M2_ROWS + row;
+      const uint32_t base = smem_u32(sA) + uint32_t(row) * 4u;
+      float tot = 0.0f;
+      for (int r = 0; r < a.q_tiles; ++r) tot = __fadd_rn(tot, ld_cluster_f32(map_to_rank(base, uint32_t(r))));
+      const float inv = rsqrtf(__fadd_rn(__fdiv_rn(tot, float(a.N)), a.eps));
+      if (m < a.M) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 8) {
+          const int64_t n0 = int64_t(tile_q) * BN + c;
+          float x[8], g[8], y[8];
+          load16(a.resid + m * a.ldc + n0, x);
+          load16(a.norm_gamma + n0, g);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(x[e], inv), g[e]);
+          store16(a.y_out + m * a.ldc + n0, y);
+        }
+      }
+    }
+    // keep every CTA's shared memory alive until all ranks have read it
+    cluster_sync_all();
   }
 
   __syncwarp();
@@ -2211,17 +2267,25 @@ extern "C" int qw_gemm_add_rmsnorm(const void* A, const void* W, int64_t M, int6
   a.resid = static_cast<bf16*>(residual);
   a.y_out = static_cast<bf16*>(y);
   a.norm_gamma = static_cast<const bf16*>(gamma);
-  auto kern = tc::gemm_tc_kernel<256, 4, false, tc::EPI_ADDNORM, true>;
-  constexpr size_t smem = tc::smem_bytes<256, 4>();
-  static bool configured = false;
-  if (!configured) {
+  // 256-row tiles while they still fill every SM at least once
+  const int64_t p256 = (M + tc::M2_ROWS - 1) / tc::M2_ROWS;
+  const bool m256 = p256 * a.q_tiles >= gv_device_sms();
+  if (m256) {
+    rc = make_map(&mA, A, 2, uint64_t(K), uint64_t(M), 1, uint64_t(K) * 2, 0, uint32_t(tc::M2_ROWS));
+    if (rc) return rc;
+    a.p_tiles = int(p256);
+  }
+  auto kern = m256 ? tc::gemm_tc_m256_kernel<tc::EPI_ADDNORM, true> : tc::gemm_tc_kernel<256, 4, false, tc::EPI_ADDNORM, true>;
+  const size_t smem = m256 ? tc::m2_smem_bytes() : tc::smem_bytes<256, 4>();
+  static bool configured[2] = {false, false};
+  if (!configured[m256]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return set_error(QW_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    configured = true;
+    configured[m256] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(a.p_tiles * a.q_tiles), 1, 1);
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(m256 ? tc::M2_THREADS : 192, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];

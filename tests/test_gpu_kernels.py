@@ -831,7 +831,8 @@ def test_qkv_gemm_epilogue_equals_two_step_path(L, T, nh, nkv, tp):
 
 
 @pytest.mark.parametrize("M,N,K,tp", [(1, 1024, 2048, 2), (300, 1024, 2048, 2), (130, 1024, 3072, 2),
-                                      (200, 512, 1024, 1), (257, 2048, 1024, 4)])
+                                      (200, 512, 1024, 1), (257, 2048, 1024, 4),
+                                      (9800, 1024, 2048, 2)])   # 256-row tiles, the last one partial
 def test_gemm_add_rmsnorm(L, M, N, K, tp):
     """Row-parallel GEMM + residual add + RMSNorm in one launch, against the two
     calls it replaces (qw_gemm ROW_REDUCE on at least 128 rows, the same tile
