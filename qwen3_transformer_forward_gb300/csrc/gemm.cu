@@ -1418,7 +1418,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
   constexpr int GV_MAXC = MAXC;
   __shared__ float red[GV_WARPS][16 * TL][NT * 8];
   extern __shared__ __align__(16) uint8_t gv_dyn[];
-  bf16* ys = reinterpret_cast<bf16*>(gv_dyn);   // NORM, STAGE: [M][K + GV_YPAD]
+  bf16* ys = reinterpret_cast<bf16*>(gv_dyn);   // NORM, STAGE: [M][K + GV_YPAD]; NORM with res_in: then res_in rows
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   // the two weight rows of this thread in each row tile (m16 tile rows g and g + 8)
   int64_t rowA[TL], rowB[TL];
@@ -1466,11 +1466,17 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
       }
   };
   __shared__ uint64_t stage_bar;   // STAGE: completion of the activation copies
+  __shared__ uint64_t norm_bar[GV_WARPS];   // NORM: completion of warp w's token rows
   if (STAGE) {
     if (threadIdx.x == 0) {
       tcx::mbar_init(smem_u32(&stage_bar), 1);
       tcx::fence_mbar_init();
     }
+    __syncthreads();
+  }
+  if (NORM) {
+    if (threadIdx.x < GV_WARPS) tcx::mbar_init(smem_u32(&norm_bar[threadIdx.x]), 1);
+    tcx::fence_mbar_init();
     __syncthreads();
   }
   // the first weights are constants: load them before the dependency wait
@@ -1479,19 +1485,41 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
   pdl_trigger();   // only now may the next kernel start its prologue
   const int ys_stride = K + GV_YPAD;
   if (NORM) {
-    // y = RMSNorm(h + res_in) * gamma for every token, into shared memory
+    // Warp w copies the rows of its tokens w, w + 8, ... (h, and res_in into rs)
+    // by bulk copies on its own mbarrier, then norms them from shared memory.
+    bf16* rs = ys + M * ys_stride;   // res_in rows
+    {
+      const uint32_t sb = smem_u32(&norm_bar[warp]);
+      if (lane == 0 && warp < M) {
+        const uint32_t ntk = uint32_t((M - 1 - warp) / GV_WARPS + 1);
+        tcx::mbar_expect_tx(sb, ntk * uint32_t(K) * (na.res_in != nullptr ? 4u : 2u));
+        for (int r = warp; r < M; r += GV_WARPS) {
+          asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                           smem_u32(ys + r * ys_stride)),
+                       "l"(A + int64_t(r) * K), "r"(uint32_t(K) * 2u), "r"(sb)
+                       : "memory");
+          if (na.res_in != nullptr)
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                             smem_u32(rs + r * ys_stride)),
+                         "l"(na.res_in + int64_t(r) * K), "r"(uint32_t(K) * 2u), "r"(sb)
+                         : "memory");
+        }
+      }
+      if (warp < M) tc::mbar_wait(sb, 0, 16u);
+    }
+    // y = RMSNorm(h + res_in) * gamma for every token, in place in ys
     for (int tk = warp; tk < M; tk += GV_WARPS) {
-      const bf16* hr = A + int64_t(tk) * K;
-      const bf16* rr = na.res_in != nullptr ? na.res_in + int64_t(tk) * K : nullptr;
+      const bf16* hr = ys + tk * ys_stride;
+      const bf16* rr = na.res_in != nullptr ? rs + tk * ys_stride : nullptr;
       float ss = 0.0f;
       for (int k0v = lane * 8; k0v < K; k0v += 4 * 256) {
         uint4 hv[4], rv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {   // a pass's loads all in flight before use
+        for (int i = 0; i < 4; ++i) {
           const int k = k0v + i * 256;
           if (k < K) {
-            hv[i] = __ldcg(reinterpret_cast<const uint4*>(hr + k));
-            if (rr != nullptr) rv[i] = __ldcg(reinterpret_cast<const uint4*>(rr + k));
+            hv[i] = *reinterpret_cast<const uint4*>(hr + k);
+            if (rr != nullptr) rv[i] = *reinterpret_cast<const uint4*>(rr + k);
           }
         }
 #pragma unroll
@@ -2068,7 +2096,7 @@ int norm_gemm_bf16(const bf16* x, const NormArgs& na, const bf16* W, bf16* C, in
   if (two_tiles) blocks = (blocks + 1) / 2;
   const int64_t ldc = epi == QW_EPI_SILU_MUL ? N / 2 : N;
   const int64_t i_l = epi == QW_EPI_SILU_MUL ? N / 2 / tp : 0;
-  const size_t smem = size_t(M) * (K + GV_YPAD) * 2;
+  const size_t smem = size_t(M) * (K + GV_YPAD) * 2 * (na.res_in != nullptr ? 2 : 1);
   cudaError_t e = cudaSuccess;
 #define QW_NG_ONE(NTV, EPIV, RPCV, MC, TLV)                                                                      \
   {                                                                                                              \
@@ -2220,8 +2248,9 @@ extern "C" int qw_add_rmsnorm_gemm(const void* x, const void* residual_in, void*
     return set_error(QW_ERR_INVALID_ARG, "qw_add_rmsnorm_gemm: epilogue %d", epilogue);
   if (K % 32 || N % 16 || N % tp || (epilogue == QW_EPI_SILU_MUL && ((N % (2 * tp)) || (N / 2 / tp) % 8)))
     return set_error(QW_ERR_SHAPE, "qw_add_rmsnorm_gemm: K %% 32, N %% 16 and the gate_up split rules");
-  // the normed rows of all tokens sit in shared memory beside the <= 16 KB reduction tile
-  if (size_t(M) * (K + GV_YPAD) * 2 > size_t(211) * 1024)
+  // the rows of all tokens (and of the residual) sit in shared memory beside
+  // the <= 16 KB reduction tile
+  if (size_t(M) * (K + GV_YPAD) * 2 * (residual_in != nullptr ? 2 : 1) > size_t(211) * 1024)
     return set_error(QW_ERR_SHAPE, "qw_add_rmsnorm_gemm: %lld tokens x K %lld exceed shared memory",
                      (long long)M, (long long)K);
   if (M == 0) return QW_OK;

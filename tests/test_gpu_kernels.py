@@ -255,7 +255,9 @@ def test_gemm_bf16(L, M, N, K, tp, mode, epi):
                                                     (1, 4096, 1024, 1, 0, False), (16, 6144, 1024, 2, 1, True),
                                                     (13, 1024, 2048, 2, 0, True), (5, 512, 96, 2, 1, False),
                                                     # 311 groups of 8 outputs: two per CTA, the last CTA half empty
-                                                    (3, 4976, 256, 1, 1, True)])
+                                                    (3, 4976, 256, 1, 1, True),
+                                                    # x and residual rows near the shared-memory limit (197 KB)
+                                                    (16, 512, 3072, 1, 0, True)])
 def test_add_rmsnorm_gemm(L, M, N, K, tp, epi, with_res):
     """Fused add + RMSNorm + column Linear (decode QKV / gate_up) against the
     oracle's add_rms_norm followed by the oracle Linear."""
