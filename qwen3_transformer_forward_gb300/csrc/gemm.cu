@@ -1403,6 +1403,14 @@ struct NormArgs {
   float eps;
 };
 constexpr int GV_YPAD = 8;   // y row padding (elements): 16-byte rows at distinct bank groups
+// WTMA weight rows in shared memory: stride K + gv_wpad(K) elements, an odd
+// multiple of 64 bytes, so the two rows a quarter-warp's 16-byte reads touch
+// fall in opposite halves of the banks (K % 32 == 0)
+__host__ __device__ constexpr int gv_wpad(int K) { return K % 64 == 0 ? 32 : 0; }
+// byte offset of the WTMA weight rows: after the staged (NORM: and residual) rows
+__host__ __device__ constexpr size_t gv_wsm_offset(int M, int K, bool norm, bool stage, bool res) {
+  return (norm || stage) ? size_t(M) * (K + GV_YPAD) * 2 * (norm && res ? 2 : 1) : 0;
+}
 
 // TL: m16 row tiles per CTA (2 only with SiluAndMul: 16 outputs per CTA, half
 // the CTAs, so a norm prologue runs in one wave).
@@ -1410,7 +1418,12 @@ constexpr int GV_YPAD = 8;   // y row padding (elements): 16-byte rows at distin
 // unit) per token row completing on an mbarrier, all in flight at once
 // (otherwise each k chunk's activations are one more L2 round trip before its
 // MMAs; per-thread 16-byte asynchronous copies queue behind the weight loads).
-template <int NT, int EPI, bool WROW, int RPC, int MAXC, bool NORM = false, int TL = 1, bool STAGE = false>
+// WTMA: the CTA's weight rows are bulk-copied into shared memory before the
+// dependency wait (one copy per row, or per shard piece of a row-split
+// weight) instead of being loaded into registers by every thread; the MMAs
+// then read them from shared memory.
+template <int NT, int EPI, bool WROW, int RPC, int MAXC, bool NORM = false, int TL = 1, bool STAGE = false,
+          bool WTMA = false>
 __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
     gemv_mma_kernel(const bf16* __restrict__ A, const bf16* __restrict__ W, bf16* __restrict__ C, int M, int N, int K,
                     int K_l, int64_t ldc, int64_t i_l, NormArgs na) {
@@ -1453,6 +1466,9 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
   for (int tl = 0; tl < TL; ++tl)
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[tl][n][0] = acc[tl][n][1] = acc[tl][n][2] = acc[tl][n][3] = 0.0f;
+  // WTMA: local row 16 tl + g holds rowA[tl], 16 tl + 8 + g holds rowB[tl]
+  const int ws_stride = K + gv_wpad(K);
+  const bf16* wsm = reinterpret_cast<const bf16*>(gv_dyn + gv_wsm_offset(M, K, NORM, STAGE, na.res_in != nullptr));
   uint4 wa[TL][GV_MAXC], wb[TL][GV_MAXC];
   auto load_w = [&](int kb) {
 #pragma unroll
@@ -1461,8 +1477,16 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
       for (int c = 0; c < GV_MAXC; ++c) {
         const int k = kb + 32 * c + 8 * t;
         const bool in = kb + 32 * c < k1;
-        wa[tl][c] = (in && okA[tl]) ? ldg_stream(wptr(rowA[tl], k)) : make_uint4(0, 0, 0, 0);
-        wb[tl][c] = (RPC == 16 && in && okB[tl]) ? ldg_stream(wptr(rowB[tl], k)) : make_uint4(0, 0, 0, 0);
+        if (WTMA) {
+          wa[tl][c] = (in && okA[tl]) ? *reinterpret_cast<const uint4*>(wsm + (16 * tl + g) * ws_stride + k)
+                                      : make_uint4(0, 0, 0, 0);
+          wb[tl][c] = (RPC == 16 && in && okB[tl])
+                          ? *reinterpret_cast<const uint4*>(wsm + (16 * tl + 8 + g) * ws_stride + k)
+                          : make_uint4(0, 0, 0, 0);
+        } else {
+          wa[tl][c] = (in && okA[tl]) ? ldg_stream(wptr(rowA[tl], k)) : make_uint4(0, 0, 0, 0);
+          wb[tl][c] = (RPC == 16 && in && okB[tl]) ? ldg_stream(wptr(rowB[tl], k)) : make_uint4(0, 0, 0, 0);
+        }
       }
   };
   __shared__ uint64_t stage_bar;   // STAGE: completion of the activation copies
@@ -1479,8 +1503,51 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
     tcx::fence_mbar_init();
     __syncthreads();
   }
-  // the first weights are constants: load them before the dependency wait
-  if (k0 < k1) load_w(k0);
+  __shared__ uint64_t w_bar;   // WTMA: completion of the weight rows' copies
+  if (WTMA) {
+    // global row of local weight row lr (its tile, half and m16 row); false past the outputs
+    auto w_row = [&](int lr, int64_t& row) -> bool {
+      const int tl = lr >> 4, h = (lr >> 3) & 1, gg = lr & 7;
+      if (EPI == tc::EPI_SILU) {
+        const int64_t o0 = (int64_t(blockIdx.x) * TL + tl) * 8;
+        const int64_t r = o0 / i_l, j = o0 % i_l + gg;
+        row = r * 2 * i_l + j + (h ? i_l : 0);
+        return (o0 + gg) < int64_t(N / 2) && j < i_l;
+      }
+      row = int64_t(blockIdx.x) * RPC + 8 * h + gg;
+      return row < N && (h == 0 || RPC == 16);
+    };
+    constexpr int NROWS = (EPI == tc::EPI_SILU || RPC == 16 ? 16 : 8) * TL;
+    const uint32_t wb_ = smem_u32(&w_bar);
+    if (threadIdx.x == 0) {
+      uint32_t bytes = 0;
+      for (int lr = 0; lr < NROWS; ++lr) {
+        int64_t row;
+        if (w_row(lr, row)) bytes += uint32_t(K) * 2u;
+      }
+      tcx::mbar_init(wb_, 1);
+      tcx::fence_mbar_init();
+      tcx::mbar_expect_tx(wb_, bytes);   // <= 32 rows x 2K bytes, far below the 2^20 - 1 limit
+    }
+    __syncthreads();
+    // the weights are constants: their copies start before the dependency wait
+    if (lane == 0)
+      for (int lr = warp; lr < NROWS; lr += GV_WARPS) {
+        int64_t row;
+        if (!w_row(lr, row)) continue;
+        const uint32_t dst = smem_u32(wsm + lr * ws_stride);
+        const int pieces = WROW ? K / K_l : 1;
+        const int len = WROW ? K_l : K;
+        for (int q = 0; q < pieces; ++q)
+          asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                           dst + uint32_t(q * len) * 2u),
+                       "l"(WROW ? W + (int64_t(q) * N + row) * K_l : W + row * int64_t(K)), "r"(uint32_t(len) * 2u),
+                       "r"(wb_)
+                       : "memory");
+      }
+  } else if (k0 < k1) {
+    load_w(k0);   // the first weights are constants: loaded before the dependency wait
+  }
   pdl_wait();      // the activations are complete and visible
   pdl_trigger();   // only now may the next kernel start its prologue
   const int ys_stride = K + GV_YPAD;
@@ -1567,8 +1634,9 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
     }
     tc::mbar_wait(sb, 0, 16u);
   }
+  if (WTMA) tc::mbar_wait(smem_u32(&w_bar), 0, 16u);
   for (int kb = k0; kb < k1; kb += GV_MAXC * 32) {
-    if (kb != k0) load_w(kb);
+    if (WTMA || kb != k0) load_w(kb);
 #pragma unroll
     for (int c = 0; c < GV_MAXC; ++c) {
       if (kb + 32 * c >= k1) break;
@@ -2008,14 +2076,26 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
     // asynchronous copies, 134.2 -> 125.1 ms on moving to one bulk copy per row)
     const size_t stage_smem = size_t(M) * (K + GV_YPAD) * 2;
     const bool stage = M <= 8 && stage_smem <= size_t(200) * 1024;
+  // and the weight rows bulk-copied into shared memory beside them (WTMA)
 #define QW_GV_ONE(NTV, EPIV, WR, RPCV, MC)                                                                     \
   if (NTV == 1 && stage) {                                                                                     \
-    auto kern = gemv_mma_kernel<1, EPIV, WR, RPCV, MC, false, 1, true>;                                        \
-    static size_t allowed = 0;                                                                                 \
-    const int rc_ = gv_allow_smem(reinterpret_cast<const void*>(kern), stage_smem, allowed);                  \
-    if (rc_) return rc_;                                                                                       \
-    e = launch_pdl(kern, dim3(blocks), dim3(GV_WARPS * 32), stage_smem, st, A, W, C, int(M), int(N), int(K),   \
-                   int(Kl), a.ldc, a.i_l, NormArgs{nullptr, nullptr, nullptr, 0.0f});                          \
+    const size_t wsm_ = size_t(EPIV == tc::EPI_SILU || RPCV == 16 ? 16 : 8) * (K + gv_wpad(int(K))) * 2;       \
+    const NormArgs na_{nullptr, nullptr, nullptr, 0.0f};                                                       \
+    if (stage_smem + wsm_ <= size_t(200) * 1024) {                                                             \
+      auto kern = gemv_mma_kernel<1, EPIV, WR, RPCV, 4, false, 1, true, true>;                                 \
+      static size_t allowed = 0;                                                                               \
+      const int rc_ = gv_allow_smem(reinterpret_cast<const void*>(kern), stage_smem + wsm_, allowed);         \
+      if (rc_) return rc_;                                                                                     \
+      e = launch_pdl(kern, dim3(blocks), dim3(GV_WARPS * 32), stage_smem + wsm_, st, A, W, C, int(M), int(N),  \
+                     int(K), int(Kl), a.ldc, a.i_l, na_);                                                      \
+    } else {                                                                                                   \
+      auto kern = gemv_mma_kernel<1, EPIV, WR, RPCV, MC, false, 1, true>;                                      \
+      static size_t allowed = 0;                                                                               \
+      const int rc_ = gv_allow_smem(reinterpret_cast<const void*>(kern), stage_smem, allowed);                \
+      if (rc_) return rc_;                                                                                     \
+      e = launch_pdl(kern, dim3(blocks), dim3(GV_WARPS * 32), stage_smem, st, A, W, C, int(M), int(N), int(K), \
+                     int(Kl), a.ldc, a.i_l, na_);                                                              \
+    }                                                                                                          \
   } else {                                                                                                     \
     e = launch_pdl(gemv_mma_kernel<NTV, EPIV, WR, RPCV, MC>, dim3(blocks), dim3(GV_WARPS * 32), 0, st, A, W, C, \
                    int(M), int(N), int(K), int(Kl), a.ldc, a.i_l, NormArgs{nullptr, nullptr, nullptr, 0.0f}); \
@@ -2100,11 +2180,21 @@ int norm_gemm_bf16(const bf16* x, const NormArgs& na, const bf16* W, bf16* C, in
   cudaError_t e = cudaSuccess;
 #define QW_NG_ONE(NTV, EPIV, RPCV, MC, TLV)                                                                      \
   {                                                                                                              \
-    auto kern = gemv_mma_kernel<NTV, EPIV, false, RPCV, MC, true, TLV>;                                          \
-    static size_t allowed = 0;                                                                                   \
-    const int rc_ = gv_allow_smem(reinterpret_cast<const void*>(kern), smem, allowed);                          \
-    if (rc_) return rc_;                                                                                         \
-    e = launch_pdl(kern, dim3(blocks), dim3(GV_WARPS * 32), smem, st, x, W, C, M, N, K, K, ldc, i_l, na);        \
+    const size_t wsm_ = size_t(EPIV == tc::EPI_SILU || RPCV == 16 ? 16 : 8) * TLV * (K + gv_wpad(K)) * 2;        \
+    if (NTV == 1 && smem + wsm_ <= size_t(200) * 1024) {   /* weight rows bulk-copied into shared memory */      \
+      auto kern = gemv_mma_kernel<1, EPIV, false, RPCV, 4, true, TLV, false, true>;                              \
+      static size_t allowed = 0;                                                                                 \
+      const int rc_ = gv_allow_smem(reinterpret_cast<const void*>(kern), smem + wsm_, allowed);                 \
+      if (rc_) return rc_;                                                                                       \
+      e = launch_pdl(kern, dim3(blocks), dim3(GV_WARPS * 32), smem + wsm_, st, x, W, C, M, N, K, K, ldc, i_l,    \
+                     na);                                                                                        \
+    } else {                                                                                                     \
+      auto kern = gemv_mma_kernel<NTV, EPIV, false, RPCV, MC, true, TLV>;                                        \
+      static size_t allowed = 0;                                                                                 \
+      const int rc_ = gv_allow_smem(reinterpret_cast<const void*>(kern), smem, allowed);                        \
+      if (rc_) return rc_;                                                                                       \
+      e = launch_pdl(kern, dim3(blocks), dim3(GV_WARPS * 32), smem, st, x, W, C, M, N, K, K, ldc, i_l, na);      \
+    }                                                                                                            \
   }
 #define QW_NG(NTV)                                                                                               \
   if (epi == QW_EPI_SILU_MUL) {                                                                                  \
