@@ -1495,6 +1495,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
     if (threadIdx.x == 0) {
       tcx::mbar_init(smem_u32(&stage_bar), 1);
       tcx::fence_mbar_init();
+      tcx::mbar_expect_tx(smem_u32(&stage_bar), uint32_t(M) * uint32_t(K) * 2u);   // before any copy is issued
     }
     __syncthreads();
   }
@@ -1621,12 +1622,12 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
     __syncthreads();
   }
   if (STAGE) {
-    // rows of 2K bytes (K % 32 == 0) to 16-byte aligned rows of ys; the
-    // transaction count M * 2K stays far below the mbarrier's 2^20 - 1 limit
+    // rows of 2K bytes (K % 32 == 0) to 16-byte aligned rows of ys, row r
+    // issued by warp r % 8; the transaction count M * 2K (expected before the
+    // wait) stays far below the mbarrier's 2^20 - 1 limit
     const uint32_t sb = smem_u32(&stage_bar);
-    if (threadIdx.x == 0) {
-      tcx::mbar_expect_tx(sb, uint32_t(M) * uint32_t(K) * 2u);
-      for (int r = 0; r < M; ++r)
+    if (lane == 0) {
+      for (int r = warp; r < M; r += GV_WARPS)
         asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                          smem_u32(ys + r * ys_stride)),
                      "l"(A + int64_t(r) * K), "r"(uint32_t(K) * 2u), "r"(sb)
