@@ -59,7 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--profile-window", action="store_true",
                     help="after the timed region, run one more step between cudaProfilerStart/Stop "
                          "(for ncu --profile-from-start off)")
-    ap.add_argument("--profile-kernel", choices=["decode.attention", "prefill.gemm_gate_up_silu", "prefill.attention"],
+    ap.add_argument("--profile-kernel", choices=["decode.attention", "decode.gemm_down", "prefill.gemm_gate_up_silu",
+                                                 "prefill.attention"],
                     default=None,
                     help="launch only this kernel, --profile-reps times, on inputs of the workload's shape "
                          "(random values, mean decode context) and exit: a small case for ncu section captures")
@@ -942,6 +943,15 @@ def profile_kernel(args):
         for _ in range(args.profile_reps):
             L.attention_decode_rope(qkv, nh, nkv, hd, m.tp, pos, cs, gamma, gamma, m.eps, slots, kc, vc, None, ctx,
                                     base, cap, hd ** -0.5, out, ws)
+    if args.profile_kernel == "decode.gemm_down":   # the decode step's row-split down projection, one weight copy per launch
+        H, I, tp = m.hidden, m.intermediate, m.tp
+        act = rnd(nb, I)
+        ws_ = [(rnd(H, I) * 0.02).to(torch.bfloat16) for _ in range(max(1, args.profile_reps))]   # [tp][H][I/tp] order
+        h = torch.empty(nb, H, dtype=torch.bfloat16, device="cuda")
+        gws = torch.zeros(max(L.gemm_workspace_size(nb, H, I, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, torch.bfloat16),
+                              16), dtype=torch.uint8, device="cuda")
+        for r in range(args.profile_reps):
+            L.gemm(act, ws_[r], h, H, tp, L.QW_GEMM_ROW_REDUCE, L.QW_EPI_NONE, gws)
     if args.profile_kernel == "prefill.gemm_gate_up_silu":   # merged gate_up + SiluAndMul over the prompt tokens
         T, H, I = sum(seqs), m.hidden, m.intermediate
         x = rnd(T, H)
