@@ -413,8 +413,7 @@ int qw_silu_mul(const void* x, void* out, int64_t T, int64_t I, int tp, int dtyp
  *   W bf16 [N, K] (column layout: tp shards stacked along N);  C bf16 [M, N],
  *   or [M, N/2] with QW_EPI_SILU_MUL (gate_up, as qw_gemm)
  * Rules: bf16; 0 <= M <= 16; K % 32 == 0, N % 16 == 0 and qw_gemm's shard
- * rules; M * (K + 8) * 2 <= 211 KiB, twice that with residual_in (the rows
- * of x and residual_in are copied into shared memory and normed there);
+ * rules; M * (K + 8) * 2 <= 211 KiB (the normed rows live in shared memory);
  * 16-byte aligned pointers; residual_out must not alias x or residual_in
  * (every CTA reads them while one writes it).  Otherwise QW_ERR_SHAPE /
  * QW_ERR_INVALID_ARG.

@@ -121,9 +121,6 @@ def test_argument_errors_are_reported_before_launch(lib):
     # 16 tokens of K = 8192 normed rows do not fit in shared memory
     assert lib.qw_add_rmsnorm_gemm(fake, None, None, fake, 1e-6, fake, fake, 16, 64, 8192, 1, 0, L.QW_BF16,
                                    None) == L.QW_ERR_SHAPE
-    # ... nor, with a residual (its rows are staged too), 16 tokens of K = 4096
-    assert lib.qw_add_rmsnorm_gemm(fake, fake, None, fake, 1e-6, fake, fake, 16, 64, 4096, 1, 0, L.QW_BF16,
-                                   None) == L.QW_ERR_SHAPE
     # QKV GEMM with the QK-norm / RoPE / KV-store epilogue: bf16, head_dim 128, an even number of heads per shard
     qg = lambda nh, nkv, hd, tp, dt: (fake, fake, 300, 1024, nh, nkv, hd, tp, fake, fake, 4096, fake, fake, 1e-6,  # noqa: E731
                                       fake, fake, fake, 100, fake, None, dt, None)

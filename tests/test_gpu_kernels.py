@@ -256,7 +256,7 @@ def test_gemm_bf16(L, M, N, K, tp, mode, epi):
                                                     (13, 1024, 2048, 2, 0, True), (5, 512, 96, 2, 1, False),
                                                     # 311 groups of 8 outputs: two per CTA, the last CTA half empty
                                                     (3, 4976, 256, 1, 1, True),
-                                                    # x and residual rows near the shared-memory limit (197 KB)
+                                                    # two tokens per warp, K = 3072 (the down projection's width)
                                                     (16, 512, 3072, 1, 0, True)])
 def test_add_rmsnorm_gemm(L, M, N, K, tp, epi, with_res):
     """Fused add + RMSNorm + column Linear (decode QKV / gate_up) against the
