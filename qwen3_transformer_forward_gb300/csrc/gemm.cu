@@ -1412,8 +1412,9 @@ __host__ __device__ constexpr size_t gv_wsm_offset(int M, int K, bool norm, bool
   return (norm || stage) ? size_t(M) * (K + GV_YPAD) * 2 : 0;
 }
 
-// TL: m16 row tiles per CTA (2 only with SiluAndMul: 16 outputs per CTA, half
-// the CTAs, so a norm prologue runs in one wave).
+// TL: m16 row tiles per CTA (2: SiluAndMul with 16 outputs per CTA, or 32
+// plain output rows; half the CTAs, so a norm prologue runs in one wave and
+// its activation reads are shared by twice the weight rows).
 // STAGE: A [M][K] is copied into shared memory first, one bulk copy (TMA
 // unit) per token row completing on an mbarrier, all in flight at once
 // (otherwise each k chunk's activations are one more L2 round trip before its
@@ -1427,7 +1428,7 @@ template <int NT, int EPI, bool WROW, int RPC, int MAXC, bool NORM = false, int 
 __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
     gemv_mma_kernel(const bf16* __restrict__ A, const bf16* __restrict__ W, bf16* __restrict__ C, int M, int N, int K,
                     int K_l, int64_t ldc, int64_t i_l, NormArgs na) {
-  static_assert(TL == 1 || EPI == tc::EPI_SILU, "two row tiles per CTA only with SiluAndMul");
+  static_assert(TL == 1 || EPI == tc::EPI_SILU || (RPC == 16 && !WROW), "two row tiles: SiluAndMul or 16-row tiles");
   constexpr int GV_MAXC = MAXC;
   __shared__ float red[GV_WARPS][16 * TL][NT * 8];
   extern __shared__ __align__(16) uint8_t gv_dyn[];
@@ -1445,7 +1446,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
       rowB[tl] = rowA[tl] + i_l;                                 // matching up row
       okA[tl] = okB[tl] = (o0 + g) < int64_t(N / 2) && j < i_l;
     } else {
-      rowA[tl] = int64_t(blockIdx.x) * RPC + g;
+      rowA[tl] = (int64_t(blockIdx.x) * TL + tl) * RPC + g;
       rowB[tl] = rowA[tl] + 8;
       okA[tl] = rowA[tl] < N;
       okB[tl] = RPC == 16 && rowB[tl] < N;
@@ -1509,7 +1510,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
         row = r * 2 * i_l + j + (h ? i_l : 0);
         return (o0 + gg) < int64_t(N / 2) && j < i_l;
       }
-      row = int64_t(blockIdx.x) * RPC + 8 * h + gg;
+      row = (int64_t(blockIdx.x) * TL + tl) * RPC + 8 * h + gg;
       return row < N && (h == 0 || RPC == 16);
     };
     constexpr int NROWS = (EPI == tc::EPI_SILU || RPC == 16 ? 16 : 8) * TL;
@@ -1656,12 +1657,12 @@ __global__ void __launch_bounds__(GV_WARPS * 32, MAXC <= 4 ? 2 : 1)
       if (o < N / 2) C[int64_t(tok) * ldc + o] = __float2bfloat16_rn(tc::silu_mul_bf16(gs, us));
     }
   } else {
-    for (int e = threadIdx.x; e < RPC * M; e += GV_WARPS * 32) {
-      const int r = e % RPC, tok = e / RPC;
+    for (int e = threadIdx.x; e < RPC * TL * M; e += GV_WARPS * 32) {
+      const int r = e % (RPC * TL), tok = e / (RPC * TL);
       float sum = 0.0f;
 #pragma unroll
-      for (int w = 0; w < GV_WARPS; ++w) sum += red[w][r][tok];   // (TL == 1 here)
-      const int64_t row = int64_t(blockIdx.x) * RPC + r;
+      for (int w = 0; w < GV_WARPS; ++w) sum += red[w][r][tok];   // (RPC == 16 when TL == 2)
+      const int64_t row = int64_t(blockIdx.x) * RPC * TL + r;
       if (row < N) C[int64_t(tok) * ldc + row] = __float2bfloat16_rn(sum);
     }
   }
@@ -2043,15 +2044,19 @@ int gemm_bf16(const bf16* A, const bf16* W, bf16* C, int64_t M, int64_t N, int64
   if (p.splits > 1 && Kl % 32 == 0) {
     const int nt = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
     const bool small_k = K <= GV_WARPS * 32 * 4;            // every warp's weights fit 4 chunks
-    const bool half = epi != QW_EPI_SILU_MUL && N <= 2048;  // 8 rows per CTA: twice the CTAs
-    const unsigned blocks =
-        unsigned(epi == QW_EPI_SILU_MUL ? (N / 2 + 7) / 8 : half ? (N + 7) / 8 : (N + 15) / 16);
-    cudaError_t e;
     // up to 8 tokens: activations staged in shared memory (measured on the
     // 28-layer decode step, 128 steps: 139.3 -> 136.3 ms with per-thread
     // asynchronous copies, 134.2 -> 125.1 ms on moving to one bulk copy per row)
     const size_t stage_smem = size_t(M) * (K + GV_YPAD) * 2;
     const bool stage = M <= 8 && stage_smem <= size_t(200) * 1024;
+    // 8 rows per CTA (twice the CTAs) for narrow outputs, except on the staged
+    // path: every CTA there copies all the activation rows, and 16 rows per CTA
+    // halve that traffic (decode o_proj / down: 118.0 -> 116.0 ms per 128 steps
+    // together with the two-tile QKV GEMV)
+    const bool half = epi != QW_EPI_SILU_MUL && N <= 2048 && !(nt == 1 && stage);
+    const unsigned blocks =
+        unsigned(epi == QW_EPI_SILU_MUL ? (N / 2 + 7) / 8 : half ? (N + 7) / 8 : (N + 15) / 16);
+    cudaError_t e;
   // and the weight rows bulk-copied into shared memory beside them (WTMA)
 #define QW_GV_ONE(NTV, EPIV, WR, RPCV, MC)                                                                     \
   if (NTV == 1 && stage) {                                                                                     \
@@ -2147,8 +2152,11 @@ int norm_gemm_bf16(const bf16* x, const NormArgs& na, const bf16* W, bf16* C, in
   const bool half = epi != QW_EPI_SILU_MUL && N <= 2048;
   unsigned blocks = unsigned(epi == QW_EPI_SILU_MUL ? (N / 2 + 7) / 8 : half ? (N + 7) / 8 : (N + 15) / 16);
   // SiluAndMul with more 8-output CTAs than fit at once (two per SM): 16 outputs
-  // per CTA, so the norm prologue is not repeated by a second wave
-  const bool two_tiles = epi == QW_EPI_SILU_MUL && small_k && blocks > unsigned(2 * gv_device_sms());
+  // per CTA, so the norm prologue is not repeated by a second wave.  Plain
+  // outputs with more 16-row CTAs than SMs: 32 rows per CTA (decode QKV: with
+  // the 16-row staged GEMVs, 118.0 -> 116.0 ms per 128 steps)
+  const bool two_tiles = small_k && !half && (epi == QW_EPI_SILU_MUL || nt == 1) &&
+                         blocks > unsigned((epi == QW_EPI_SILU_MUL ? 2 : 1) * gv_device_sms());
   if (two_tiles) blocks = (blocks + 1) / 2;
   const int64_t ldc = epi == QW_EPI_SILU_MUL ? N / 2 : N;
   const int64_t i_l = epi == QW_EPI_SILU_MUL ? N / 2 / tp : 0;
@@ -2180,7 +2188,8 @@ int norm_gemm_bf16(const bf16* x, const NormArgs& na, const bf16* W, bf16* C, in
   } else if (half) {                                                                                             \
     QW_NG_ONE(NTV, tc::EPI_NONE, 8, 12, 1)                                                                       \
   } else if (small_k) {                                                                                          \
-    QW_NG_ONE(NTV, tc::EPI_NONE, 16, 4, 1)                                                                       \
+    if (two_tiles) QW_NG_ONE(NTV, tc::EPI_NONE, 16, 4, 2)                                                        \
+    else QW_NG_ONE(NTV, tc::EPI_NONE, 16, 4, 1)                                                                  \
   } else {                                                                                                       \
     QW_NG_ONE(NTV, tc::EPI_NONE, 16, 12, 1)                                                                      \
   }

@@ -224,6 +224,7 @@ GEMM_CASES = [
     (130, 1000 // 8 * 16, 1000, 1, 0, 0),   # K not a multiple of 64 (TMA zero fill)
     (1, 4096, 1024, 2, 0, 0),       # decode path (swapped operands, split K)
     (7, 1024, 2048, 2, 1, 0),
+    (8, 1024, 3072, 2, 1, 0),       # decode down: staged activations, 16 weight rows per CTA in shared memory
     (16, 6144, 1024, 2, 0, 1),
     (33, 1024, 3072, 2, 1, 0),
     (64, 4096, 1024, 1, 0, 0),
@@ -257,7 +258,9 @@ def test_gemm_bf16(L, M, N, K, tp, mode, epi):
                                                     # 311 groups of 8 outputs: two per CTA, the last CTA half empty
                                                     (3, 4976, 256, 1, 1, True),
                                                     # two tokens per warp, K = 3072 (the down projection's width)
-                                                    (16, 512, 3072, 1, 0, True)])
+                                                    (16, 512, 3072, 1, 0, True),
+                                                    # 32-row CTAs, the last one's second tile past N
+                                                    (8, 4880, 1024, 1, 0, True)])
 def test_add_rmsnorm_gemm(L, M, N, K, tp, epi, with_res):
     """Fused add + RMSNorm + column Linear (decode QKV / gate_up) against the
     oracle's add_rms_norm followed by the oracle Linear."""
