@@ -225,6 +225,8 @@ GEMM_CASES = [
     (1, 4096, 1024, 2, 0, 0),       # decode path (swapped operands, split K)
     (7, 1024, 2048, 2, 1, 0),
     (8, 1024, 3072, 2, 1, 0),       # decode down: staged activations, 16 weight rows per CTA in shared memory
+    (5, 6144, 1024, 2, 0, 1),       # SiluAndMul on the staged path: gate and up rows side by side in shared memory
+    (8, 2048, 1024, 1, 0, 0),       # column layout, narrow output, staged path
     (16, 6144, 1024, 2, 0, 1),
     (33, 1024, 3072, 2, 1, 0),
     (64, 4096, 1024, 1, 0, 0),
@@ -260,7 +262,9 @@ def test_gemm_bf16(L, M, N, K, tp, mode, epi):
                                                     # two tokens per warp, K = 3072 (the down projection's width)
                                                     (16, 512, 3072, 1, 0, True),
                                                     # 32-row CTAs, the last one's second tile past N
-                                                    (8, 4880, 1024, 1, 0, True)])
+                                                    (8, 4880, 1024, 1, 0, True),
+                                                    # 8 weight rows per CTA (narrow output), rows in shared memory
+                                                    (4, 1024, 2048, 2, 0, True)])
 def test_add_rmsnorm_gemm(L, M, N, K, tp, epi, with_res):
     """Fused add + RMSNorm + column Linear (decode QKV / gate_up) against the
     oracle's add_rms_norm followed by the oracle Linear."""
