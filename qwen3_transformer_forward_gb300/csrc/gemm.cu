@@ -15,9 +15,11 @@
 //   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator, convert,
 //               store (or fp32 split-K partials)
 // Prefill (many tokens): MMA-A = activations, MMA-B = weights, BN = 256.
-// Decode (<= 64 tokens): operands swapped (MMA-A = 128 weight rows,
+// Few tokens (<= 64): operands swapped (MMA-A = 128 weight rows,
 // MMA-B = the tokens padded to 16/32/64) and split along K so that enough
-// CTAs stream the weights.  The K-splits of one weight tile form a thread-
+// CTAs stream the weights -- when the planner finds one split enough (the
+// lm_head's 151936 rows) or K does not suit the warp-level GEMV; otherwise
+// the few-token GEMV below (gemv_mma_kernel) runs.  The K-splits of one weight tile form a thread-
 // block cluster (<= 8 CTAs): each leaves its fp32 partial tile in its own
 // shared memory and cluster rank 0 sums them in split order over distributed
 // shared memory, then applies the epilogue (bf16, or SiluAndMul with 64 gate
@@ -1362,11 +1364,12 @@ __global__ void __launch_bounds__(32) selftest_wait_kernel() {
 //
 // C[M, N] = A[M, K] W^T for M <= 64.  The weights are read once and dominate
 // the bytes, so the kernel is built for memory-level parallelism: a CTA owns
-// 16 weight rows (SiluAndMul: 8 gate rows and the matching 8 up rows) across
-// the whole K, split over its 8 warps; each warp issues all its weight loads
-// (16-byte, non-caching) up front into registers -- before the programmatic
-// dependency wait, since weights are constants -- then multiplies with
-// mma.sync m16n8k16.  Weights and tokens use the same permutation of the 32
+// 16 weight rows (SiluAndMul: 8 gate rows and the matching 8 up rows; 8 rows
+// for narrow outputs above 8 tokens) across the whole K, split over its 8
+// warps.  The weights are constants, so their transfer starts before the
+// programmatic dependency wait: up to 8 tokens (WTMA) as bulk copies of
+// whole rows into shared memory, otherwise as 16-byte non-caching loads into
+// registers issued up front by each warp.  The MMAs are mma.sync m16n8k16.  Weights and tokens use the same permutation of the 32
 // k values of a chunk (thread t holds k 8t..8t+7: logical k 2t,2t+1 | 2t+8,2t+9
 // of two k-steps), so no shuffles are needed.  The 8 warps' partial tiles are
 // added in shared memory in warp order (deterministic) and the epilogue
