@@ -385,8 +385,11 @@ int qw_selftest_wait_timeout(void* stream);
  *                       [r*K/tp, (r+1)*K/tp)); C[M, N] = sum_r A[:, shard r] W_r^T,
  *                       accumulated in fp32 across shards (the all_reduce), rounded once.
  *   workspace: unused (pass NULL, 0); qw_gemm_workspace_size returns 0.  With
- *   few tokens the K range is split over a thread-block cluster and the
- *   partial sums are added in shared memory, in a fixed order.
+ *   few tokens (<= 64) the K range is split either over the 8 warps of a CTA
+ *   that owns 16 weight rows (K/tp % 32 == 0; up to 8 tokens the rows are
+ *   bulk-copied into shared memory ahead of the programmatic wait) or over a
+ *   thread-block cluster; the partial sums are added in shared memory, in a
+ *   fixed order.
  * Rules (bf16): K % 8 == 0, K/tp % 8 == 0 (row), N % 16 == 0 (N/2/tp % 8 == 0 for
  * SILU_MUL), A/W/C 16-byte aligned.  f32 runs on CUDA cores (exact fp32 FMA).
  */
